@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark of the few-row packed-weight verify matmul on GB300.
+
+One step = one verify pass of M drafted rows through a stack of distinct
+packed weight matrices of the workload (a model-like stack, so consecutive
+calls never find their weights in L2: the stack is larger than 4x L2), run
+back to back on one stream through the C ABI.  Metric: packed-weight GB/s
+(algorithmic bytes: packed weights + X + Y per call) and us per call, at
+M = 1..8 rows, as a fraction of the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl lbv|reference]
+
+N > 1 (under torchrun): independent replicas, one per GPU; no data-path
+collective (the verify path shards by output columns, and each replica here
+owns its own stack).  value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "us/call and packed-weight GB/s at M=1..8 rows, as % of GB300 HBM peak"
+DEFAULT_WORKLOAD = "sign1_mlp_up_5120x17408"
+FMT_IDS = {synth.SIGN1_G128: 0, synth.AFFINE2: 1, synth.Q4_0: 2}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="lbv", choices=["lbv", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--M", type=int, default=8)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the M=1..8 table")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--json-out", default="")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def call_bytes(mat, M):
+    import few_row_packed_gb300 as lbv
+    fmt = FMT_IDS[mat.fmt]
+    return lbv.packed_bytes(fmt, mat.K, mat.N, mat.group) + M * mat.K * 2 + M * mat.N * 4
+
+
+# ---------------------------------------------------------------------------
+# clocks during the measurement
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the lbv arm
+
+class Stack:
+    """Distinct packed matrices of a workload resident on the device."""
+
+    def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int):
+        import torch
+
+        import few_row_packed_gb300 as lbv
+        wl = synth.WORKLOADS[workload]
+        self.mats = list(wl.matrices)
+        flags = lbv.PLAN_PDL if pdl else 0
+        self.layers = []
+        if len(self.mats) == 1:
+            mat = self.mats[0]
+            per = lbv.packed_bytes(FMT_IDS[mat.fmt], mat.K, mat.N, mat.group)
+            L = max(64 if per < 100e6 else 3, math.ceil(4 * l2_bytes / per))
+            ndistinct = min(L, 4)
+            gens = [synth.gen_matrix(mat, [wl.seed, i]) for i in range(ndistinct)]
+            mats = [mat] * L
+            gen_of = [gens[i % ndistinct] for i in range(L)]
+        else:
+            mats = self.mats
+            gen_of = [synth.gen_matrix(m, synth.matrix_seed(wl, i)) for i, m in enumerate(mats)]
+        plans = {}
+        packed_cache = {}
+        for i, (mat, (parts, xb)) in enumerate(zip(mats, gen_of)):
+            key = (mat.fmt, mat.K, mat.N, mat.group, mat.xdtype)
+            if key not in plans:
+                plans[key] = lbv.Plan(FMT_IDS[mat.fmt], mat.K, mat.N, mat.group,
+                                      lbv.DTYPE_BY_NAME[mat.xdtype], flags)
+                if shape:
+                    plans[key].set_shape(*[int(v) for v in shape.split(",")])
+            pid = id(parts[0])
+            if pid not in packed_cache:
+                packed_cache[pid] = lbv.pack(FMT_IDS[mat.fmt], parts, mat.K, mat.N, mat.group)
+            Wp = torch.from_numpy(packed_cache[pid]).cuda()       # a distinct allocation
+            X = torch.from_numpy(xb.view(np.int16)).cuda()
+            Xr = torch.zeros_like(X) if mat.rotate else None
+            Y = torch.zeros((8, mat.N), dtype=torch.float32, device="cuda")
+            self.layers.append((mat, plans[key], Wp, X, Xr, Y))
+        self.plans = plans
+        self.bytes_per_step = {m: sum(call_bytes(l[0], m) for l in self.layers) for m in range(1, 9)}
+        self.calls = len(self.layers)
+        self.launches_per_step = sum(2 if l[0].rotate else 1 for l in self.layers)
+
+    def step(self, M, verify_only=False):
+        import few_row_packed_gb300 as lbv
+        for mat, plan, Wp, X, Xr, Y in self.layers:
+            if mat.rotate and not verify_only:
+                lbv.fwht128(X, Xr, M, mat.K, lbv.DTYPE_BY_NAME[mat.xdtype])
+                lbv.verify_gemm(plan, Xr, M, Wp, Y)
+            else:
+                lbv.verify_gemm(plan, X, M, Wp, Y)
+
+
+def timed(torch, fn, steps, warmup, barrier):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1)
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "few_row_packed_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, M):
+    """DRAM bytes per verify launch from the committed ncu capture, if it was
+    taken on the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[workload]
+        if e.get("kernel_hash") == kernel_hash() and int(e.get("M", -1)) == M:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(workload, M, budget_s=10.0):
+    """The fp64 oracle as it stands, single-threaded on the host: verify calls
+    on full matrices of the workload until about budget_s has passed."""
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS[workload]
+    done_bytes, t_total, calls, cols_done = 0, 0.0, 0, 0
+    i = 0
+    while t_total < budget_s and i < 64:
+        mat = wl.matrices[i % len(wl.matrices)]
+        parts, xb = synth.gen_matrix(mat, synth.matrix_seed(wl, i % len(wl.matrices)))
+        Xf = oracle.x_to_f64(xb[:M], mat.xdtype)
+        if mat.rotate:
+            Xf = oracle.x_to_f64(oracle.round_x(oracle.fwht128(Xf), mat.xdtype), mat.xdtype)
+        # columns: whole matrix if it fits in the remaining budget, else a sample
+        ncols = mat.N if mat.N <= 20000 else 16384
+        cols = np.arange(ncols)
+        t0 = time.perf_counter()
+        oracle.verify(FMT_IDS[mat.fmt], parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+        dt = time.perf_counter() - t0
+        frac = ncols / mat.N
+        done_bytes += call_bytes(mat, M) * frac
+        t_total += dt
+        cols_done += ncols
+        calls += 1
+        i += 1
+    gbs = done_bytes / t_total / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "us_per_call": t_total / (done_bytes / call_bytes(wl.matrices[0], M)) * 1e6,
+            "sample": f"{calls} oracle verify call(s), {cols_done} output columns x {M} rows "
+                      f"of {workload}, {t_total:.1f} s single-threaded; GB/s of the sample's "
+                      "algorithmic bytes"}
+
+
+def run_lbv(args, rank, world, barrier, reduce_max):
+    import torch
+
+    import few_row_packed_gb300 as lbv
+    lbv.build()
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M)
+    peak, peak_kind = peaks()
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
+
+    # sustained warm-up with clock sampling, then the timed region
+    sampler = ClockSampler(int(phys) if phys.isdigit() else dev)
+    sampler.start()
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        for _ in range(max(1, args.warmup)):
+            stack.step(args.M)
+        torch.cuda.synchronize()
+    ms = timed(torch, lambda: stack.step(args.M), args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+    ms = reduce_max(ms)
+    ms_per_step = ms / args.steps
+    bytes_step = stack.bytes_per_step[args.M]
+    value = bytes_step * world / (ms_per_step * 1e-3) / 1e9
+
+    # dominant kernel: the verify launch, timed alone (verify-only loop)
+    if any(l[0].rotate for l in stack.layers):
+        ms_v = reduce_max(timed(torch, lambda: stack.step(args.M, verify_only=True), args.steps,
+                                args.warmup, barrier))
+    else:
+        ms_v = ms
+    us_launch = ms_v * 1e3 / (args.steps * stack.calls)
+    bytes_launch = bytes_step / stack.calls
+    achieved = bytes_launch / (us_launch * 1e-6) / 1e9
+    traffic = recorded_traffic(args.workload, args.M)
+
+    per_M = {}
+    if not args.no_sweep:
+        for M in range(1, 9):
+            msm = reduce_max(timed(torch, lambda: stack.step(M), max(10, args.steps // 4),
+                                   args.warmup, barrier))
+            us = msm * 1e3 / (max(10, args.steps // 4) * stack.calls)
+            gbs = stack.bytes_per_step[M] / stack.calls / (us * 1e-6) / 1e9
+            per_M[str(M)] = {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
+                             "frac_of_measured_hbm": round(gbs / peak, 4)}
+
+    # end to end through the public API with host buffers: per step, X from
+    # pinned host memory to the device, the verify stack, the last Y back
+    mat0 = stack.layers[0][0]
+    x_host = torch.from_numpy(stack.layers[0][3].cpu().numpy()).pin_memory()
+    y_host = torch.zeros((args.M, stack.layers[-1][0].N), dtype=torch.float32).pin_memory()
+    X_dev = stack.layers[0][3]
+    Y_last = stack.layers[-1][5]
+
+    def e2e_step():
+        X_dev[:args.M].copy_(x_host[:args.M], non_blocking=True)
+        stack.step(args.M)
+        y_host.copy_(Y_last[:args.M], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    t_e2e = reduce_max((time.perf_counter() - t0) * 1e3)
+    e2e_val = bytes_step * world / (t_e2e / args.steps * 1e-3) / 1e9
+
+    shape = next(iter(stack.plans.values())).shape()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16" if mat0.xdtype == "f16" else "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "M": args.M,
+            "calls_per_step": stack.calls,
+            "us_per_call": round(ms_per_step * 1e3 / stack.calls, 3),
+            "l2": f"inputs larger than L2: {stack.calls} distinct resident matrices, "
+                  f"{bytes_step / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
+            "launch": ("programmatic dependent launch, " if not args.no_pdl else "") +
+                      "back to back on one stream",
+            "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
+                      "ctas_n": shape[3]},
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "per_M": per_M,
+        "m8_over_m1": (round(per_M["8"]["us_per_call"] / per_M["1"]["us_per_call"], 3)
+                       if per_M else None),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind, "kernel": "lbv_verify_kernel",
+                     "bytes_per_launch": bytes_launch, "us_per_launch": round(us_launch, 3)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": args.M * mat0.K * 2,
+                "d2h_bytes_per_step": args.M * stack.layers[-1][0].N * 4},
+        "gpu_launches": args.steps * stack.launches_per_step,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.M)
+    return line
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands on the host cores; each
+    step is a bounded sample (a slice of output columns) of the workload."""
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS[args.workload]
+    mat = wl.matrices[0]
+    parts, xb = synth.gen_matrix(mat, synth.matrix_seed(wl, 0))
+    M = args.M
+    Xf = oracle.x_to_f64(xb[:M], mat.xdtype)
+    if mat.rotate:
+        Xf = oracle.x_to_f64(oracle.round_x(oracle.fwht128(Xf), mat.xdtype), mat.xdtype)
+    ncols = min(mat.N, 256)
+    cols = np.arange(ncols)
+    fmt = FMT_IDS[mat.fmt]
+    for _ in range(max(0, args.warmup)):
+        oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+    dt = time.perf_counter() - t0
+    sample_bytes = call_bytes(mat, M) * ncols / mat.N
+    gbs = sample_bytes * args.steps / dt / 1e9
+    sample = (f"{ncols} of {mat.N} output columns x {M} rows of {args.workload} per step, "
+              "fp64 oracle, single-threaded")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "sample_columns": ncols},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            line = run_reference(args)
+            print(json.dumps(line))
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    barrier = lambda: None  # noqa: E731
+    reduce_max = lambda v: v  # noqa: E731
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+        def barrier():
+            dist.barrier()
+
+        def reduce_max(v):
+            t = torch.tensor([v], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+
+    line = run_lbv(args, rank, world, barrier, reduce_max)
+    if rank == 0:
+        print(json.dumps(line))
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                json.dump(line, f, indent=1)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

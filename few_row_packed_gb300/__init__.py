@@ -1,0 +1,250 @@
+"""few_row_packed_gb300 -- Python binding of liblbv, the few-row low-bit
+verify matmul for GB300 (sm_103a).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of liblbv.so, called through its C ABI (include/lbv.h).  PyTorch is
+used only for device memory and streams.  There is no fallback: if the
+library is not built, ``lib()`` raises.
+
+    Y[M,N] = X[M,K] . dequant(Wp)[K,N],   1 <= M <= 8
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+FMT_SIGN1_G128 = 0
+FMT_AFFINE2 = 1
+FMT_Q4_0 = 2
+F16 = 0
+BF16 = 1
+PLAN_MEASURE = 0x1
+PLAN_FORCE_FEWROW = 0x2
+PLAN_FORCE_GEMV = 0x4
+PLAN_PDL = 0x8
+KERNEL_FEWROW = 1
+KERNEL_GEMV = 2
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblbv.so")
+_lib = None
+
+FMT_BY_NAME = {"sign1_g128": FMT_SIGN1_G128, "affine2": FMT_AFFINE2, "q4_0": FMT_Q4_0}
+DTYPE_BY_NAME = {"f16": F16, "bf16": BF16}
+
+
+class LbvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"lbv status {status}: {msg}")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile liblbv.so in-tree for sm_103a (nvcc); returns its path."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib():
+    """The loaded liblbv.so.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "few_row_packed_gb300.build() (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, U, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+        st = ctypes.c_int
+        sig = {
+            "lbv_packed_bytes": (S, [I, I, I, I]),
+            "lbv_pack_sign_g128": (st, [P, P, I, I, P, S]),
+            "lbv_pack_affine2": (st, [P, P, P, I, I, I, P, S]),
+            "lbv_pack_q4_0": (st, [P, I, I, P, S]),
+            "lbv_plan_create": (st, [I, I, I, I, I, U, ctypes.POINTER(P)]),
+            "lbv_plan_destroy": (st, [P]),
+            "lbv_plan_query": (st, [P, I, ctypes.POINTER(I), ctypes.POINTER(I),
+                                    ctypes.POINTER(S)]),
+            "lbv_plan_shape": (st, [P] + [ctypes.POINTER(I)] * 4),
+            "lbv_plan_set_shape": (st, [P, I, I, I, I]),
+            "lbv_plan_measured": (st, [P, I, ctypes.POINTER(ctypes.c_float),
+                                       ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
+            "lbv_verify_gemm": (st, [P, P, I, I, P, P, I, P, S, P]),
+            "lbv_fwht128": (st, [P, P, I, I, I, P, P]),
+            "lbv_dequant_fp16": (st, [P, P, P, P]),
+            "lbv_last_error": (ctypes.c_char_p, []),
+            "lbv_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().lbv_last_error().decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise LbvError(status, last_error())
+
+
+def _ptr(t):
+    """Device or host address of a torch tensor / numpy array / int / None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# --- packing (host) -------------------------------------------------------------
+
+def packed_bytes(fmt: int, K: int, N: int, group: int = 128) -> int:
+    return int(lib().lbv_packed_bytes(fmt, K, N, group))
+
+
+def _out(fmt, K, N, group):
+    n = packed_bytes(fmt, K, N, group)
+    if n == 0:
+        raise LbvError(ERR_INVALID_ARG, f"invalid shape K={K} N={N} group={group}")
+    return np.zeros(n, np.uint8)
+
+
+def pack_sign_g128(bits, scales, K: int, N: int) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, np.uint32)
+    scales = np.ascontiguousarray(scales, np.uint16)
+    if bits.size != N * (K // 32) or scales.size != N * (K // 128):
+        raise LbvError(ERR_INVALID_ARG, "bits/scales size mismatch")
+    out = _out(FMT_SIGN1_G128, K, N, 128)
+    _check(lib().lbv_pack_sign_g128(_ptr(bits), _ptr(scales), K, N, _ptr(out), out.size))
+    return out
+
+
+def pack_affine2(codes, scales, biases, K: int, N: int, group: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint32)
+    scales = np.ascontiguousarray(scales, np.uint16)
+    biases = np.ascontiguousarray(biases, np.uint16)
+    if codes.size != N * (K // 16) or scales.size != N * (K // group) or biases.size != scales.size:
+        raise LbvError(ERR_INVALID_ARG, "codes/scales/biases size mismatch")
+    out = _out(FMT_AFFINE2, K, N, group)
+    _check(lib().lbv_pack_affine2(_ptr(codes), _ptr(scales), _ptr(biases), K, N, group,
+                                  _ptr(out), out.size))
+    return out
+
+
+def pack_q4_0(blocks, K: int, N: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    if blocks.size != N * (K // 32) * 18:
+        raise LbvError(ERR_INVALID_ARG, "blocks size mismatch")
+    out = _out(FMT_Q4_0, K, N, 32)
+    _check(lib().lbv_pack_q4_0(_ptr(blocks), K, N, _ptr(out), out.size))
+    return out
+
+
+def pack(fmt: int, parts, K: int, N: int, group: int = 128) -> np.ndarray:
+    """Canonical arrays (as produced for the format) -> device-layout bytes."""
+    if fmt == FMT_SIGN1_G128:
+        return pack_sign_g128(parts[0], parts[1], K, N)
+    if fmt == FMT_AFFINE2:
+        return pack_affine2(parts[0], parts[1], parts[2], K, N, group)
+    return pack_q4_0(parts[0], K, N)
+
+
+# --- plans -----------------------------------------------------------------------
+
+class Plan:
+    """A verify plan for one (format, K, N, group, activation dtype)."""
+
+    def __init__(self, fmt: int, K: int, N: int, group: int = 128, xdtype: int = F16,
+                 flags: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().lbv_plan_create(fmt, K, N, group, xdtype, flags, ctypes.byref(h)))
+        self.handle = h
+        self.fmt, self.K, self.N, self.group, self.xdtype, self.flags = fmt, K, N, group, xdtype, flags
+
+    def close(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.lbv_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def packed_bytes(self) -> int:
+        return packed_bytes(self.fmt, self.K, self.N, self.group)
+
+    def query(self, M: int):
+        k, s, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+        _check(lib().lbv_plan_query(self.handle, M, ctypes.byref(k), ctypes.byref(s),
+                                    ctypes.byref(w)))
+        return k.value, s.value, w.value
+
+    def shape(self):
+        v = [ctypes.c_int() for _ in range(4)]
+        _check(lib().lbv_plan_shape(self.handle, *[ctypes.byref(x) for x in v]))
+        return tuple(x.value for x in v)
+
+    def set_shape(self, warps: int, tiles_per_warp: int, splits: int, ctas_n: int = 0):
+        _check(lib().lbv_plan_set_shape(self.handle, warps, tiles_per_warp, splits, ctas_n))
+
+    def measured(self, M: int):
+        f, g, c = ctypes.c_float(), ctypes.c_float(), ctypes.c_int()
+        _check(lib().lbv_plan_measured(self.handle, M, ctypes.byref(f), ctypes.byref(g),
+                                       ctypes.byref(c)))
+        return f.value, g.value, c.value
+
+
+# --- device calls ------------------------------------------------------------------
+
+def verify_gemm(plan: Plan, X, M: int, Wp, Y, ldx: int | None = None, ldy: int | None = None,
+                stream=None):
+    """Y[:M, :N] = X[:M, :K] . W (device tensors; X fp16/bf16 bits, Y fp32)."""
+    ldx = plan.K if ldx is None else ldx
+    ldy = plan.N if ldy is None else ldy
+    _check(lib().lbv_verify_gemm(plan.handle, _ptr(X), M, ldx, _ptr(Wp), _ptr(Y), ldy, None, 0,
+                                 _stream(stream)))
+
+
+def verify_gemm_host(plan: Plan, x_host, M: int, Wp, y_host, x_dev, y_dev, stream=None):
+    """End-to-end call with host buffers: copies X (pinned host) to the device,
+    runs the verify, copies Y back and waits.  x_dev / y_dev are caller-owned
+    device staging tensors; Wp stays resident on the device."""
+    x_dev[:M].copy_(x_host[:M], non_blocking=True)
+    verify_gemm(plan, x_dev, M, Wp, y_dev, stream=stream)
+    y_host[:M].copy_(y_dev[:M], non_blocking=True)
+
+
+def fwht128(X, Xr, M: int, K: int, dtype: int = F16, signs=None, stream=None):
+    """Blockwise normalized Walsh-Hadamard rotation of M rows of length K."""
+    _check(lib().lbv_fwht128(_ptr(X), _ptr(Xr), M, K, dtype, _ptr(signs), _stream(stream)))
+
+
+def dequant_fp16(plan: Plan, Wp, W, stream=None):
+    """Test export: dense fp16 W[K][N] (device) from the packed device layout."""
+    _check(lib().lbv_dequant_fp16(plan.handle, _ptr(Wp), _ptr(W), _stream(stream)))
+
+
+def version() -> str:
+    return lib().lbv_version().decode()

@@ -1,0 +1,708 @@
+// api.cpp -- the C ABI of include/lbv.h: argument checks, host packers, plan
+// selection and dispatch.  Every error is returned as an lbv_status with a
+// thread-local message; nothing here aborts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "lbv_internal.h"
+#include "verify_ops.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+lbv_status fail(lbv_status st, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+lbv_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(LBV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+const lbv::VerifyOps* ops_for(lbv_format fmt, int group)
+{
+    switch (fmt) {
+    case LBV_FMT_SIGN1_G128:
+        return &lbv::sign1_ops;
+    case LBV_FMT_AFFINE2:
+        return group == 32 ? &lbv::affine2_g32_ops
+               : group == 64 ? &lbv::affine2_g64_ops
+                             : &lbv::affine2_g128_ops;
+    case LBV_FMT_Q4_0:
+        return &lbv::q4_0_ops;
+    }
+    return nullptr;
+}
+
+bool valid_fmt(int fmt)
+{
+    return fmt == LBV_FMT_SIGN1_G128 || fmt == LBV_FMT_AFFINE2 || fmt == LBV_FMT_Q4_0;
+}
+
+// The K granularity the canonical layout of each format can represent.
+int k_quantum(lbv_format fmt, int group)
+{
+    switch (fmt) {
+    case LBV_FMT_SIGN1_G128:
+        return 128;
+    case LBV_FMT_AFFINE2:
+        return group;          // also a multiple of 16 (codes per word)
+    case LBV_FMT_Q4_0:
+        return 32;
+    }
+    return 0;
+}
+
+// Shape bookkeeping: clamp the split so every slice has >= 1 chunk.
+void finish_shape(lbv::Shape& sh, int64_t nchunks)
+{
+    int cps = (int)((nchunks + sh.splits - 1) / sh.splits);
+    sh.splits = (int)((nchunks + cps - 1) / cps);
+}
+
+int shape_cps(const lbv::Shape& sh, int64_t nchunks)
+{
+    return (int)((nchunks + sh.splits - 1) / sh.splits);
+}
+
+constexpr size_t kSmemCap = 200 * 1024;        // per CTA, of 227 KB
+constexpr size_t kSmemTwoCta = 100 * 1024;     // keep 2 CTAs per SM when possible
+
+// Fills sh.smem and sh.ctas_n for a (warps, tpw, splits) choice.  Returns
+// false if it does not fit.
+bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_n_req)
+{
+    const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
+    finish_shape(sh, P->layout.nchunks);
+    const int cps = shape_cps(sh, P->layout.nchunks);
+    sh.smem = ops->smem(sh.warps, sh.tpw, cps);
+    if (sh.smem > kSmemCap)
+        return false;
+    const int64_t nunits = (P->layout.ntiles + sh.tpw - 1) / sh.tpw;
+    const int64_t nblocks = (nunits + sh.warps - 1) / sh.warps;
+    if (sh.splits > 1) {
+        sh.ctas_n = (int)nblocks;              // one column block per cluster
+    } else {
+        sh.ctas_n = 0;
+        if (ops->prepare(P->xdtype, sh) != cudaSuccess)
+            return false;
+        int occ = ops->occupancy(P->xdtype, sh);
+        if (occ < 1)
+            return false;
+        int64_t cap = (int64_t)P->sms * occ;
+        if (ctas_n_req > 0)
+            cap = std::min<int64_t>(cap, ctas_n_req);
+        sh.ctas_n = (int)std::max<int64_t>(1, std::min<int64_t>(nblocks, cap));
+    }
+    return ops->prepare(P->xdtype, sh) == cudaSuccess;
+}
+
+// Default launch shape: 8 warps, 1 tile per warp; the smallest K split that
+// gives about two CTAs per SM and keeps the staged slice small.
+lbv::Shape default_shape(const lbv_plan* P)
+{
+    const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
+    const int64_t nblocks = (P->layout.ntiles + 7) / 8;
+    const int64_t target = 2 * (int64_t)P->sms;
+    lbv::Shape best = {8, 1, 8, 0, 0};
+    for (int s = 1; s <= 8; ++s) {
+        lbv::Shape sh = {8, 1, s, 0, 0};
+        finish_shape(sh, P->layout.nchunks);
+        if (sh.splits != s && s > 1)
+            continue;
+        const int cps = shape_cps(sh, P->layout.nchunks);
+        if (ops->smem(8, 1, cps) > kSmemTwoCta)
+            continue;
+        best = sh;
+        if (nblocks * s >= target)
+            break;
+    }
+    return best;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lbv_last_error(void)
+{
+    return g_err.c_str();
+}
+
+const char* lbv_version(void)
+{
+    return "lbv 0.1.0 (sm_103a)";
+}
+
+size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group)
+{
+    lbv::FmtInfo fi;
+    if (!valid_fmt(fmt) || K <= 0 || N <= 0)
+        return 0;
+    if (fmt != LBV_FMT_AFFINE2)
+        group = fmt == LBV_FMT_SIGN1_G128 ? 128 : 32;
+    if (!lbv::fmt_info(fmt, group, &fi))
+        return 0;
+    if (K % k_quantum(fmt, group) != 0 || (fmt == LBV_FMT_AFFINE2 && K % 16 != 0))
+        return 0;
+    return lbv::make_layout(fi, K, N).total;
+}
+
+// --------------------------------------------------------------------------
+// Host packers.  Each walks the device layout (layout.h) and fetches the
+// code of weight (k, n) from the canonical arrays.
+
+lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int K, int N,
+                              void* out, size_t out_bytes)
+{
+    g_err.clear();
+    if (!bits || !scales || !out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_sign_g128: null pointer");
+    const size_t need = lbv_packed_bytes(LBV_FMT_SIGN1_G128, K, N, 128);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_sign_g128: K=%d N=%d (need K%%128==0, N>0)", K, N);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_sign_g128: out_bytes %zu < %zu", out_bytes, need);
+    lbv::FmtInfo fi;
+    lbv::fmt_info(LBV_FMT_SIGN1_G128, 128, &fi);
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint32_t* codes = static_cast<uint32_t*>(out);
+    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    const int wk = K / 32, sk = K / 128;
+    auto bit = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        return (bits[(size_t)n * wk + k / 32] >> (k % 32)) & 1u;
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 16; ++s) {
+                        const int kt = (wi >> 1) * 8 + (s >> 1);
+                        const int k0 = (int)ch * 256 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= bit(n, k0) << s;
+                        w |= bit(n, k0 + 1) << (16 + s);
+                    }
+                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 2; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int grp = (int)ch * 2 + j;
+                        const bool ok = n < N && grp < sk;
+                        side[(tc * 8 + g) * 4 + 2 * j + hi] = ok ? scales[(size_t)n * sk + grp] : 0;
+                    }
+        }
+    return LBV_OK;
+}
+
+lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
+                            const uint16_t* biases, int K, int N, int group, void* out,
+                            size_t out_bytes)
+{
+    g_err.clear();
+    if (!codes_in || !scales || !biases || !out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_affine2: null pointer");
+    if (group != 32 && group != 64 && group != 128)
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_pack_affine2: group %d (supported: 32, 64, 128)", group);
+    const size_t need = lbv_packed_bytes(LBV_FMT_AFFINE2, K, N, group);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_affine2: K=%d N=%d group=%d (need K%%group==0)", K, N, group);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_affine2: out_bytes %zu < %zu", out_bytes, need);
+    lbv::FmtInfo fi;
+    lbv::fmt_info(LBV_FMT_AFFINE2, group, &fi);
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint32_t* codes = static_cast<uint32_t*>(out);
+    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    const int wk = K / 16, gk = K / group, gpc = 128 / group;
+    auto code = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        return (codes_in[(size_t)n * wk + k / 16] >> (2 * (k % 16))) & 3u;
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 8; ++s) {
+                        const int kt = (wi >> 1) * 4 + (s >> 1);
+                        const int k0 = (int)ch * 128 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= code(n, k0) << (2 * s);
+                        w |= code(n, k0 + 1) << (16 + 2 * s);
+                    }
+                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < gpc; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int grp = (int)ch * gpc + j;
+                        const bool ok = n < N && grp < gk;
+                        uint16_t* e = side + (tc * 8 + g) * (4 * gpc) + 4 * j;
+                        e[hi] = ok ? scales[(size_t)n * gk + grp] : 0;
+                        e[2 + hi] = ok ? biases[(size_t)n * gk + grp] : 0;
+                    }
+        }
+    return LBV_OK;
+}
+
+lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t out_bytes)
+{
+    g_err.clear();
+    if (!blocks || !out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_q4_0: null pointer");
+    const size_t need = lbv_packed_bytes(LBV_FMT_Q4_0, K, N, 32);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_q4_0: K=%d N=%d (need K%%32==0)", K, N);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_q4_0: out_bytes %zu < %zu", out_bytes, need);
+    lbv::FmtInfo fi;
+    lbv::fmt_info(LBV_FMT_Q4_0, 32, &fi);
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint32_t* codes = static_cast<uint32_t*>(out);
+    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    const int nb = K / 32;
+    auto nib = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        const uint8_t* blk = blocks + ((size_t)n * nb + k / 32) * 18;
+        const int j = k % 32;
+        return j < 16 ? (blk[2 + j] & 15u) : (uint32_t)(blk[2 + j - 16] >> 4);
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 4; ++s) {
+                        const int kt = (wi >> 1) * 2 + (s >> 1);
+                        const int k0 = (int)ch * 64 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= nib(n, k0) << (4 * s);
+                        w |= nib(n, k0 + 1) << (16 + 4 * s);
+                    }
+                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 2; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int b = (int)ch * 2 + j;
+                        uint16_t d = 0;
+                        if (n < N && b < nb) {
+                            const uint8_t* blk = blocks + ((size_t)n * nb + b) * 18;
+                            d = (uint16_t)(blk[0] | (blk[1] << 8));
+                        }
+                        side[(tc * 8 + g) * 4 + 2 * j + hi] = d;
+                    }
+        }
+    return LBV_OK;
+}
+
+// --------------------------------------------------------------------------
+// Plans
+
+lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xdtype,
+                           unsigned flags, lbv_plan** out)
+{
+    g_err.clear();
+    if (!out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: out is NULL");
+    *out = nullptr;
+    if (!valid_fmt(fmt))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: unknown format %d", (int)fmt);
+    if (xdtype != LBV_F16 && xdtype != LBV_BF16)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: unknown dtype %d", (int)xdtype);
+    if (fmt == LBV_FMT_AFFINE2 && group != 32 && group != 64 && group != 128)
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: affine group %d (supported: 32, 64, 128)", group);
+    if (fmt != LBV_FMT_AFFINE2)
+        group = fmt == LBV_FMT_SIGN1_G128 ? 128 : 32;
+    if (K <= 0 || N <= 0 || K % k_quantum(fmt, group) != 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: K=%d N=%d not valid for the format", K, N);
+    if ((flags & LBV_PLAN_FORCE_FEWROW) && (flags & LBV_PLAN_FORCE_GEMV))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: both FORCE flags set");
+
+    lbv_plan* P = new (std::nothrow) lbv_plan();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: out of host memory");
+    P->fmt = fmt;
+    P->xdtype = xdtype;
+    P->K = K;
+    P->N = N;
+    P->group = group;
+    P->flags = flags;
+    lbv::fmt_info(fmt, group, &P->fi);
+    P->layout = lbv::make_layout(P->fi, K, N);
+    cudaError_t e = cudaGetDevice(&P->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device);
+    if (e != cudaSuccess) {
+        delete P;
+        return cuda_fail(e, "lbv_plan_create: device query");
+    }
+    lbv::Shape sh = default_shape(P);
+    if (!complete_shape(P, sh, 0)) {
+        delete P;
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: no launch shape fits K=%d", K);
+    }
+    P->shape = sh;
+    for (int m = 0; m <= 8; ++m)
+        P->use_gemv[m] = (flags & LBV_PLAN_FORCE_GEMV) ? 1 : 0;
+    P->crossover = (flags & LBV_PLAN_FORCE_GEMV) ? 9 : 1;
+    memset(P->measured_us, 0, sizeof P->measured_us);
+    if (flags & LBV_PLAN_MEASURE) {
+        extern lbv_status lbv_plan_measure_internal(lbv_plan * P);
+        lbv_status st = lbv_plan_measure_internal(P);
+        if (st != LBV_OK) {
+            delete P;
+            return st;
+        }
+    }
+    *out = P;
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_destroy(lbv_plan* plan)
+{
+    delete plan;
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_query(const lbv_plan* P, int M, int* kernel_id, int* splits,
+                          size_t* workspace_bytes)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_query: plan is NULL");
+    if (M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_query: M=%d outside 1..8", M);
+    if (kernel_id)
+        *kernel_id = P->use_gemv[M] ? LBV_KERNEL_GEMV : LBV_KERNEL_FEWROW;
+    if (splits)
+        *splits = P->use_gemv[M] ? 1 : P->shape.splits;
+    if (workspace_bytes)
+        *workspace_bytes = 0;
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_shape(const lbv_plan* P, int* warps, int* tpw, int* splits, int* ctas_n)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_shape: plan is NULL");
+    if (warps) *warps = P->shape.warps;
+    if (tpw) *tpw = P->shape.tpw;
+    if (splits) *splits = P->shape.splits;
+    if (ctas_n) *ctas_n = P->shape.ctas_n;
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int ctas_n)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: plan is NULL");
+    if ((warps != 4 && warps != 8) || (tpw != 1 && tpw != 2) || splits < 1 || splits > 8 ||
+        ctas_n < 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: warps=%d tpw=%d splits=%d ctas_n=%d",
+                    warps, tpw, splits, ctas_n);
+    lbv::Shape sh = {warps, tpw, splits, 0, 0};
+    if (!complete_shape(P, sh, ctas_n))
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_set_shape: shape does not fit (smem or occupancy)");
+    P->shape = sh;
+    return LBV_OK;
+}
+
+// --------------------------------------------------------------------------
+// Verify
+
+static lbv_status check_verify_args(const lbv_plan* P, const void* X, int M, int ldx,
+                                    const void* Wp, const float* Y, int ldy,
+                                    const void* workspace, size_t workspace_bytes)
+{
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: plan is NULL");
+    if (M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: M=%d outside 1..8", M);
+    if (!X || !Wp || !Y)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: null X, Wp or Y");
+    if (ldx < P->K || ldy < P->N)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: ldx=%d < K=%d or ldy=%d < N=%d", ldx,
+                    P->K, ldy, P->N);
+    if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: Wp not 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(X) & 1u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 3u) != 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: X or Y misaligned for its element type");
+    if (workspace_bytes != 0 && !workspace)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: workspace_bytes without workspace");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: current device %d is not the plan's %d",
+                    dev, P->device);
+    return LBV_OK;
+}
+
+static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, int ldx,
+                                     const void* Wp, float* Y, int ldy)
+{
+    lbv::VerifyParams p;
+    p.X = X;
+    p.codes = static_cast<const uint4*>(Wp);
+    p.side = static_cast<const uint8_t*>(Wp) + P->layout.side_offset;
+    p.Y = Y;
+    p.ldx = ldx;
+    p.ldy = ldy;
+    p.M = M;
+    p.K = P->K;
+    p.N = P->N;
+    p.ntiles = (int)P->layout.ntiles;
+    p.nchunks = (int)P->layout.nchunks;
+    p.splits = P->shape.splits;
+    p.cps = shape_cps(P->shape, P->layout.nchunks);
+    p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
+    return p;
+}
+
+// Internal: launch a given path (used by the plan measurement as well).
+lbv_status lbv_verify_launch_internal(const lbv_plan* P, const void* X, int M, int ldx,
+                                      const void* Wp, float* Y, int ldy, bool gemv,
+                                      cudaStream_t st)
+{
+    const lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, ldy);
+    cudaError_t e;
+    if (gemv) {
+        e = cudaSuccess;
+        for (int r = 0; r < M && e == cudaSuccess; ++r)
+            e = lbv::launch_gemv(P->fmt, P->xdtype, P->group, p, r, st);
+    } else {
+        lbv::LaunchOpts o;
+        o.pdl = (P->flags & LBV_PLAN_PDL) != 0;
+        e = ops_for(P->fmt, P->group)->launch(P->xdtype, P->shape, p, o, st);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_verify_gemm: launch");
+    return LBV_OK;
+}
+
+lbv_status lbv_verify_gemm(const lbv_plan* P, const void* X, int M, int ldx, const void* Wp,
+                           float* Y, int ldy, void* workspace, size_t workspace_bytes,
+                           lbv_stream stream)
+{
+    g_err.clear();
+    lbv_status st = check_verify_args(P, X, M, ldx, Wp, Y, ldy, workspace, workspace_bytes);
+    if (st != LBV_OK)
+        return st;
+    return lbv_verify_launch_internal(P, X, M, ldx, Wp, Y, ldy, P->use_gemv[M] != 0,
+                                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+lbv_status lbv_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
+                       const uint32_t* signs, lbv_stream stream)
+{
+    g_err.clear();
+    if (!X || !Xr)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fwht128: null X or Xr");
+    if (M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fwht128: M=%d outside 1..8", M);
+    if (K <= 0 || K % 128 != 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fwht128: K=%d not a positive multiple of 128", K);
+    if (dtype != LBV_F16 && dtype != LBV_BF16)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fwht128: unknown dtype %d", (int)dtype);
+    if ((reinterpret_cast<uintptr_t>(X) & 1u) || (reinterpret_cast<uintptr_t>(Xr) & 1u) ||
+        (reinterpret_cast<uintptr_t>(signs) & 3u))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fwht128: misaligned pointer");
+    cudaError_t e = lbv::launch_fwht128(X, Xr, M, K, dtype, signs,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_fwht128: launch");
+    return LBV_OK;
+}
+
+lbv_status lbv_dequant_fp16(const lbv_plan* P, const void* Wp, uint16_t* W, lbv_stream stream)
+{
+    g_err.clear();
+    if (!P || !Wp || !W)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: null argument");
+    if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0 || (reinterpret_cast<uintptr_t>(W) & 1u))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: misaligned pointer");
+    cudaError_t e = lbv::launch_dequant(
+        P->fmt, P->group, static_cast<const uint4*>(Wp),
+        static_cast<const uint8_t*>(Wp) + P->layout.side_offset, P->K, P->N,
+        (int)P->layout.ntiles, (int)P->layout.nchunks, W, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_dequant_fp16: launch");
+    return LBV_OK;
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------------------
+// Plan-time measurement (LBV_PLAN_MEASURE): time every launch shape that fits
+// and the 1-row path on scratch buffers with a cold L2, keep the fastest
+// shape, and pick per row count the faster of the few-row kernel and the
+// 1-row path run M times (Ishizuki releases v0.6.1: the verify kernel starts
+// at the row count where it is faster, per matrix).
+
+namespace {
+
+struct Scratch {
+    void* w = nullptr;
+    void* x = nullptr;
+    float* y = nullptr;
+    void* flush = nullptr;
+    size_t flush_bytes = 0;
+    ~Scratch()
+    {
+        cudaFree(w);
+        cudaFree(x);
+        cudaFree(y);
+        cudaFree(flush);
+    }
+};
+
+// Median time (us) of `reps` single launches, each after an L2 flush.
+template <class F>
+lbv_status time_cold(F&& launch, Scratch& s, cudaStream_t st, int reps, float* us)
+{
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    std::vector<float> v;
+    lbv_status rc = LBV_OK;
+    for (int i = 0; i < reps + 2 && rc == LBV_OK; ++i) {
+        cudaMemsetAsync(s.flush, i & 0xFF, s.flush_bytes, st);
+        cudaEventRecord(a, st);
+        rc = launch();
+        cudaEventRecord(b, st);
+        if (cudaEventSynchronize(b) != cudaSuccess) {
+            rc = fail(LBV_ERR_CUDA, "plan measure: %s", cudaGetErrorString(cudaGetLastError()));
+            break;
+        }
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, a, b);
+        if (i >= 2)
+            v.push_back(ms * 1000.f);
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    if (rc != LBV_OK)
+        return rc;
+    std::sort(v.begin(), v.end());
+    *us = v[v.size() / 2];
+    return LBV_OK;
+}
+
+}  // namespace
+
+lbv_status lbv_verify_launch_internal(const lbv_plan* P, const void* X, int M, int ldx,
+                                      const void* Wp, float* Y, int ldy, bool gemv,
+                                      cudaStream_t st);
+
+lbv_status lbv_plan_measure_internal(lbv_plan* P)
+{
+    Scratch s;
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, P->device);
+    s.flush_bytes = (size_t)std::max(l2, 1 << 20) * 2;
+    cudaError_t e = cudaMalloc(&s.w, P->layout.total);
+    if (e == cudaSuccess) e = cudaMalloc(&s.x, (size_t)8 * P->K * 2);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&s.y, (size_t)8 * P->N * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&s.flush, s.flush_bytes);
+    if (e == cudaSuccess) e = cudaMemset(s.w, 0x5A, P->layout.total);
+    if (e == cudaSuccess) e = cudaMemset(s.x, 0x11, (size_t)8 * P->K * 2);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "plan measure: scratch");
+    cudaStream_t st = nullptr;
+    const int reps = 7;
+
+    // 1) few-row launch shape
+    lbv::Shape best = P->shape;
+    float best_us = 1e30f;
+    const int warps_c[] = {4, 8};
+    const int tpw_c[] = {1, 2};
+    for (int w : warps_c)
+        for (int t : tpw_c)
+            for (int sp = 1; sp <= 8; ++sp) {
+                lbv::Shape sh = {w, t, sp, 0, 0};
+                if (!complete_shape(P, sh, 0) || sh.splits != sp)
+                    continue;
+                P->shape = sh;
+                float us = 0.f;
+                lbv_status rc = time_cold(
+                    [&] { return lbv_verify_launch_internal(P, s.x, 8, P->K, s.w, s.y, P->N, false, st); },
+                    s, st, reps, &us);
+                if (rc != LBV_OK)
+                    return rc;
+                if (us < best_us) {
+                    best_us = us;
+                    best = sh;
+                }
+            }
+    P->shape = best;
+    complete_shape(P, P->shape, 0);
+
+    // 2) per row count: few-row vs the 1-row path run M times
+    float gemv1 = 0.f;
+    lbv_status rc = time_cold(
+        [&] { return lbv_verify_launch_internal(P, s.x, 1, P->K, s.w, s.y, P->N, true, st); }, s,
+        st, reps, &gemv1);
+    if (rc != LBV_OK)
+        return rc;
+    P->crossover = 9;
+    for (int m = 1; m <= 8; ++m) {
+        float few = 0.f;
+        rc = time_cold(
+            [&] { return lbv_verify_launch_internal(P, s.x, m, P->K, s.w, s.y, P->N, false, st); },
+            s, st, reps, &few);
+        if (rc != LBV_OK)
+            return rc;
+        P->measured_us[m][0] = few;
+        P->measured_us[m][1] = gemv1 * m;
+        const bool g = !(P->flags & LBV_PLAN_FORCE_FEWROW) &&
+                       ((P->flags & LBV_PLAN_FORCE_GEMV) || gemv1 * m < few);
+        P->use_gemv[m] = g ? 1 : 0;
+        if (!g && P->crossover == 9)
+            P->crossover = m;
+    }
+    return LBV_OK;
+}
+
+extern "C" lbv_status lbv_plan_measured(const lbv_plan* P, int M, float* fewrow_us,
+                                        float* gemv_us, int* crossover)
+{
+    g_err.clear();
+    if (!P || M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_measured: bad plan or M");
+    if (fewrow_us) *fewrow_us = P->measured_us[M][0];
+    if (gemv_us) *gemv_us = P->measured_us[M][1];
+    if (crossover) *crossover = P->crossover;
+    return LBV_OK;
+}

@@ -1,0 +1,338 @@
+// aux_kernels.cu -- the blockwise FWHT-128 activation rotation, the 1-row
+// (GEMV) path and the dense fp16 dequant test export.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "lbv_internal.h"
+
+namespace lbv {
+
+// ---------------------------------------------------------------------------
+// FWHT-128: one warp per 128-element block; lane holds elements 4*lane + i.
+// Butterflies in fp64 are exact for fp16 inputs (and for bf16 blocks whose
+// magnitudes span less than 2^45), so the only rounding is the IEEE division
+// by sqrt(128) and the final round to nearest even in the output dtype.
+// dflash-mlx-bonsai2 README, "What this fork adds" (sign, Hadamard prep);
+// Sylvester natural order: H[i][j] = (-1)^popcount(i & j).
+
+template <int DT>
+__device__ __forceinline__ double to_f64(uint16_t b)
+{
+    if constexpr (DT == LBV_F16)
+        return (double)__half2float(__ushort_as_half(b));
+    else
+        return (double)__bfloat162float(__ushort_as_bfloat16(b));
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t from_f64(double v)
+{
+    if constexpr (DT == LBV_F16)
+        return __half_as_ushort(__double2half(v));
+    else
+        return __bfloat16_as_ushort(__double2bfloat16(v));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) lbv_fwht128_kernel(const uint16_t* X, uint16_t* Xr, int M,
+                                                           int K, const uint32_t* signs)
+{
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 128;
+    const int blk = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (blk >= M * nb)
+        return;
+    const int row = blk / nb, b = blk - row * nb;
+    const size_t base = (size_t)row * K + (size_t)b * 128 + 4 * lane;
+    double v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        double x = to_f64<DT>(X[base + i]);
+        if (signs) {
+            const int k = b * 128 + 4 * lane + i;
+            if ((signs[k >> 5] >> (k & 31)) & 1u)
+                x = -x;
+        }
+        v[i] = x;
+    }
+    // h = 1, 2: within the lane
+#pragma unroll
+    for (int h = 1; h <= 2; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (!(i & h)) {
+                const double a = v[i], c = v[i + h];
+                v[i] = a + c;
+                v[i + h] = a - c;
+            }
+    // h = 4 .. 64: partner lane = lane ^ (h / 4)
+#pragma unroll
+    for (int lm = 1; lm <= 16; lm <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const double o = __shfl_xor_sync(0xffffffffu, v[i], lm);
+            v[i] = (lane & lm) ? (o - v[i]) : (v[i] + o);
+        }
+    }
+    __syncwarp();
+    const double norm = sqrt(128.0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        Xr[base + i] = from_f64<DT>(v[i] / norm);
+}
+
+cudaError_t launch_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dt,
+                           const uint32_t* signs, cudaStream_t st)
+{
+    const int nblk = M * (K / 128);
+    const dim3 grid((unsigned)((nblk + 7) / 8));
+    if (dt == LBV_F16)
+        lbv_fwht128_kernel<LBV_F16><<<grid, 256, 0, st>>>((const uint16_t*)X, (uint16_t*)Xr, M,
+                                                           K, signs);
+    else
+        lbv_fwht128_kernel<LBV_BF16><<<grid, 256, 0, st>>>((const uint16_t*)X, (uint16_t*)Xr,
+                                                            M, K, signs);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Per-format constants of the device layout (see layout.h).
+
+template <int FMT, int GROUP>
+struct AuxTraits;
+template <>
+struct AuxTraits<LBV_FMT_SIGN1_G128, 128> {
+    static constexpr int CK = 256, KT = 16, W = 1, SLOTS = 16, GK = 128, SIDE_W = 2;
+};
+template <int G>
+struct AuxTraits<LBV_FMT_AFFINE2, G> {
+    static constexpr int CK = 128, KT = 8, W = 2, SLOTS = 8, GK = G, SIDE_W = 2 * (128 / G);
+};
+template <>
+struct AuxTraits<LBV_FMT_Q4_0, 32> {
+    static constexpr int CK = 64, KT = 4, W = 4, SLOTS = 4, GK = 32, SIDE_W = 2;
+};
+
+// fp16 of one scale/bias half of a side word: lo half = column g, hi = g + 8.
+__device__ __forceinline__ uint16_t side_half(uint32_t word, int hi)
+{
+    return hi ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFFu);
+}
+
+__device__ __forceinline__ float h2f(uint16_t b)
+{
+    return __half2float(__ushort_as_half(b));
+}
+
+// ---------------------------------------------------------------------------
+// Dense fp16 dequant (test export): one thread per (tile, chunk, lane).
+// sign1: +-s exactly; affine: s*q + b exact in fp64, rounded once; Q4_0:
+// d*(q-8) exact in fp32, rounded once.
+
+template <int FMT, int GROUP>
+__global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint4* codes,
+                                                          const uint8_t* side, int K, int N,
+                                                          int ntiles, int nchunks, uint16_t* W)
+{
+    using A = AuxTraits<FMT, GROUP>;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long total = (long long)ntiles * nchunks * 32;
+    if (idx >= total)
+        return;
+    const int lane = (int)(idx & 31);
+    const long long tc = idx >> 5;
+    const int tile = (int)(tc / nchunks), chunk = (int)(tc - (long long)tile * nchunks);
+    const int g = lane >> 2, t = lane & 3;
+    const uint4 q = codes[idx];
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(side + (tc * 8 + g) * (A::SIDE_W * 4));
+    for (int wi = 0; wi < 4; ++wi) {
+        const int col = tile * 16 + g + 8 * (wi & 1);
+        const int hi = wi & 1;
+        const int half = wi >> 1;
+        if (col >= N)
+            continue;
+        for (int s = 0; s < A::SLOTS; ++s) {
+            const int kt = half * (A::KT / 2) + (s >> 1);
+            const int k0 = chunk * A::CK + 16 * kt + 8 * (s & 1) + 2 * t;
+            const int gi = (16 * kt) / A::GK;        // group within the chunk
+            for (int h = 0; h < 2; ++h) {
+                const int k = k0 + h;
+                if (k >= K)
+                    continue;
+                const uint32_t code = (wv[wi] >> (s * A::W + 16 * h)) & ((1u << A::W) - 1u);
+                uint16_t out;
+                if constexpr (FMT == LBV_FMT_SIGN1_G128) {
+                    const uint16_t sb = side_half(sw[gi], hi);
+                    out = code ? sb : (uint16_t)(sb ^ 0x8000u);
+                } else if constexpr (FMT == LBV_FMT_AFFINE2) {
+                    const double sc = (double)h2f(side_half(sw[2 * gi], hi));
+                    const double bi = (double)h2f(side_half(sw[2 * gi + 1], hi));
+                    out = __half_as_ushort(__double2half(sc * (double)code + bi));
+                } else {
+                    const float d = h2f(side_half(sw[gi], hi));
+                    out = __half_as_ushort(__float2half_rn(d * (float)((int)code - 8)));
+                }
+                W[(size_t)k * N + col] = out;
+            }
+        }
+    }
+}
+
+cudaError_t launch_dequant(lbv_format fmt, int group, const uint4* codes, const uint8_t* side,
+                           int K, int N, int ntiles, int nchunks, uint16_t* W, cudaStream_t st)
+{
+    const long long total = (long long)ntiles * nchunks * 32;
+    const dim3 grid((unsigned)((total + 255) / 256));
+    switch (fmt) {
+    case LBV_FMT_SIGN1_G128:
+        lbv_dequant_kernel<LBV_FMT_SIGN1_G128, 128>
+            <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+        break;
+    case LBV_FMT_AFFINE2:
+        if (group == 32)
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 32>
+                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+        else if (group == 64)
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 64>
+                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+        else
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 128>
+                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+        break;
+    case LBV_FMT_Q4_0:
+        lbv_dequant_kernel<LBV_FMT_Q4_0, 32>
+            <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// 1-row path (the plain decode step): one warp per 16-column tile over all of
+// K, fp32 FMAs on the FMA pipe, run once per row.  Each lane decodes the same
+// codes the few-row kernel's lane does; the 4 lanes of a column pair reduce
+// by shuffles.
+
+template <int DT>
+__device__ __forceinline__ float2 x_pair(const uint16_t* x, int k)
+{
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(x + k);   // k even
+    if constexpr (DT == LBV_F16) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&v));
+    } else {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    }
+}
+
+template <int FMT, int DT, int GROUP>
+__global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int row)
+{
+    using A = AuxTraits<FMT, GROUP>;
+    constexpr int KTG = A::GK / 16;                  // k-tiles per scale group
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int tile = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (tile >= p.ntiles)
+        return;
+    const uint16_t* x = reinterpret_cast<const uint16_t*>(p.X) + (size_t)row * p.ldx;
+    float y0 = 0.f, y1 = 0.f;                        // columns g and g + 8
+    for (int chunk = 0; chunk < p.nchunks; ++chunk) {
+        const size_t tc = (size_t)tile * p.nchunks + chunk;
+        const uint4 q = __ldg(p.codes + tc * 32 + lane);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.side + (tc * 8 + g) * (A::SIDE_W * 4));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            // k-tiles of this half, grouped by scale group
+#pragma unroll
+            for (int kt0 = 0; kt0 < A::KT / 2; kt0 += (KTG < A::KT / 2 ? KTG : A::KT / 2)) {
+                float a0 = 0.f, a1 = 0.f, r = 0.f;   // column g, column g + 8, row sum
+                constexpr int span = KTG < A::KT / 2 ? KTG : A::KT / 2;
+#pragma unroll
+                for (int kk = 0; kk < span; ++kk) {
+                    const int ktl = kt0 + kk;
+                    const int kt = half * (A::KT / 2) + ktl;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int s = 2 * ktl + rr;
+                        const int k = chunk * A::CK + 16 * kt + 8 * rr + 2 * t;
+                        float2 xv = make_float2(0.f, 0.f);
+                        if (k < p.K)
+                            xv = x_pair<DT>(x, k);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float xs = h ? xv.y : xv.x;
+                            const int sh = s * A::W + 16 * h;
+                            const uint32_t c0 = (wv[2 * half] >> sh) & ((1u << A::W) - 1u);
+                            const uint32_t c1 = (wv[2 * half + 1] >> sh) & ((1u << A::W) - 1u);
+                            if constexpr (FMT == LBV_FMT_SIGN1_G128) {
+                                a0 += c0 ? xs : -xs;
+                                a1 += c1 ? xs : -xs;
+                            } else if constexpr (FMT == LBV_FMT_AFFINE2) {
+                                a0 = fmaf((float)c0, xs, a0);
+                                a1 = fmaf((float)c1, xs, a1);
+                                r += xs;
+                            } else {
+                                a0 = fmaf((float)((int)c0 - 8), xs, a0);
+                                a1 = fmaf((float)((int)c1 - 8), xs, a1);
+                            }
+                        }
+                    }
+                }
+                const int gi = (16 * (half * (A::KT / 2) + kt0)) / A::GK;
+                if constexpr (FMT == LBV_FMT_AFFINE2) {
+                    const uint32_t sc = sw[2 * gi], bi = sw[2 * gi + 1];
+                    y0 = fmaf(h2f(side_half(sc, 0)), a0, fmaf(h2f(side_half(bi, 0)), r, y0));
+                    y1 = fmaf(h2f(side_half(sc, 1)), a1, fmaf(h2f(side_half(bi, 1)), r, y1));
+                } else {
+                    const uint32_t sc = sw[gi];
+                    y0 = fmaf(h2f(side_half(sc, 0)), a0, y0);
+                    y1 = fmaf(h2f(side_half(sc, 1)), a1, y1);
+                }
+            }
+        }
+    }
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t == 0) {
+        const int n0 = tile * 16 + g, n1 = n0 + 8;
+        float* yr = p.Y + (size_t)row * p.ldy;
+        if (n0 < p.N)
+            yr[n0] = y0;
+        if (n1 < p.N)
+            yr[n1] = y1;
+    }
+}
+
+template <int FMT, int GROUP>
+static cudaError_t gemv_t(lbv_dtype xt, const VerifyParams& p, int row, cudaStream_t st)
+{
+    const dim3 grid((unsigned)((p.ntiles + 7) / 8));
+    if (xt == LBV_F16)
+        lbv_gemv_kernel<FMT, LBV_F16, GROUP><<<grid, 256, 0, st>>>(p, row);
+    else
+        lbv_gemv_kernel<FMT, LBV_BF16, GROUP><<<grid, 256, 0, st>>>(p, row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv(lbv_format fmt, lbv_dtype xt, int group, const VerifyParams& p, int row,
+                        cudaStream_t st)
+{
+    switch (fmt) {
+    case LBV_FMT_SIGN1_G128:
+        return gemv_t<LBV_FMT_SIGN1_G128, 128>(xt, p, row, st);
+    case LBV_FMT_AFFINE2:
+        if (group == 32)
+            return gemv_t<LBV_FMT_AFFINE2, 32>(xt, p, row, st);
+        if (group == 64)
+            return gemv_t<LBV_FMT_AFFINE2, 64>(xt, p, row, st);
+        return gemv_t<LBV_FMT_AFFINE2, 128>(xt, p, row, st);
+    case LBV_FMT_Q4_0:
+        return gemv_t<LBV_FMT_Q4_0, 32>(xt, p, row, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace lbv

@@ -1,0 +1,219 @@
+/*
+ * lbv.h -- few-row low-bit verify matmul for GB300 (sm_103a).
+ *
+ *   Y[M,N] = X[M,K] . dequant(Wp)[K,N],   1 <= M <= 8 drafted rows.
+ *
+ * Wp is a packed low-bit weight matrix that is consumed directly: every
+ * weight is decoded once, in registers, and used against every row; it is
+ * never expanded in memory.  (Ishizuki README, "Kernels written for the
+ * verify": the verify kernel decodes each weight once into a matrix fragment
+ * and multiplies it against every drafted row; Bonsai-27B-mlx-1bit model card:
+ * packed weights are consumed directly, never expanded back to FP16.)
+ *
+ * Conventions for every entry point:
+ *   - Plain C ABI: pointers and sizes only.  "dev" pointers are CUDA device
+ *     memory of the current device, "host" pointers are host memory.
+ *   - The caller owns every buffer.  The library never allocates in
+ *     lbv_verify_gemm, lbv_fwht128 or lbv_dequant_fp16.  Plans are created and
+ *     destroyed by the caller and are immutable in between (safe to share
+ *     between host threads).
+ *   - Device work is asynchronous on the given stream; a status of LBV_OK
+ *     means the work was enqueued.  Errors are returned, never aborted on; no
+ *     kernel traps.  lbv_last_error() gives a thread-local message for the
+ *     last failing call of the calling thread.
+ *   - X rows are fp16 or bf16 (the plan's xdtype), row-major with leading
+ *     dimension ldx (elements); Y is fp32 row-major with leading dimension ldy.
+ *     Rows >= M of Y are never written.
+ */
+#ifndef LBV_H
+#define LBV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LBV_API __attribute__((visibility("default")))
+#else
+#define LBV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (binary-compatible with cudaStream_t); NULL = legacy stream. */
+typedef struct CUstream_st* lbv_stream;
+
+typedef enum {
+    LBV_OK = 0,
+    LBV_ERR_INVALID_ARG = 1,   /* bad pointer, size, M, dtype or leading dimension */
+    LBV_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement     */
+    LBV_ERR_CUDA = 3,          /* a CUDA runtime call failed (message has details) */
+    LBV_ERR_WORKSPACE = 4,     /* caller buffer too small                           */
+    LBV_ERR_TIMEOUT = 5        /* a bounded device wait gave up                     */
+} lbv_status;
+
+typedef enum {
+    /* 1-bit sign, one fp16 scale per 128 K-weights of a column: bit 0 -> -s,
+     * bit 1 -> +s, 1.125 bits/weight.  Bonsai-27B-mlx-1bit model card,
+     * format description. */
+    LBV_FMT_SIGN1_G128 = 0,
+    /* 2-bit affine groups, w = s*q + b, q in {0..3}, fp16 (s, b) per group of
+     * 32, 64 or 128 K-weights: 2 + 32/g bits/weight.  Ishizuki README ("plain
+     * MLX affine packs"); dflash-mlx-bonsai2 README ("Why"). */
+    LBV_FMT_AFFINE2 = 1,
+    /* GGUF Q4_0 blocks of 32: fp16 d and 16 bytes of nibbles, w = d*(q-8),
+     * 4.5 bits/weight.  Ishizuki README, "Credits" (GGUF blocks read as they
+     * are). */
+    LBV_FMT_Q4_0 = 2
+} lbv_format;
+
+typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
+
+/* Plan flags. */
+#define LBV_PLAN_MEASURE     0x1u  /* time the candidate launch shapes and the
+                                      1-row path at plan creation and keep the
+                                      fastest per row count (allocates and
+                                      synchronises inside lbv_plan_create) */
+#define LBV_PLAN_FORCE_FEWROW 0x2u /* always use the few-row kernel           */
+#define LBV_PLAN_FORCE_GEMV   0x4u /* always use the 1-row path (run per row) */
+#define LBV_PLAN_PDL          0x8u /* launch with programmatic dependent launch:
+                                      the kernel starts streaming Wp before the
+                                      previous kernel on the stream has finished
+                                      (X is read and Y written only after it has).
+                                      Only valid if the kernel launched just
+                                      before on the stream never writes Wp. */
+
+/* Kernel ids reported by lbv_plan_query. */
+#define LBV_KERNEL_FEWROW 1
+#define LBV_KERNEL_GEMV   2
+
+typedef struct lbv_plan lbv_plan;   /* opaque, library-owned */
+
+/* ------------------------------------------------------------------------ */
+/* Packing (host): canonical file layout -> the library's device layout.     */
+
+/*
+ * Size in bytes of the device layout of a K x N matrix, or 0 for an invalid
+ * shape.  For N % 16 == 0 and K a multiple of the format's chunk (256 for
+ * sign1, 128 for affine2, 64 for Q4_0) it equals the canonical size exactly
+ * (1.125, 2 + 32/g and 4.5 bits per weight); otherwise the last column tile
+ * and K chunk are padded with zero codes and zero scales, which contribute
+ * exactly 0.  `group` is ignored except for LBV_FMT_AFFINE2.
+ */
+LBV_API size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group);
+
+/*
+ * bits: host uint32 [N][K/32], bit k%32 of word k/32 = sign bit of weight
+ * (k, n) (little end first); scales: host fp16 bit patterns [N][K/128].
+ * K % 128 == 0.  out: host buffer of lbv_packed_bytes() bytes.
+ * Bonsai-27B-mlx-1bit model card, format description.
+ */
+LBV_API lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int K, int N,
+                              void* out, size_t out_bytes);
+
+/*
+ * codes: host uint32 [N][K/16], code of weight (k, n) in bits 2*(k%16)..+1 of
+ * word k/16 ("16 per uint32, little end first"); scales, biases: host fp16
+ * bit patterns [N][K/group], group in {32, 64, 128}, K % group == 0.
+ */
+LBV_API lbv_status lbv_pack_affine2(const uint32_t* codes, const uint16_t* scales,
+                            const uint16_t* biases, int K, int N, int group, void* out,
+                            size_t out_bytes);
+
+/*
+ * blocks: host bytes [N][K/32][18] in GGUF order: d (fp16, little-endian),
+ * then qs[16]; element j < 16 = qs[j] & 15, element j + 16 = qs[j] >> 4.
+ * K % 32 == 0.
+ */
+LBV_API lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t out_bytes);
+
+/* ------------------------------------------------------------------------ */
+/* Plans: all kernel and launch-shape selection happens here, once per shape
+ * (Ishizuki releases v0.6.1: each weight shape's kernel is set up once when
+ * the model loads; the verify kernel starts at the row count where it is
+ * faster, per matrix).  The activation dtype is part of the key (Ishizuki
+ * releases v0.6.1, "Verify kernels no longer mix up precisions"). */
+
+/* Creates a plan for the current device.  Returns LBV_ERR_INVALID_ARG for
+ * K, N <= 0 or a K the format cannot hold, LBV_ERR_UNSUPPORTED for a group
+ * other than 32/64/128 (affine2).  *out is NULL on failure. */
+LBV_API lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xdtype,
+                           unsigned flags, lbv_plan** out);
+LBV_API lbv_status lbv_plan_destroy(lbv_plan* plan);
+
+/* For a row count M (1..8): the kernel that lbv_verify_gemm will launch
+ * (LBV_KERNEL_FEWROW or LBV_KERNEL_GEMV), its K split (cluster size) and the
+ * workspace it needs (always 0 in this build).  Any output may be NULL. */
+LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, int* splits,
+                          size_t* workspace_bytes);
+
+/* The plan's launch shape for the few-row kernel: warps per CTA, column tiles
+ * (16 columns each) per warp, K split and CTAs along N.  For tests and
+ * benchmarks; any output may be NULL. */
+LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_per_warp, int* splits,
+                          int* ctas_n);
+
+/* Overrides the few-row launch shape (warps in {4, 8}, tiles_per_warp in
+ * {1, 2}, splits in 1..8, ctas_n >= 1 or 0 for automatic).  Returns
+ * LBV_ERR_UNSUPPORTED if the shape does not fit the device (shared memory).
+ * For tuning sweeps; not thread-safe against concurrent verify calls. */
+LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_warp, int splits,
+                              int ctas_n);
+
+/* With LBV_PLAN_MEASURE: the measured cold-L2 time (us) of the few-row kernel
+ * and of the 1-row path run M times at row count M, and the crossover (the
+ * smallest M that uses the few-row kernel; 9 if none).  Zero times without
+ * LBV_PLAN_MEASURE.  Any output may be NULL. */
+LBV_API lbv_status lbv_plan_measured(const lbv_plan* plan, int M, float* fewrow_us, float* gemv_us,
+                             int* crossover);
+
+/* ------------------------------------------------------------------------ */
+/* The verify matmul.                                                         */
+
+/*
+ * Y[m][n] = sum_k X[m][k] * w[k][n] for m < M, n < N, fp32 accumulation.
+ * X: dev [M][ldx] (plan xdtype), ldx >= K; Wp: dev, the device layout from
+ * lbv_pack_* (lbv_packed_bytes bytes, 16-byte aligned); Y: dev fp32 [M][ldy],
+ * ldy >= N.  1 <= M <= 8, else LBV_ERR_INVALID_ARG.  workspace may be NULL
+ * with workspace_bytes 0 (no plan in this build needs one).  Rows >= M cost
+ * the same as a full block of 8 and are never read or written (Ishizuki
+ * releases v0.6.1; dflash-mlx-bonsai2 README: 2-8-row calls are padded to 8).
+ * The result of row m depends only on row m of X (bitwise).
+ */
+LBV_API lbv_status lbv_verify_gemm(const lbv_plan* plan, const void* X, int M, int ldx,
+                           const void* Wp, float* Y, int ldy, void* workspace,
+                           size_t workspace_bytes, lbv_stream stream);
+
+/*
+ * Blockwise normalized Walsh-Hadamard rotation of activation rows:
+ * Xr[m][b*128 + i] = RNE( sum_j H[i][j] * sx_j / sqrt(128) ), where
+ * H[i][j] = (-1)^popcount(i & j) (Sylvester, natural order), x_j = X[m][b*128+j]
+ * and sx_j = -x_j where bit (b*128+j) of `signs` is set (signs: dev uint32
+ * [K/32], NULL for none).  The sum is exact and the one rounding is to the
+ * dtype, so the result is the correctly rounded rotation.  X, Xr: dev [M][K]
+ * contiguous, K % 128 == 0, 1 <= M <= 8; in place (X == Xr) allowed.
+ * dflash-mlx-bonsai2 README, "What this fork adds" (fused sign, Hadamard
+ * prep); Ishizuki README (2-bit Hadamard-rotated weights).
+ */
+LBV_API lbv_status lbv_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
+                       const uint32_t* signs, lbv_stream stream);
+
+/*
+ * Test export: the dense fp16 dequantized matrix, W[k][n] (dev, [K][N]
+ * row-major, ldw = N) rounded once to nearest even from the exact weight.
+ * Not part of the verify path (the verify never expands weights).
+ */
+LBV_API lbv_status lbv_dequant_fp16(const lbv_plan* plan, const void* Wp, uint16_t* W,
+                            lbv_stream stream);
+
+/* Thread-local message of the calling thread's last failing call ("" if none). */
+LBV_API const char* lbv_last_error(void);
+
+/* Library version string. */
+LBV_API const char* lbv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LBV_H */

@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
+    ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
     ap.add_argument("--json-out", default="")
     return ap.parse_args()
 
@@ -134,8 +136,11 @@ class ClockSampler:
 class Stack:
     """Distinct packed matrices of a workload resident on the device."""
 
-    def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int):
+    def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int,
+                 use_graphs: bool = True):
         import torch
+        self.use_graphs = use_graphs
+        self.graphs = {}
 
         import few_row_packed_gb300 as lbv
         wl = synth.WORKLOADS[workload]
@@ -174,6 +179,29 @@ class Stack:
         self.bytes_per_step = {m: sum(call_bytes(l[0], m) for l in self.layers) for m in range(1, 9)}
         self.calls = len(self.layers)
         self.launches_per_step = sum(2 if l[0].rotate else 1 for l in self.layers)
+
+    def graph(self, M, verify_only=False):
+        """A CUDA graph of one step (launches captured through the C ABI)."""
+        import torch
+        key = (M, verify_only)
+        if key not in self.graphs:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                self.step(M, verify_only)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(M, verify_only)
+            self.graphs[key] = g
+        return self.graphs[key]
+
+    def run(self, M, verify_only=False):
+        if self.use_graphs:
+            self.graph(M, verify_only).replay()
+        else:
+            self.step(M, verify_only)
 
     def step(self, M, verify_only=False):
         import few_row_packed_gb300 as lbv
@@ -266,19 +294,21 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     dev = torch.cuda.current_device()
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
-    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M)
+    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M,
+                  use_graphs=not args.no_graph)
     peak, peak_kind = peaks()
     phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
 
     # sustained warm-up with clock sampling, then the timed region
     sampler = ClockSampler(int(phys) if phys.isdigit() else dev)
     sampler.start()
-    t_end = time.time() + 1.5
+    stack.run(args.M)
+    t_end = time.time() + (0.0 if args.quick else 1.5)
     while time.time() < t_end:
         for _ in range(max(1, args.warmup)):
-            stack.step(args.M)
+            stack.run(args.M)
         torch.cuda.synchronize()
-    ms = timed(torch, lambda: stack.step(args.M), args.steps, args.warmup, barrier)
+    ms = timed(torch, lambda: stack.run(args.M), args.steps, args.warmup, barrier)
     clocks = sampler.stop()
     ms = reduce_max(ms)
     ms_per_step = ms / args.steps
@@ -287,7 +317,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
 
     # dominant kernel: the verify launch, timed alone (verify-only loop)
     if any(l[0].rotate for l in stack.layers):
-        ms_v = reduce_max(timed(torch, lambda: stack.step(args.M, verify_only=True), args.steps,
+        ms_v = reduce_max(timed(torch, lambda: stack.run(args.M, verify_only=True), args.steps,
                                 args.warmup, barrier))
     else:
         ms_v = ms
@@ -299,7 +329,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     per_M = {}
     if not args.no_sweep:
         for M in range(1, 9):
-            msm = reduce_max(timed(torch, lambda: stack.step(M), max(10, args.steps // 4),
+            msm = reduce_max(timed(torch, lambda: stack.run(M), max(10, args.steps // 4),
                                    args.warmup, barrier))
             us = msm * 1e3 / (max(10, args.steps // 4) * stack.calls)
             gbs = stack.bytes_per_step[M] / stack.calls / (us * 1e-6) / 1e9
@@ -316,7 +346,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
 
     def e2e_step():
         X_dev[:args.M].copy_(x_host[:args.M], non_blocking=True)
-        stack.step(args.M)
+        stack.run(args.M)
         y_host.copy_(Y_last[:args.M], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -350,7 +380,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "us_per_call": round(ms_per_step * 1e3 / stack.calls, 3),
             "l2": f"inputs larger than L2: {stack.calls} distinct resident matrices, "
                   f"{bytes_step / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
-            "launch": ("programmatic dependent launch, " if not args.no_pdl else "") +
+            "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
+                      ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
             "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
                       "ctas_n": shape[3]},

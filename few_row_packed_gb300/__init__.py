@@ -72,6 +72,7 @@ def lib():
             "lbv_plan_set_shape": (st, [P, I, I, I, I]),
             "lbv_plan_measured": (st, [P, I, ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
+            "lbv_plan_device_status": (st, [P]),
             "lbv_verify_gemm": (st, [P, P, I, I, P, P, I, P, S, P]),
             "lbv_fwht128": (st, [P, P, I, I, I, P, P]),
             "lbv_dequant_fp16": (st, [P, P, P, P]),
@@ -208,6 +209,11 @@ class Plan:
 
     def set_shape(self, warps: int, tiles_per_warp: int, splits: int, ctas_n: int = 0):
         _check(lib().lbv_plan_set_shape(self.handle, warps, tiles_per_warp, splits, ctas_n))
+
+    def device_status(self):
+        """Raises LbvError(ERR_TIMEOUT) if a kernel of this plan gave up a
+        bounded wait since the last check (synchronises the device)."""
+        _check(lib().lbv_plan_device_status(self.handle))
 
     def measured(self, M: int):
         f, g, c = ctypes.c_float(), ctypes.c_float(), ctypes.c_int()

@@ -80,57 +80,66 @@ int shape_cps(const lbv::Shape& sh, int64_t nchunks)
     return (int)((nchunks + sh.splits - 1) / sh.splits);
 }
 
-constexpr size_t kSmemCap = 200 * 1024;        // per CTA, of 227 KB
-constexpr size_t kSmemTwoCta = 100 * 1024;     // keep 2 CTAs per SM when possible
+constexpr size_t kSmemCap = 220 * 1024;        // per CTA, of 227 KB
 
-// Fills sh.smem and sh.ctas_n for a (warps, tpw, splits) choice.  Returns
-// false if it does not fit.
-bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_n_req)
+// Bytes per (tile, chunk) of the device layout and X bytes per chunk staged.
+size_t tile_chunk_bytes(const lbv_plan* P)
+{
+    return 512u + 8u * (size_t)P->fi.side_bytes;
+}
+
+// Fills sh.splits (clamped), sh.ctas_n and sh.smem for a (warps, tpw,
+// splits) choice: one cluster of `splits` CTAs per `splits` SMs, as many
+// clusters as can be resident at once, each owning a contiguous tile range.
+// ctas_req > 0 caps the number of clusters.  Returns false if nothing fits.
+bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
 {
     const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
     finish_shape(sh, P->layout.nchunks);
     const int cps = shape_cps(sh, P->layout.nchunks);
-    sh.smem = ops->smem(sh.warps, sh.tpw, cps);
-    if (sh.smem > kSmemCap)
-        return false;
-    const int64_t nunits = (P->layout.ntiles + sh.tpw - 1) / sh.tpw;
-    const int64_t nblocks = (nunits + sh.warps - 1) / sh.warps;
-    if (sh.splits > 1) {
-        sh.ctas_n = (int)nblocks;              // one column block per cluster
-    } else {
-        sh.ctas_n = 0;
+    const int64_t ntiles = P->layout.ntiles;
+    int64_t G = std::max<int64_t>(1, std::min<int64_t>(ntiles, P->sms / sh.splits));
+    if (ctas_req > 0)
+        G = std::min<int64_t>(G, ctas_req);
+    for (int it = 0; it < 4; ++it) {
+        const int tiles_max = (int)((ntiles + G - 1) / G);
+        sh.smem = ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits);
+        if (sh.smem > kSmemCap)
+            return false;
+        sh.ctas_n = (int)G;
         if (ops->prepare(P->xdtype, sh) != cudaSuccess)
             return false;
-        int occ = ops->occupancy(P->xdtype, sh);
-        if (occ < 1)
+        const int maxc = ops->max_clusters(P->xdtype, sh);
+        if (maxc < 1)
             return false;
-        int64_t cap = (int64_t)P->sms * occ;
-        if (ctas_n_req > 0)
-            cap = std::min<int64_t>(cap, ctas_n_req);
-        sh.ctas_n = (int)std::max<int64_t>(1, std::min<int64_t>(nblocks, cap));
+        if (G <= maxc)
+            return true;
+        G = maxc;
     }
+    sh.smem = ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits);
+    sh.ctas_n = (int)G;
     return ops->prepare(P->xdtype, sh) == cudaSuccess;
 }
 
-// Default launch shape: 8 warps, 1 tile per warp; the smallest K split that
-// gives about two CTAs per SM and keeps the staged slice small.
-lbv::Shape default_shape(const lbv_plan* P)
+// Default launch shape: 16 warps, one tile per warp unit; the K split that
+// minimises the bytes one CTA streams (its tile range times its slice) plus
+// half the activation bytes it stages.
+lbv::Shape default_shape(lbv_plan* P)
 {
-    const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
-    const int64_t nblocks = (P->layout.ntiles + 7) / 8;
-    const int64_t target = 2 * (int64_t)P->sms;
-    lbv::Shape best = {8, 1, 8, 0, 0};
+    lbv::Shape best = {16, 1, 1, 0, 0};
+    double best_cost = 1e300;
     for (int s = 1; s <= 8; ++s) {
-        lbv::Shape sh = {8, 1, s, 0, 0};
-        finish_shape(sh, P->layout.nchunks);
-        if (sh.splits != s && s > 1)
+        lbv::Shape sh = {16, 1, s, 0, 0};
+        if (!complete_shape(P, sh, 0) || sh.splits != s)
             continue;
         const int cps = shape_cps(sh, P->layout.nchunks);
-        if (ops->smem(8, 1, cps) > kSmemTwoCta)
-            continue;
-        best = sh;
-        if (nblocks * s >= target)
-            break;
+        const int64_t tmax = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
+        const double cost = (double)tmax * cps * tile_chunk_bytes(P) +
+                            0.5 * (double)cps * P->fi.chunk_k * 16.0;
+        if (cost < best_cost * 0.98) {
+            best_cost = cost;
+            best = sh;
+        }
     }
     return best;
 }
@@ -368,9 +377,17 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         delete P;
         return cuda_fail(e, "lbv_plan_create: device query");
     }
+    e = cudaMalloc((void**)&P->dev_err, 256);
+    if (e == cudaSuccess)
+        e = cudaMemset(P->dev_err, 0, 256);
+    if (e != cudaSuccess) {
+        cudaFree(P->dev_err);
+        delete P;
+        return cuda_fail(e, "lbv_plan_create: status word");
+    }
     lbv::Shape sh = default_shape(P);
     if (!complete_shape(P, sh, 0)) {
-        delete P;
+        lbv_plan_destroy(P);
         return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: no launch shape fits K=%d", K);
     }
     P->shape = sh;
@@ -382,7 +399,7 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         extern lbv_status lbv_plan_measure_internal(lbv_plan * P);
         lbv_status st = lbv_plan_measure_internal(P);
         if (st != LBV_OK) {
-            delete P;
+            lbv_plan_destroy(P);
             return st;
         }
     }
@@ -392,7 +409,26 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
 
 lbv_status lbv_plan_destroy(lbv_plan* plan)
 {
-    delete plan;
+    if (plan) {
+        cudaFree(plan->dev_err);
+        delete plan;
+    }
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_device_status(const lbv_plan* P)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_device_status: plan is NULL");
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpy(&v, P->dev_err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_plan_device_status");
+    if (v) {
+        cudaMemset(P->dev_err, 0, sizeof v);
+        return fail(LBV_ERR_TIMEOUT, "a verify kernel gave up waiting for its weight copies");
+    }
     return LBV_OK;
 }
 
@@ -430,7 +466,7 @@ lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int c
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: plan is NULL");
-    if ((warps != 4 && warps != 8) || (tpw != 1 && tpw != 2) || splits < 1 || splits > 8 ||
+    if ((warps != 8 && warps != 16) || (tpw != 1 && tpw != 2) || splits < 1 || splits > 8 ||
         ctas_n < 0)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: warps=%d tpw=%d splits=%d ctas_n=%d",
                     warps, tpw, splits, ctas_n);
@@ -488,6 +524,7 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.splits = P->shape.splits;
     p.cps = shape_cps(P->shape, P->layout.nchunks);
     p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
+    p.err = P->dev_err;
     return p;
 }
 
@@ -646,7 +683,7 @@ lbv_status lbv_plan_measure_internal(lbv_plan* P)
     // 1) few-row launch shape
     lbv::Shape best = P->shape;
     float best_us = 1e30f;
-    const int warps_c[] = {4, 8};
+    const int warps_c[] = {8, 16};
     const int tpw_c[] = {1, 2};
     for (int w : warps_c)
         for (int t : tpw_c)

@@ -14,6 +14,7 @@ struct VerifyParams {
     const uint4* codes;     // codes region of the device layout
     const uint8_t* side;    // side region
     float* Y;               // [M][ldy]
+    unsigned* err;          // device status word of the plan (bounded waits)
     int ldx, ldy;
     int M, K, N;
     int ntiles, nchunks;
@@ -24,27 +25,16 @@ struct VerifyParams {
 
 // Launch shape of the few-row kernel.
 struct Shape {
-    int warps;              // 4 or 8
-    int tpw;                // column tiles per warp, 1 or 2
-    int splits;             // 1..8
-    int ctas_n;             // CTAs along N (grid y)
+    int warps;              // 8 or 16
+    int tpw;                // column tiles per warp unit, 1 or 2
+    int splits;             // K slices (cluster size), 1..8
+    int ctas_n;             // clusters along N (grid y); each owns a contiguous tile range
     size_t smem;            // dynamic shared memory bytes
 };
 
 struct LaunchOpts {
     bool pdl;               // programmatic dependent launch
 };
-
-// Few-row kernel launcher for one (format, xdtype, group); defined in the
-// per-format .cu files.  Returns a CUDA error code.
-cudaError_t launch_verify(lbv_format fmt, lbv_dtype xt, int group, const Shape& sh,
-                          const VerifyParams& p, const LaunchOpts& o, cudaStream_t st);
-// Shared memory the few-row kernel needs for a slice of `cps` chunks.
-size_t verify_smem_bytes(lbv_format fmt, int group, int warps, int tpw, int cps);
-// Sets the kernel's dynamic shared memory limit (once per kernel/shape).
-cudaError_t prepare_verify(lbv_format fmt, lbv_dtype xt, int group, const Shape& sh);
-// Max resident CTAs per SM for the shape (0 if it does not fit).
-int verify_occupancy(lbv_format fmt, lbv_dtype xt, int group, const Shape& sh);
 
 // One-row (GEMV) path, FMA pipe, run once per row.
 cudaError_t launch_gemv(lbv_format fmt, lbv_dtype xt, int group, const VerifyParams& p,
@@ -69,5 +59,6 @@ struct lbv_plan {
     lbv::Shape shape;        // few-row launch shape
     int use_gemv[9];         // per M (1..8): 1 = run the 1-row path M times
     int crossover;           // smallest M that uses the few-row kernel
+    unsigned* dev_err;       // device status word (set when a bounded wait gives up)
     float measured_us[9][2]; // per M: [few-row, 1-row x M] (LBV_PLAN_MEASURE), else 0
 };

@@ -2,28 +2,34 @@
 // M <= 8, for the packed formats of layout.h.
 //
 // Design (GB300, sm_103a):
-//   * One warp owns TPW 16-column tiles and streams their packed codes with
-//     one 16-byte non-caching load per lane per chunk, D chunks in flight.
+//   * Persistent grid of thread-block clusters.  Cluster y owns a contiguous,
+//     balanced range of 16-column tiles; the S CTAs of a cluster split K into
+//     slices, and their partial sums are reduced through distributed shared
+//     memory in rank order (deterministic, no workspace).
+//   * Each CTA stages its K slice of X once, in mma fragment order, with the
+//     per-group corrections (below).  X is read only after griddepcontrol.wait;
+//     the packed weights, which no kernel writes, start streaming before it.
+//   * Each warp streams its tiles' packed codes and scales through a private
+//     ring of shared-memory stages filled by 1-D bulk async copies (TMA engine)
+//     and tracked by mbarriers, so a few tens of KB per SM stay in flight with
+//     no registers held.  Every wait is bounded; a wait that gives up sets the
+//     plan's status word and the warp stops.
 //   * Decode is one LOP3 per A-fragment register: (word_variant & mask) ^ base
 //     places a code in the mantissa/exponent field of an fp16 or bf16 whose
 //     value is  code_value + c  for a small integer c fixed by the bit position
-//     (the pages' "codes turned into exact halves with 0x6400 less 1024" idea,
-//     extended to every position of the word).  Only 1-3 shifts per 32-bit
-//     word bring the remaining positions into place.
-//   * mma.sync m16n8k16 (fp16 or bf16 in, fp32 accumulate): the 16 weight
-//     columns are the M side, the M <= 8 activation rows the N side (rows >= M
-//     are zero), so each decoded weight is used against every row at once
-//     (Ishizuki README, "Kernels written for the verify").
+//     (the "codes turned into exact halves with 0x6400 less 1024" idea of the
+//     Ishizuki README credits, extended to every position of the word); 1-3
+//     shifts per 32-bit word bring the remaining positions into place.
+//   * mma.sync m16n8k16 (fp16 or bf16 in, fp32 accumulate): 16 weight columns
+//     are the M side and the M <= 8 activation rows the N side (rows >= M are
+//     zero), so each decoded weight meets every drafted row at once (Ishizuki
+//     README, "Kernels written for the verify").  The k-tiles of a chunk are
+//     issued alternately from two independent accumulator chains.
 //   * The offsets c enter each group's accumulator as its initial value
-//     -sum_k c_k x_k (precomputed per group and row from the staged
-//     activations, the "row-sum prep" of the dflash-mlx-bonsai2 README); the
-//     group scale (and bias * row sum for affine) is applied in fp32 once per
-//     group, so every operand of the tensor core is an exact small integer.
-//   * The CTA stages its K slice of X once in shared memory in fragment order.
-//     A split of K across a thread-block cluster is reduced through
-//     distributed shared memory in a fixed order (deterministic, no workspace).
-//   * Weight loads for the first chunks are issued before griddepcontrol.wait,
-//     so under programmatic dependent launch they overlap the previous kernel.
+//     -sum_k c_k x_k, computed once per CTA from the staged activations (the
+//     "row-sum prep" of the dflash-mlx-bonsai2 README); the group scale (and
+//     bias * row sum for affine) is applied in fp32 once per group, so every
+//     tensor-core operand is an exact small integer.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -148,20 +154,9 @@ __device__ __forceinline__ uint32_t decode(uint32_t w)
     return (v & mask) ^ base;
 }
 
-// Offset c of slot s (runtime s: prologue only).
-template <int FMT, int XT>
-__device__ __forceinline__ float slot_coef(int s)
-{
-    float c = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (i == s)
-            c = (float)dec_spec<FMT>(XT, i).c;
-    return c;
-}
 
 // ---------------------------------------------------------------------------
-// Small device helpers
+// Device helpers
 
 template <int XT>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -180,22 +175,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
     }
 }
 
-__device__ __forceinline__ uint4 ldg_stream16(const uint4* p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint2 ldg_nc8(const void* p)
-{
-    uint2 r;
-    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];\n" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -204,6 +183,63 @@ __device__ __forceinline__ void griddep_wait()
 __device__ __forceinline__ void griddep_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  Returns false if it did
+// not complete within roughly a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    constexpr uint32_t kSpin = 1u << 12, kLimit = 1u << 20;
+    for (uint32_t i = 0; i < kLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if (i >= kSpin)
+            __nanosleep(1000);
+    }
+    return false;
 }
 
 template <int XT>
@@ -224,16 +260,36 @@ __device__ __forceinline__ float2 f16pair(uint32_t v)
     return __half22float2(h);
 }
 
-template <int NW_>
-struct SideBuf {
-    uint32_t w[NW_];
+// ---------------------------------------------------------------------------
+// Compile-time geometry of one (format, group, warps, tiles-per-warp) kernel.
+
+template <int FMT, int GROUP, int NW, int TPW>
+struct Geometry {
+    using T = Traits<FMT, GROUP>;
+    static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (tile, chunk, g)
+    static constexpr int TILE_B = 512 + 8 * SIDE_B;           // bytes per tile and chunk
+    static constexpr int SLOT_B = TPW * TILE_B;               // one ring stage
+    static constexpr int STAGES_RAW = 65536 / (NW * SLOT_B);
+    static constexpr int STAGES = STAGES_RAW < 4 ? 4 : STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
+    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8;
+    // corrections and row sums per group of the slice
+    static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
 };
 
-// ---------------------------------------------------------------------------
-// Shared memory carve-up (bytes): xf | corr | rsum (affine) | part
-__host__ __device__ inline size_t smem_xf_bytes(int kt, int cps)
+// Shared memory carve-up (bytes):
+//   ring | mbarriers | xf (X fragments) | corr | rsum (affine) | part (K split)
+template <int FMT, int GROUP, int NW, int TPW>
+__host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
 {
-    return (size_t)cps * kt * 256u;
+    using G = Geometry<FMT, GROUP, NW, TPW>;
+    using T = Traits<FMT, GROUP>;
+    size_t b = G::RING_B + G::BAR_B;
+    b += (size_t)cps * T::KT * 256u;
+    b += (size_t)cps * T::GPC * 8 * 4 * G::CORR_ARRAYS;
+    if (splits > 1)
+        b += (size_t)tiles_max * 512u;
+    return b;
 }
 
 // ---------------------------------------------------------------------------
@@ -241,293 +297,156 @@ __host__ __device__ inline size_t smem_xf_bytes(int kt, int cps)
 template <int FMT, int XT, int GROUP, int NW, int TPW>
 struct VerifyKernel {
     using T = Traits<FMT, GROUP>;
-    static constexpr int D = 4;                    // chunks in flight per warp
-    using Side = SideBuf<T::SIDE_W>;
+    using G = Geometry<FMT, GROUP, NW, TPW>;
+    static constexpr int STAGES = G::STAGES;
+    static constexpr int NSET = T::GPC >= 2 ? T::GPC : 2;   // accumulator chains per tile
 
-    static __device__ __forceinline__ void load_chunk(const VerifyParams& p, int unit, int chunk,
-                                                      int lane, uint4 (&w)[TPW], Side (&s)[TPW])
+    // All lanes of a warp track the same cursor; lane 0 issues the copies of
+    // (unit, chunk) into ring stage `slot`.
+    static __device__ __forceinline__ void issue(const VerifyParams& p, int t0, int t1, int unit,
+                                                 int chunk, uint32_t ring_w, uint32_t bars_w,
+                                                 int slot)
     {
+        const uint32_t bar = bars_w + slot * 8;
+        const uint32_t dst = ring_w + slot * G::SLOT_B;
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl)
+            if (t0 + unit * TPW + tl < t1)
+                bytes += G::TILE_B;
+        mbar_expect_tx(bar, bytes);
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
-            const int tile = unit * TPW + tl;
-            if (tile < p.ntiles) {
+            const int tile = t0 + unit * TPW + tl;
+            if (tile < t1) {
                 const size_t tc = (size_t)tile * p.nchunks + chunk;
-                w[tl] = ldg_stream16(p.codes + tc * 32 + lane);
-                const uint8_t* sp = p.side + (tc * 8 + (lane >> 2)) * (T::SIDE_W * 4);
-#pragma unroll
-                for (int i = 0; i < T::SIDE_W; i += 2) {
-                    const uint2 v = ldg_nc8(sp + i * 4);
-                    s[tl].w[i] = v.x;
-                    s[tl].w[i + 1] = v.y;
-                }
-            } else {
-                w[tl] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int i = 0; i < T::SIDE_W; ++i)
-                    s[tl].w[i] = 0u;
+                bulk_g2s(dst + tl * 512, p.codes + tc * 32, 512u, bar);
+                bulk_g2s(dst + TPW * 512 + tl * 8 * G::SIDE_B, p.side + tc * 8 * G::SIDE_B,
+                         8u * G::SIDE_B, bar);
             }
         }
     }
 
-    // One k-tile (chunk-local index KTC) of TPW tiles: decode the four A
-    // registers of slots 2*ktl and 2*ktl + 1 from the column-g word and the
-    // column-(g+8) word of the right half, then one mma per tile.
-    template <int KTC>
-    static __device__ __forceinline__ void do_ktile(const uint4 (&w)[TPW], uint32_t b0,
-                                                    uint32_t b1, float (&acc)[TPW][4])
+    // One k-tile: decode the four A registers (slots 2*ktl, 2*ktl+1 of the
+    // column-g word and the column-(g+8) word of half HALF) and issue the mma.
+    template <int HALF, int KTL>
+    static __device__ __forceinline__ void ktile(const uint4 (&w)[TPW], uint32_t b0, uint32_t b1,
+                                                 float (&acc)[TPW][NSET][4])
     {
-        constexpr int half = KTC / (T::KT / 2);
-        constexpr int ktl = KTC % (T::KT / 2);
+        constexpr int kt = HALF * (T::KT / 2) + KTL;
+        constexpr int set = T::GPC >= 2 ? kt / T::KTG : HALF;
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
-            const uint32_t wa = half ? w[tl].z : w[tl].x;
-            const uint32_t wb = half ? w[tl].w : w[tl].y;
-            const uint32_t a0 = decode<FMT, XT, 2 * ktl>(wa);
-            const uint32_t a1 = decode<FMT, XT, 2 * ktl>(wb);
-            const uint32_t a2 = decode<FMT, XT, 2 * ktl + 1>(wa);
-            const uint32_t a3 = decode<FMT, XT, 2 * ktl + 1>(wb);
-            mma16816<XT>(acc[tl], a0, a1, a2, a3, b0, b1);
+            const uint32_t wa = HALF ? w[tl].z : w[tl].x;
+            const uint32_t wb = HALF ? w[tl].w : w[tl].y;
+            const uint32_t a0 = decode<FMT, XT, 2 * KTL>(wa);
+            const uint32_t a1 = decode<FMT, XT, 2 * KTL>(wb);
+            const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa);
+            const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb);
+            mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
         }
     }
 
-    template <int GI, int... P>
-    static __device__ __forceinline__ void do_pairs(std::integer_sequence<int, P...>,
-                                                    const uint4 (&w)[TPW], int cl,
-                                                    const uint4* __restrict__ xf, int lane,
-                                                    float (&acc)[TPW][4])
+    // k-tile pair P of both halves, alternating between the two halves'
+    // accumulator chains.
+    template <int... P>
+    static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
+                                                 const uint4 (&w)[TPW], const uint4* xrow,
+                                                 int lane, float (&acc)[TPW][NSET][4])
     {
         (
             [&] {
-                constexpr int ktc = GI * T::KTG + 2 * P;
-                const uint4 bq = xf[((cl * T::KT + ktc) >> 1) * 32 + lane];
-                do_ktile<ktc>(w, bq.x, bq.y, acc);
-                do_ktile<ktc + 1>(w, bq.z, bq.w, acc);
+                const uint4 q0 = xrow[(2 * P) / 2 * 32 + lane];
+                const uint4 q1 = xrow[(T::KT / 2 + 2 * P) / 2 * 32 + lane];
+                ktile<0, 2 * P>(w, q0.x, q0.y, acc);
+                ktile<1, 2 * P>(w, q1.x, q1.y, acc);
+                ktile<0, 2 * P + 1>(w, q0.z, q0.w, acc);
+                ktile<1, 2 * P + 1>(w, q1.z, q1.w, acc);
             }(),
             ...);
     }
 
-    // One scale group GI of a chunk: accumulate from the group's correction,
-    // then y += scale * acc (+ bias * rowsum for affine) in fp32.
-    template <int GI>
-    static __device__ __forceinline__ void do_group(const uint4 (&w)[TPW], const Side (&s)[TPW],
-                                                    int cl, const uint4* __restrict__ xf,
-                                                    const float* __restrict__ corr,
-                                                    const float* __restrict__ rsum,
-                                                    float (&y)[TPW][4], int lane)
+    template <int... GI>
+    static __device__ __forceinline__ void epilogue(std::integer_sequence<int, GI...>,
+                                                    const uint32_t (&sd)[TPW][T::SIDE_W],
+                                                    const float* corr_c, const float* rsum_c,
+                                                    float (&acc)[TPW][NSET][4],
+                                                    float (&y)[TPW][4], int t)
     {
-        const int t = lane & 3;
-        const int gr = cl * T::GPC + GI;
-        const float2 I = *reinterpret_cast<const float2*>(corr + gr * 8 + 2 * t);
-        float acc[TPW][4];
+        (
+            [&] {
+                constexpr int gi = GI;
 #pragma unroll
-        for (int tl = 0; tl < TPW; ++tl) {
-            acc[tl][0] = I.x;
-            acc[tl][1] = I.y;
-            acc[tl][2] = I.x;
-            acc[tl][3] = I.y;
-        }
-        do_pairs<GI>(std::make_integer_sequence<int, T::KTG / 2>{}, w, cl, xf, lane, acc);
+                for (int tl = 0; tl < TPW; ++tl) {
+                    float a[4];
 #pragma unroll
-        for (int tl = 0; tl < TPW; ++tl) {
-            if constexpr (T::AFFINE) {
-                const float2 sc = f16pair(s[tl].w[2 * GI]);
-                const float2 bi = f16pair(s[tl].w[2 * GI + 1]);
-                const float2 R = *reinterpret_cast<const float2*>(rsum + gr * 8 + 2 * t);
-                y[tl][0] = fmaf(sc.x, acc[tl][0], fmaf(bi.x, R.x, y[tl][0]));
-                y[tl][1] = fmaf(sc.x, acc[tl][1], fmaf(bi.x, R.y, y[tl][1]));
-                y[tl][2] = fmaf(sc.y, acc[tl][2], fmaf(bi.y, R.x, y[tl][2]));
-                y[tl][3] = fmaf(sc.y, acc[tl][3], fmaf(bi.y, R.y, y[tl][3]));
-            } else {
-                const float2 sc = f16pair(s[tl].w[GI]);
-                y[tl][0] = fmaf(sc.x, acc[tl][0], y[tl][0]);
-                y[tl][1] = fmaf(sc.x, acc[tl][1], y[tl][1]);
-                y[tl][2] = fmaf(sc.y, acc[tl][2], y[tl][2]);
-                y[tl][3] = fmaf(sc.y, acc[tl][3], y[tl][3]);
-            }
-        }
+                    for (int j = 0; j < 4; ++j)
+                        a[j] = T::GPC >= 2 ? acc[tl][gi][j] : acc[tl][0][j] + acc[tl][1][j];
+                    if constexpr (T::AFFINE) {
+                        const float2 sc = f16pair(sd[tl][2 * gi]);
+                        const float2 bi = f16pair(sd[tl][2 * gi + 1]);
+                        const float2 R = *reinterpret_cast<const float2*>(rsum_c + gi * 8 + 2 * t);
+                        y[tl][0] = fmaf(sc.x, a[0], fmaf(bi.x, R.x, y[tl][0]));
+                        y[tl][1] = fmaf(sc.x, a[1], fmaf(bi.x, R.y, y[tl][1]));
+                        y[tl][2] = fmaf(sc.y, a[2], fmaf(bi.y, R.x, y[tl][2]));
+                        y[tl][3] = fmaf(sc.y, a[3], fmaf(bi.y, R.y, y[tl][3]));
+                    } else {
+                        const float2 sc = f16pair(sd[tl][gi]);
+                        y[tl][0] = fmaf(sc.x, a[0], y[tl][0]);
+                        y[tl][1] = fmaf(sc.x, a[1], y[tl][1]);
+                        y[tl][2] = fmaf(sc.y, a[2], y[tl][2]);
+                        y[tl][3] = fmaf(sc.y, a[3], y[tl][3]);
+                    }
+                }
+            }(),
+            ...);
     }
 
-    template <int... G>
-    static __device__ __forceinline__ void do_groups(std::integer_sequence<int, G...>,
-                                                     const uint4 (&w)[TPW], const Side (&s)[TPW],
-                                                     int cl, const uint4* __restrict__ xf,
-                                                     const float* __restrict__ corr,
-                                                     const float* __restrict__ rsum,
-                                                     float (&y)[TPW][4], int lane)
-    {
-        (do_group<G>(w, s, cl, xf, corr, rsum, y, lane), ...);
-    }
-
-    // One chunk (cl = chunk index within the slice) of TPW tiles.
+    // One chunk (cl = chunk index within the slice) of a warp's unit.
     static __device__ __forceinline__ void process_chunk(const uint4 (&w)[TPW],
-                                                         const Side (&s)[TPW], int cl,
-                                                         const uint4* __restrict__ xf,
+                                                         const uint32_t (&sd)[TPW][T::SIDE_W],
+                                                         int cl, const uint4* __restrict__ xf,
                                                          const float* __restrict__ corr,
                                                          const float* __restrict__ rsum,
                                                          float (&y)[TPW][4], int lane)
     {
-        do_groups(std::make_integer_sequence<int, T::GPC>{}, w, s, cl, xf, corr, rsum, y, lane);
+        const int t = lane & 3;
+        const float* corr_c = corr + cl * T::GPC * 8;
+        const float* rsum_c = rsum + cl * T::GPC * 8;
+        float acc[TPW][NSET][4];
+#pragma unroll
+        for (int j = 0; j < NSET; ++j) {
+            float2 I = make_float2(0.f, 0.f);
+            if (T::GPC >= 2 || j == 0)
+                I = *reinterpret_cast<const float2*>(corr_c + (T::GPC >= 2 ? j : 0) * 8 + 2 * t);
+#pragma unroll
+            for (int tl = 0; tl < TPW; ++tl) {
+                acc[tl][j][0] = I.x;
+                acc[tl][j][1] = I.y;
+                acc[tl][j][2] = I.x;
+                acc[tl][j][3] = I.y;
+            }
+        }
+        const uint4* xrow = xf + (size_t)cl * (T::KT / 2) * 32;
+        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xrow, lane, acc);
+        epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
     }
 
-    static __device__ void run(const VerifyParams& p, unsigned char* smem)
-    {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        const int g = lane >> 2, t = lane & 3;
-        const int c0 = blockIdx.x * p.cps;
-        const int nch = min(p.cps, p.nchunks - c0);   // >= 1 (host guarantees)
-
-        uint4* xf = reinterpret_cast<uint4*>(smem);
-        float* corr = reinterpret_cast<float*>(smem + smem_xf_bytes(T::KT, p.cps));
-        float* rsum = corr + p.cps * T::GPC * 8;
-        float* part = rsum + (T::AFFINE ? p.cps * T::GPC * 8 : 0);
-
-        // this warp's units of TPW tiles
-        const int nunits = (p.ntiles + TPW - 1) / TPW;
-        const int ustride = gridDim.y * NW;
-        const int u0 = blockIdx.y * NW + warp;
-        const int nu = (u0 < nunits) ? (nunits - 1 - u0) / ustride + 1 : 0;
-        const int Q = nu * nch;
-
-        // Weights are read-only: start streaming before waiting on the
-        // previous kernel in the stream.
-        uint4 wb[D][TPW];
-        Side sb[D][TPW];
-        int lq = 0, lu = u0, lc = 0;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-            if (lq < Q) {
-                load_chunk(p, lu, c0 + lc, lane, wb[d], sb[d]);
-                ++lq;
-                if (++lc == nch) {
-                    lc = 0;
-                    lu += ustride;
-                }
-            }
-        }
-
-        griddep_wait();
-
-        // ---- stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order ----
-        {
-            const int kb = c0 * T::CHUNK_K;
-            const int p8 = (nch * T::CHUNK_K) / 8;      // 8-element pieces per row
-            uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
-            const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
-            for (int i = threadIdx.x; i < 8 * p8; i += NW * 32) {
-                const int m = i / p8;
-                const int k8 = (i - m * p8) * 8;
-                const int kg = kb + k8;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (m < p.M && kg < p.K) {            // K % 8 == 0: all 8 in range
-                    const uint16_t* src = X + (size_t)m * p.ldx + kg;
-                    if (p.x_vec) {
-                        v = *reinterpret_cast<const uint4*>(src);
-                    } else {
-                        v.x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
-                        v.y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
-                        v.z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
-                        v.w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
-                    }
-                }
-                const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
-                const int base = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
-                xw[base + 0] = v.x;
-                xw[base + 4] = v.y;
-                xw[base + 8] = v.z;
-                xw[base + 12] = v.w;
-            }
-        }
-        __syncthreads();
-
-        // ---- per-group corrections: init = -sum_k c_k x_k (and row sums) ----
-        {
-            const int ngr = nch * T::GPC;
-            for (int gr = warp; gr < ngr; gr += NW) {
-                const int cl = gr / T::GPC, gi = gr - cl * T::GPC;
-                float cs = 0.f, rs = 0.f;
-#pragma unroll
-                for (int ktg = 0; ktg < T::KTG; ++ktg) {
-                    const int ktc = gi * T::KTG + ktg;
-                    const int kts = cl * T::KT + ktc;
-                    const uint4 q = xf[(kts >> 1) * 32 + lane];
-                    const float2 f0 = pair_to_float2<XT>((kts & 1) ? q.z : q.x);
-                    const float2 f1 = pair_to_float2<XT>((kts & 1) ? q.w : q.y);
-                    const int ktl = ktc % (T::KT / 2);
-                    const float s0 = f0.x + f0.y, s1 = f1.x + f1.y;
-                    cs += slot_coef<FMT, XT>(2 * ktl) * s0 + slot_coef<FMT, XT>(2 * ktl + 1) * s1;
-                    rs += s0 + s1;
-                }
-                cs += __shfl_xor_sync(0xffffffffu, cs, 1);
-                cs += __shfl_xor_sync(0xffffffffu, cs, 2);
-                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-                if (t == 0) {
-                    if constexpr (FMT == LBV_FMT_Q4_0)
-                        corr[gr * 8 + g] = -(float)(dec_spec<FMT>(XT, 0).c + 8) * rs;
-                    else
-                        corr[gr * 8 + g] = -cs;
-                    if constexpr (T::AFFINE)
-                        rsum[gr * 8 + g] = rs;
-                }
-            }
-        }
-        __syncthreads();
-        griddep_launch_dependents();
-
-        // ---- main loop ----
-        float y[TPW][4];
-#pragma unroll
-        for (int tl = 0; tl < TPW; ++tl)
-            y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
-        int cu = u0, cc = 0;
-#pragma unroll 1
-        for (int q0 = 0; q0 < Q; q0 += D) {
-#pragma unroll
-            for (int d = 0; d < D; ++d) {
-                if (q0 + d < Q) {
-                    uint4 w[TPW];
-                    Side s[TPW];
-#pragma unroll
-                    for (int tl = 0; tl < TPW; ++tl) {
-                        w[tl] = wb[d][tl];
-                        s[tl] = sb[d][tl];
-                    }
-                    if (lq < Q) {
-                        load_chunk(p, lu, c0 + lc, lane, wb[d], sb[d]);
-                        ++lq;
-                        if (++lc == nch) {
-                            lc = 0;
-                            lu += ustride;
-                        }
-                    }
-                    process_chunk(w, s, cc, xf, corr, rsum, y, lane);
-                    if (++cc == nch) {
-                        if (p.splits == 1)
-                            store_y(p, cu, y, g, t);
-                        else
-                            store_part(part, warp, y, lane);
-#pragma unroll
-                        for (int tl = 0; tl < TPW; ++tl)
-                            y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
-                        cc = 0;
-                        cu += ustride;
-                    }
-                }
-            }
-        }
-
-        if (p.splits > 1)
-            cluster_reduce(p, part);
-    }
-
-    static __device__ __forceinline__ void store_y(const VerifyParams& p, int unit,
-                                                   const float (&y)[TPW][4], int g, int t)
+    static __device__ __forceinline__ void store_unit(const VerifyParams& p, int t1, int tile0,
+                                                      const float (&y)[TPW][4], int g, int t,
+                                                      float* part, int tbase, int lane)
     {
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
-            const int tile = unit * TPW + tl;
-            if (tile >= p.ntiles)
+            const int tile = tile0 + tl;
+            if (tile >= t1)
                 continue;
+            if (p.splits > 1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    part[(tile - tbase) * 128 + j * 32 + lane] = y[tl][j];
+                continue;
+            }
             const int n0 = tile * 16 + g, n1 = n0 + 8;
             const int m0 = 2 * t, m1 = 2 * t + 1;
             if (m0 < p.M) {
@@ -541,37 +460,242 @@ struct VerifyKernel {
         }
     }
 
-    static __device__ __forceinline__ void store_part(float* part, int warp,
-                                                      const float (&y)[TPW][4], int lane)
+    // Stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order (rows >= M
+    // and K >= p.K are zero).
+    static __device__ __forceinline__ void stage_x(const VerifyParams& p, uint4* xf, int c0,
+                                                   int nch)
     {
+        const int kb = c0 * T::CHUNK_K;
+        const int p8 = (nch * T::CHUNK_K) / 8;   // 8-element pieces per row
+        uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
+        const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
+        for (int i = threadIdx.x; i < 8 * p8; i += NW * 32) {
+            const int m = i / p8;
+            const int k8 = (i - m * p8) * 8;
+            const int kg = kb + k8;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (m < p.M && kg < p.K) {             // K % 8 == 0: all 8 in range
+                const uint16_t* src = X + (size_t)m * p.ldx + kg;
+                if (p.x_vec) {
+                    v = *reinterpret_cast<const uint4*>(src);
+                } else {
+                    v.x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
+                    v.y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
+                    v.z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
+                    v.w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
+                }
+            }
+            const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
+            const int base = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
+            xw[base + 0] = v.x;
+            xw[base + 4] = v.y;
+            xw[base + 8] = v.z;
+            xw[base + 12] = v.w;
+        }
+    }
+
+    // Per-group corrections of the slice, one warp per chunk:
+    //   corr = -sum_k c_k x_k (Q4_0: -(c + 8) * rowsum), rsum = rowsum.
+    template <int... KP>
+    static __device__ __forceinline__ void corr_pairs(std::integer_sequence<int, KP...>,
+                                                      const uint4* xrow, int lane,
+                                                      float (&cs)[T::GPC], float (&rs)[T::GPC])
+    {
+        (
+            [&] {
+                constexpr int kt0 = 2 * KP;
+                const uint4 q = xrow[KP * 32 + lane];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kt = kt0 + e;                       // folds after unrolling
+                    const float2 f0 = pair_to_float2<XT>(e ? q.z : q.x);
+                    const float2 f1 = pair_to_float2<XT>(e ? q.w : q.y);
+                    const float s0 = f0.x + f0.y, s1 = f1.x + f1.y;
+                    const int ktl = kt % (T::KT / 2);
+                    const int gi = kt / T::KTG;
+                    cs[gi] += coef(2 * ktl) * s0 + coef(2 * ktl + 1) * s1;
+                    rs[gi] += s0 + s1;
+                }
+            }(),
+            ...);
+    }
+
+    static __device__ __forceinline__ float coef(int s)
+    {
+        // s is a constant after unrolling; the chain folds to one value.
+        float c = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i == s)
+                c = (float)dec_spec<FMT>(XT, i).c;
+        return c;
+    }
+
+    static __device__ __forceinline__ void corrections(uint4* xf, float* corr, float* rsum,
+                                                       int nch, int warp, int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        for (int cl = warp; cl < nch; cl += NW) {
+            float cs[T::GPC], rs[T::GPC];
+#pragma unroll
+            for (int i = 0; i < T::GPC; ++i)
+                cs[i] = rs[i] = 0.f;
+            corr_pairs(std::make_integer_sequence<int, T::KT / 2>{},
+                       xf + (size_t)cl * (T::KT / 2) * 32, lane, cs, rs);
+#pragma unroll
+            for (int i = 0; i < T::GPC; ++i) {
+                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 1);
+                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 2);
+                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+                if (t == 0) {
+                    const int gr = cl * T::GPC + i;
+                    if constexpr (FMT == LBV_FMT_Q4_0)
+                        corr[gr * 8 + g] = -(float)(dec_spec<FMT>(XT, 0).c + 8) * rs[i];
+                    else
+                        corr[gr * 8 + g] = -cs[i];
+                    if constexpr (T::AFFINE)
+                        rsum[gr * 8 + g] = rs[i];
+                }
+            }
+        }
+    }
+
+    static __device__ void run(const VerifyParams& p, unsigned char* smem)
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int g = lane >> 2, t = lane & 3;
+        const int S = p.splits;
+        const int c0 = blockIdx.x * p.cps;
+        const int nch = min(p.cps, p.nchunks - c0);          // >= 1 (host guarantees)
+        const int t0 = (int)(((long long)p.ntiles * blockIdx.y) / gridDim.y);
+        const int t1 = (int)(((long long)p.ntiles * (blockIdx.y + 1)) / gridDim.y);
+
+        unsigned char* ring = smem;
+        unsigned char* bars = ring + G::RING_B;
+        uint4* xf = reinterpret_cast<uint4*>(bars + G::BAR_B);
+        float* corr = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xf) +
+                                               (size_t)p.cps * T::KT * 256u);
+        float* rsum = corr + p.cps * T::GPC * 8;
+        float* part = corr + p.cps * T::GPC * 8 * G::CORR_ARRAYS;
+
+        const uint32_t ring_w = smem_u32(ring) + warp * STAGES * G::SLOT_B;
+        const uint32_t bars_w = smem_u32(bars) + warp * STAGES * 8;
+        const unsigned char* ring_wp = ring + (size_t)warp * STAGES * G::SLOT_B;
+
+        // this warp's units of TPW tiles within [t0, t1)
+        const int nunits = (t1 - t0 + TPW - 1) / TPW;
+        const int nu = warp < nunits ? (nunits - 1 - warp) / NW + 1 : 0;
+        const int Q = nu * nch;
+
+        if (lane == 0) {
+#pragma unroll 1
+            for (int s = 0; s < STAGES; ++s)
+                mbar_init(bars_w + s * 8, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+
+        // Packed weights are read-only: start streaming before waiting on the
+        // previous kernel in the stream.
+        int lq = 0, lu = warp, lc = 0;                        // load cursor
+#pragma unroll 1
+        for (int s = 0; s < STAGES && lq < Q; ++s) {
+            if (lane == 0)
+                issue(p, t0, t1, lu, c0 + lc, ring_w, bars_w, s);
+            ++lq;
+            if (++lc == nch) {
+                lc = 0;
+                lu += NW;
+            }
+        }
+
+        griddep_wait();
+        stage_x(p, xf, c0, nch);
+        __syncthreads();
+        corrections(xf, corr, rsum, nch, warp, lane);
+        __syncthreads();
+        griddep_launch_dependents();
+
+        float y[TPW][4];
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl)
+            y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
+        int cu = warp, cc = 0;                                // compute cursor
+        bool ok = true;
+        int q = 0;
+#pragma unroll 1
+        for (; q < Q; ++q) {
+            const int slot = q % STAGES;
+            if (!mbar_wait(bars_w + slot * 8, (uint32_t)((q / STAGES) & 1))) {
+                ok = false;
+                break;
+            }
+            uint4 w[TPW];
+            uint32_t sd[TPW][T::SIDE_W];
+            const unsigned char* src = ring_wp + slot * G::SLOT_B;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                part[((warp * TPW + tl) * 4 + j) * 32 + lane] = y[tl][j];
+            for (int tl = 0; tl < TPW; ++tl) {
+                w[tl] = reinterpret_cast<const uint4*>(src + tl * 512)[lane];
+                const uint32_t* sp = reinterpret_cast<const uint32_t*>(
+                    src + TPW * 512 + tl * 8 * G::SIDE_B + g * G::SIDE_B);
+#pragma unroll
+                for (int i = 0; i < T::SIDE_W; ++i)
+                    sd[tl][i] = sp[i];
+            }
+            __syncwarp();
+            if (lq < Q) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue(p, t0, t1, lu, c0 + lc, ring_w, bars_w, slot);
+                }
+                ++lq;
+                if (++lc == nch) {
+                    lc = 0;
+                    lu += NW;
+                }
+            }
+            process_chunk(w, sd, cc, xf, corr, rsum, y, lane);
+            if (++cc == nch) {
+                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane);
+#pragma unroll
+                for (int tl = 0; tl < TPW; ++tl)
+                    y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
+                cc = 0;
+                cu += NW;
+            }
+        }
+        if (!ok) {
+            if (lane == 0)
+                atomicOr(p.err, 1u);
+            // let the copies already issued into this warp's ring land
+            for (int r = q; r < lq; ++r)
+                mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
+        }
+
+        if (S > 1)
+            cluster_reduce(p, part, t0, t1);
     }
 
     // Sum the K-slice partials of the cluster's CTAs in rank order 0..S-1 and
-    // write Y; each CTA writes 1/S of the block's outputs.
-    static __device__ void cluster_reduce(const VerifyParams& p, float* part)
+    // write Y; CTA rank r writes the r-th share of the cluster's tiles.
+    static __device__ void cluster_reduce(const VerifyParams& p, float* part, int t0, int t1)
     {
         cg::cluster_group cl = cg::this_cluster();
         cl.sync();
         const int S = p.splits;
-        const int V = NW * TPW * 4 * 32;
-        const int per = (V + S - 1) / S;
+        const int E = (t1 - t0) * 128;
         const int rank = (int)cl.block_rank();
-        const int vend = min(V, (rank + 1) * per);
-        for (int v = rank * per + (int)threadIdx.x; v < vend; v += NW * 32) {
+        const int e0 = (int)(((long long)E * rank) / S), e1 = (int)(((long long)E * (rank + 1)) / S);
+        for (int e = e0 + (int)threadIdx.x; e < e1; e += NW * 32) {
             float acc = 0.f;
-            for (int q = 0; q < S; ++q)
-                acc += cl.map_shared_rank(part, q)[v];
-            const int ln = v & 31, j = (v >> 5) & 3, wt = v >> 7;   // wt = warp*TPW + tl
-            const int w_ = wt / TPW, tl = wt - w_ * TPW;
-            const int tile = (blockIdx.y * NW + w_) * TPW + tl;
+            for (int r = 0; r < S; ++r)
+                acc += cl.map_shared_rank(part, r)[e];
+            const int tile = t0 + (e >> 7);
+            const int j = (e >> 5) & 3, ln = e & 31;
             const int n = tile * 16 + (ln >> 2) + 8 * (j >> 1);
             const int m = 2 * (ln & 3) + (j & 1);
-            if (tile < p.ntiles && n < p.N && m < p.M)
+            if (n < p.N && m < p.M)
                 p.Y[(size_t)m * p.ldy + n] = acc;
         }
         cl.sync();
@@ -579,33 +703,58 @@ struct VerifyKernel {
 };
 
 template <int FMT, int XT, int GROUP, int NW, int TPW>
-__global__ void __launch_bounds__(NW * 32) lbv_verify_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(NW * 32, 2) lbv_verify_kernel(const VerifyParams p)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem);
 }
 
 // ---------------------------------------------------------------------------
-// Host side: launch / smem / occupancy for one (FMT, XT, GROUP)
-
-template <int FMT, int GROUP>
-inline size_t smem_bytes_t(int warps, int tpw, int cps)
-{
-    using T = Traits<FMT, GROUP>;
-    size_t b = smem_xf_bytes(T::KT, cps);
-    b += (size_t)cps * T::GPC * 8 * sizeof(float) * (T::AFFINE ? 2 : 1);
-    b += (size_t)warps * tpw * 4 * 32 * sizeof(float);
-    return b;
-}
+// Host side: launch / smem / cluster occupancy for one (FMT, XT, GROUP)
 
 template <int FMT, int XT, int GROUP>
 inline void* kernel_ptr(int warps, int tpw)
 {
-    if (warps == 4 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 4, 1>;
-    if (warps == 4 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 4, 2>;
     if (warps == 8 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 1>;
     if (warps == 8 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 2>;
+    if (warps == 16 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 1>;
+    if (warps == 16 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 2>;
     return nullptr;
+}
+
+template <int FMT, int GROUP>
+inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits)
+{
+    if (warps == 8 && tpw == 1) return smem_bytes_for<FMT, GROUP, 8, 1>(cps, tiles_max, splits);
+    if (warps == 8 && tpw == 2) return smem_bytes_for<FMT, GROUP, 8, 2>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 1) return smem_bytes_for<FMT, GROUP, 16, 1>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 2) return smem_bytes_for<FMT, GROUP, 16, 2>(cps, tiles_max, splits);
+    return (size_t)1 << 40;
+}
+
+inline void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const Shape& sh,
+                        bool pdl, cudaStream_t st)
+{
+    cfg = {};
+    cfg.gridDim = dim3((unsigned)sh.splits, (unsigned)sh.ctas_n, 1u);
+    cfg.blockDim = dim3((unsigned)(sh.warps * 32), 1u, 1u);
+    cfg.dynamicSmemBytes = sh.smem;
+    cfg.stream = st;
+    unsigned na = 0;
+    if (sh.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)sh.splits;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
 }
 
 template <int FMT, int XT, int GROUP>
@@ -615,27 +764,9 @@ inline cudaError_t launch_t(const Shape& sh, const VerifyParams& p, const Launch
     void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
     if (!k)
         return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)sh.splits, (unsigned)sh.ctas_n, 1u);
-    cfg.blockDim = dim3((unsigned)(sh.warps * 32), 1u, 1u);
-    cfg.dynamicSmemBytes = sh.smem;
-    cfg.stream = st;
+    cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    unsigned na = 0;
-    if (sh.splits > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)sh.splits;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    if (o.pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
+    fill_config(cfg, attr, sh, o.pdl, st);
     void* args[] = {const_cast<VerifyParams*>(&p)};
     return cudaLaunchKernelExC(&cfg, k, args);
 }
@@ -646,24 +777,34 @@ inline cudaError_t prepare_t(const Shape& sh)
     void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
     if (!k)
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sh.smem);
-    if (e != cudaSuccess)
-        return e;
-    if (sh.splits > 1)
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    return e;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
 }
 
+// Clusters of the shape that can be resident at once (0 if none fits).
 template <int FMT, int XT, int GROUP>
-inline int occupancy_t(const Shape& sh)
+inline int max_clusters_t(const Shape& sh)
 {
     void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, sh.warps * 32, sh.smem) !=
-                  cudaSuccess)
+    if (!k || prepare_t<FMT, XT, GROUP>(sh) != cudaSuccess)
         return 0;
-    return n;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    Shape s1 = sh;
+    s1.ctas_n = 1;
+    fill_config(cfg, attr, s1, false, nullptr);
+    int n = 0;
+    if (sh.splits > 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess)
+            return 0;
+        return n;
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, sh.warps * 32, sh.smem) !=
+        cudaSuccess)
+        return 0;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return n * sms;
 }
 
 }  // namespace lbv

@@ -10,8 +10,8 @@ struct VerifyOps {
     cudaError_t (*launch)(lbv_dtype xt, const Shape& sh, const VerifyParams& p,
                           const LaunchOpts& o, cudaStream_t st);
     cudaError_t (*prepare)(lbv_dtype xt, const Shape& sh);
-    int (*occupancy)(lbv_dtype xt, const Shape& sh);
-    size_t (*smem)(int warps, int tpw, int cps);
+    int (*max_clusters)(lbv_dtype xt, const Shape& sh);
+    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits);
 };
 
 extern const VerifyOps sign1_ops;
@@ -37,15 +37,15 @@ extern const VerifyOps q4_0_ops;
         return xt == LBV_F16 ? prepare_t<FMT, LBV_F16, GROUP>(sh)                           \
                              : prepare_t<FMT, LBV_BF16, GROUP>(sh);                         \
     }                                                                                       \
-    static int NAME##_occupancy(lbv_dtype xt, const Shape& sh)                              \
+    static int NAME##_max_clusters(lbv_dtype xt, const Shape& sh)                           \
     {                                                                                       \
-        return xt == LBV_F16 ? occupancy_t<FMT, LBV_F16, GROUP>(sh)                         \
-                             : occupancy_t<FMT, LBV_BF16, GROUP>(sh);                       \
+        return xt == LBV_F16 ? max_clusters_t<FMT, LBV_F16, GROUP>(sh)                      \
+                             : max_clusters_t<FMT, LBV_BF16, GROUP>(sh);                    \
     }                                                                                       \
-    static size_t NAME##_smem(int warps, int tpw, int cps)                                  \
+    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits)       \
     {                                                                                       \
-        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps);                                   \
+        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits);                \
     }                                                                                       \
-    const VerifyOps NAME##_ops = {NAME##_launch, NAME##_prepare, NAME##_occupancy,          \
+    const VerifyOps NAME##_ops = {NAME##_launch, NAME##_prepare, NAME##_max_clusters,       \
                                   NAME##_smem};                                             \
     }

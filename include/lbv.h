@@ -154,8 +154,9 @@ LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, i
 LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_per_warp, int* splits,
                           int* ctas_n);
 
-/* Overrides the few-row launch shape (warps in {4, 8}, tiles_per_warp in
- * {1, 2}, splits in 1..8, ctas_n >= 1 or 0 for automatic).  Returns
+/* Overrides the few-row launch shape (warps in {8, 16}, tiles_per_warp in
+ * {1, 2}, splits in 1..8, ctas_n = clusters along N >= 1, or 0 for as many
+ * as can be resident).  Returns
  * LBV_ERR_UNSUPPORTED if the shape does not fit the device (shared memory).
  * For tuning sweeps; not thread-safe against concurrent verify calls. */
 LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_warp, int splits,
@@ -167,6 +168,12 @@ LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_w
  * LBV_PLAN_MEASURE.  Any output may be NULL. */
 LBV_API lbv_status lbv_plan_measured(const lbv_plan* plan, int M, float* fewrow_us, float* gemv_us,
                              int* crossover);
+
+/* Reads (and clears) the plan's device status word: LBV_ERR_TIMEOUT if a
+ * verify kernel of this plan gave up a bounded wait for its weight copies
+ * since the last check (its output is then incomplete), else LBV_OK.
+ * Synchronises with the device. */
+LBV_API lbv_status lbv_plan_device_status(const lbv_plan* plan);
 
 /* ------------------------------------------------------------------------ */
 /* The verify matmul.                                                         */

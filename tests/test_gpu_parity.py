@@ -61,6 +61,7 @@ class Case:
         Y = torch.full((8, self.N), float(SENTINEL), dtype=torch.float32, device="cuda")
         lbv.verify_gemm(plan or self.plan, self.X if X is None else X, M, self.Wp, Y)
         torch.cuda.synchronize()
+        (plan or self.plan).device_status()
         return Y.cpu().numpy()
 
     def check(self, Y, M):
@@ -100,7 +101,7 @@ def test_tiny_1bit_seed0_every_shape():
     K split): all within tolerance, each shape deterministic."""
     c = Case(synth.SIGN1_G128, 512, 256, 128, "f16", seed=0)
     seen = 0
-    for warps in (4, 8):
+    for warps in (8, 16):
         for tpw in (1, 2):
             for splits in (1, 2):
                 c.plan.set_shape(warps, tpw, splits)
@@ -119,14 +120,18 @@ def test_tiny_1bit_seed0_every_shape():
     (synth.Q4_0, 1280, 80, 32, "f16")])
 def test_split_k_shapes(fmtname, K, N, group, xdtype):
     c = Case(fmtname, K, N, group, xdtype, seed=3)
+    tried = 0
     for splits in (1, 2, 3, 4, 5, 8):
-        for warps, tpw in ((8, 1), (4, 2)):
-            try:
-                c.plan.set_shape(warps, tpw, splits)
-            except lbv.LbvError:
-                continue
-            for M in (2, 8):
-                c.check(c.run(M), M)
+        for ctas in (0, 1, 3):
+            for warps, tpw in ((16, 1), (8, 2), (16, 2)):
+                try:
+                    c.plan.set_shape(warps, tpw, splits, ctas)
+                except lbv.LbvError:
+                    continue
+                tried += 1
+                for M in (2, 8):
+                    c.check(c.run(M), M)
+    assert tried >= 20
 
 
 def test_row_and_M_independence_bitwise():

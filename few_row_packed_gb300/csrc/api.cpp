@@ -81,11 +81,14 @@ int shape_cps(const lbv::Shape& sh, int64_t nchunks)
 }
 
 constexpr size_t kSmemCap = 220 * 1024;        // per CTA, of 227 KB
+// Requesting more than half of an SM's shared memory keeps the scheduler from
+// placing two CTAs of one grid on an SM while other SMs stay empty.
+constexpr size_t kSmemOnePerSm = 116 * 1024;
 
 // Bytes per (tile, chunk) of the device layout and X bytes per chunk staged.
 size_t tile_chunk_bytes(const lbv_plan* P)
 {
-    return 512u + 8u * (size_t)P->fi.side_bytes;
+    return P->layout.rec_bytes;
 }
 
 // Fills sh.splits (clamped), sh.ctas_n and sh.smem for a (warps, tpw,
@@ -103,7 +106,7 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
         G = std::min<int64_t>(G, ctas_req);
     for (int it = 0; it < 4; ++it) {
         const int tiles_max = (int)((ntiles + G - 1) / G);
-        sh.smem = ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits);
+        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits), kSmemOnePerSm);
         if (sh.smem > kSmemCap)
             return false;
         sh.ctas_n = (int)G;
@@ -116,25 +119,28 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
             return true;
         G = maxc;
     }
-    sh.smem = ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits);
+    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits),
+                       kSmemOnePerSm);
     sh.ctas_n = (int)G;
     return ops->prepare(P->xdtype, sh) == cudaSuccess;
 }
 
-// Default launch shape: 16 warps, one tile per warp unit; the K split that
-// minimises the bytes one CTA streams (its tile range times its slice) plus
-// half the activation bytes it stages.
+// Default launch shape: 16 warps of two-tile units; the K split that
+// minimises what the busiest warp of a CTA streams (its units times the
+// slice) plus half the activation bytes the CTA stages.
 lbv::Shape default_shape(lbv_plan* P)
 {
-    lbv::Shape best = {16, 1, 1, 0, 0};
+    const int warps = 16, tpw = 2;
+    lbv::Shape best = {warps, tpw, 1, 0, 0};
     double best_cost = 1e300;
     for (int s = 1; s <= 8; ++s) {
-        lbv::Shape sh = {16, 1, s, 0, 0};
+        lbv::Shape sh = {warps, tpw, s, 0, 0};
         if (!complete_shape(P, sh, 0) || sh.splits != s)
             continue;
         const int cps = shape_cps(sh, P->layout.nchunks);
         const int64_t tmax = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
-        const double cost = (double)tmax * cps * tile_chunk_bytes(P) +
+        const int64_t umax = ((tmax + tpw - 1) / tpw + warps - 1) / warps;
+        const double cost = (double)umax * tpw * warps * cps * tile_chunk_bytes(P) +
                             0.5 * (double)cps * P->fi.chunk_k * 16.0;
         if (cost < best_cost * 0.98) {
             best_cost = cost;
@@ -190,8 +196,7 @@ lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int 
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_SIGN1_G128, 128, &fi);
     const lbv::Layout L = lbv::make_layout(fi, K, N);
-    uint32_t* codes = static_cast<uint32_t*>(out);
-    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    uint8_t* base = static_cast<uint8_t*>(out);
     const int wk = K / 32, sk = K / 128;
     auto bit = [&](int n, int k) -> uint32_t {
         if (n >= N || k >= K) return 0u;
@@ -200,6 +205,8 @@ lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int 
     for (int64_t tile = 0; tile < L.ntiles; ++tile)
         for (int64_t ch = 0; ch < L.nchunks; ++ch) {
             const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
             for (int lane = 0; lane < 32; ++lane) {
                 const int g = lane >> 2, t = lane & 3;
                 for (int wi = 0; wi < 4; ++wi) {
@@ -211,7 +218,7 @@ lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int 
                         w |= bit(n, k0) << s;
                         w |= bit(n, k0 + 1) << (16 + s);
                     }
-                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                    codes[lane * 4 + wi] = w;
                 }
             }
             for (int g = 0; g < 8; ++g)
@@ -220,7 +227,7 @@ lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int 
                         const int n = (int)tile * 16 + g + 8 * hi;
                         const int grp = (int)ch * 2 + j;
                         const bool ok = n < N && grp < sk;
-                        side[(tc * 8 + g) * 4 + 2 * j + hi] = ok ? scales[(size_t)n * sk + grp] : 0;
+                        side[g * 4 + 2 * j + hi] = ok ? scales[(size_t)n * sk + grp] : 0;
                     }
         }
     return LBV_OK;
@@ -243,8 +250,7 @@ lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_AFFINE2, group, &fi);
     const lbv::Layout L = lbv::make_layout(fi, K, N);
-    uint32_t* codes = static_cast<uint32_t*>(out);
-    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    uint8_t* base = static_cast<uint8_t*>(out);
     const int wk = K / 16, gk = K / group, gpc = 128 / group;
     auto code = [&](int n, int k) -> uint32_t {
         if (n >= N || k >= K) return 0u;
@@ -253,6 +259,8 @@ lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
     for (int64_t tile = 0; tile < L.ntiles; ++tile)
         for (int64_t ch = 0; ch < L.nchunks; ++ch) {
             const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
             for (int lane = 0; lane < 32; ++lane) {
                 const int g = lane >> 2, t = lane & 3;
                 for (int wi = 0; wi < 4; ++wi) {
@@ -264,7 +272,7 @@ lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
                         w |= code(n, k0) << (2 * s);
                         w |= code(n, k0 + 1) << (16 + 2 * s);
                     }
-                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                    codes[lane * 4 + wi] = w;
                 }
             }
             for (int g = 0; g < 8; ++g)
@@ -273,7 +281,7 @@ lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
                         const int n = (int)tile * 16 + g + 8 * hi;
                         const int grp = (int)ch * gpc + j;
                         const bool ok = n < N && grp < gk;
-                        uint16_t* e = side + (tc * 8 + g) * (4 * gpc) + 4 * j;
+                        uint16_t* e = side + g * (4 * gpc) + 4 * j;
                         e[hi] = ok ? scales[(size_t)n * gk + grp] : 0;
                         e[2 + hi] = ok ? biases[(size_t)n * gk + grp] : 0;
                     }
@@ -294,8 +302,7 @@ lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t 
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_Q4_0, 32, &fi);
     const lbv::Layout L = lbv::make_layout(fi, K, N);
-    uint32_t* codes = static_cast<uint32_t*>(out);
-    uint16_t* side = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + L.side_offset);
+    uint8_t* base = static_cast<uint8_t*>(out);
     const int nb = K / 32;
     auto nib = [&](int n, int k) -> uint32_t {
         if (n >= N || k >= K) return 0u;
@@ -306,6 +313,8 @@ lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t 
     for (int64_t tile = 0; tile < L.ntiles; ++tile)
         for (int64_t ch = 0; ch < L.nchunks; ++ch) {
             const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
             for (int lane = 0; lane < 32; ++lane) {
                 const int g = lane >> 2, t = lane & 3;
                 for (int wi = 0; wi < 4; ++wi) {
@@ -317,7 +326,7 @@ lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t 
                         w |= nib(n, k0) << (4 * s);
                         w |= nib(n, k0 + 1) << (16 + 4 * s);
                     }
-                    codes[(tc * 32 + lane) * 4 + wi] = w;
+                    codes[lane * 4 + wi] = w;
                 }
             }
             for (int g = 0; g < 8; ++g)
@@ -330,7 +339,7 @@ lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t 
                             const uint8_t* blk = blocks + ((size_t)n * nb + b) * 18;
                             d = (uint16_t)(blk[0] | (blk[1] << 8));
                         }
-                        side[(tc * 8 + g) * 4 + 2 * j + hi] = d;
+                        side[g * 4 + 2 * j + hi] = d;
                     }
         }
     return LBV_OK;
@@ -466,7 +475,9 @@ lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int c
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: plan is NULL");
-    if ((warps != 8 && warps != 16) || (tpw != 1 && tpw != 2) || splits < 1 || splits > 8 ||
+    const bool shape_ok = (warps == 8 && (tpw == 2 || tpw == 4)) ||
+                          (warps == 16 && (tpw == 1 || tpw == 2));
+    if (!shape_ok || splits < 1 || splits > 8 ||
         ctas_n < 0)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: warps=%d tpw=%d splits=%d ctas_n=%d",
                     warps, tpw, splits, ctas_n);
@@ -511,8 +522,7 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
 {
     lbv::VerifyParams p;
     p.X = X;
-    p.codes = static_cast<const uint4*>(Wp);
-    p.side = static_cast<const uint8_t*>(Wp) + P->layout.side_offset;
+    p.W = static_cast<const uint8_t*>(Wp);
     p.Y = Y;
     p.ldx = ldx;
     p.ldy = ldy;
@@ -525,6 +535,7 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.cps = shape_cps(P->shape, P->layout.nchunks);
     p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
     p.err = P->dev_err;
+    p.zero = 0;
     return p;
 }
 
@@ -591,8 +602,7 @@ lbv_status lbv_dequant_fp16(const lbv_plan* P, const void* Wp, uint16_t* W, lbv_
     if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0 || (reinterpret_cast<uintptr_t>(W) & 1u))
         return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: misaligned pointer");
     cudaError_t e = lbv::launch_dequant(
-        P->fmt, P->group, static_cast<const uint4*>(Wp),
-        static_cast<const uint8_t*>(Wp) + P->layout.side_offset, P->K, P->N,
+        P->fmt, P->group, static_cast<const uint8_t*>(Wp), P->K, P->N,
         (int)P->layout.ntiles, (int)P->layout.nchunks, W, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "lbv_dequant_fp16: launch");
@@ -683,12 +693,10 @@ lbv_status lbv_plan_measure_internal(lbv_plan* P)
     // 1) few-row launch shape
     lbv::Shape best = P->shape;
     float best_us = 1e30f;
-    const int warps_c[] = {8, 16};
-    const int tpw_c[] = {1, 2};
-    for (int w : warps_c)
-        for (int t : tpw_c)
+    const int shapes_c[][2] = {{8, 2}, {8, 4}, {16, 1}, {16, 2}};
+    for (const auto& wt : shapes_c)
             for (int sp = 1; sp <= 8; ++sp) {
-                lbv::Shape sh = {w, t, sp, 0, 0};
+                lbv::Shape sh = {wt[0], wt[1], sp, 0, 0};
                 if (!complete_shape(P, sh, 0) || sh.splits != sp)
                     continue;
                 P->shape = sh;

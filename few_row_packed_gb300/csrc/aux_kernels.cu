@@ -103,14 +103,17 @@ struct AuxTraits;
 template <>
 struct AuxTraits<LBV_FMT_SIGN1_G128, 128> {
     static constexpr int CK = 256, KT = 16, W = 1, SLOTS = 16, GK = 128, SIDE_W = 2;
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 template <int G>
 struct AuxTraits<LBV_FMT_AFFINE2, G> {
     static constexpr int CK = 128, KT = 8, W = 2, SLOTS = 8, GK = G, SIDE_W = 2 * (128 / G);
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 template <>
 struct AuxTraits<LBV_FMT_Q4_0, 32> {
     static constexpr int CK = 64, KT = 4, W = 4, SLOTS = 4, GK = 32, SIDE_W = 2;
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 
 // fp16 of one scale/bias half of a side word: lo half = column g, hi = g + 8.
@@ -130,8 +133,7 @@ __device__ __forceinline__ float h2f(uint16_t b)
 // d*(q-8) exact in fp32, rounded once.
 
 template <int FMT, int GROUP>
-__global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint4* codes,
-                                                          const uint8_t* side, int K, int N,
+__global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint8_t* Wp, int K, int N,
                                                           int ntiles, int nchunks, uint16_t* W)
 {
     using A = AuxTraits<FMT, GROUP>;
@@ -143,9 +145,10 @@ __global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint4* codes,
     const long long tc = idx >> 5;
     const int tile = (int)(tc / nchunks), chunk = (int)(tc - (long long)tile * nchunks);
     const int g = lane >> 2, t = lane & 3;
-    const uint4 q = codes[idx];
+    const uint8_t* rec = Wp + (size_t)tc * A::REC;
+    const uint4 q = reinterpret_cast<const uint4*>(rec)[lane];
     const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-    const uint32_t* sw = reinterpret_cast<const uint32_t*>(side + (tc * 8 + g) * (A::SIDE_W * 4));
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
     for (int wi = 0; wi < 4; ++wi) {
         const int col = tile * 16 + g + 8 * (wi & 1);
         const int hi = wi & 1;
@@ -179,30 +182,30 @@ __global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint4* codes,
     }
 }
 
-cudaError_t launch_dequant(lbv_format fmt, int group, const uint4* codes, const uint8_t* side,
-                           int K, int N, int ntiles, int nchunks, uint16_t* W, cudaStream_t st)
+cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, int N,
+                           int ntiles, int nchunks, uint16_t* W, cudaStream_t st)
 {
     const long long total = (long long)ntiles * nchunks * 32;
     const dim3 grid((unsigned)((total + 255) / 256));
     switch (fmt) {
     case LBV_FMT_SIGN1_G128:
         lbv_dequant_kernel<LBV_FMT_SIGN1_G128, 128>
-            <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+            <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     case LBV_FMT_AFFINE2:
         if (group == 32)
             lbv_dequant_kernel<LBV_FMT_AFFINE2, 32>
-                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         else if (group == 64)
             lbv_dequant_kernel<LBV_FMT_AFFINE2, 64>
-                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         else
             lbv_dequant_kernel<LBV_FMT_AFFINE2, 128>
-                <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     case LBV_FMT_Q4_0:
         lbv_dequant_kernel<LBV_FMT_Q4_0, 32>
-            <<<grid, 256, 0, st>>>(codes, side, K, N, ntiles, nchunks, W);
+            <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     }
     return cudaGetLastError();
@@ -238,9 +241,10 @@ __global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int
     float y0 = 0.f, y1 = 0.f;                        // columns g and g + 8
     for (int chunk = 0; chunk < p.nchunks; ++chunk) {
         const size_t tc = (size_t)tile * p.nchunks + chunk;
-        const uint4 q = __ldg(p.codes + tc * 32 + lane);
+        const uint8_t* rec = p.W + tc * A::REC;
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
         const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-        const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.side + (tc * 8 + g) * (A::SIDE_W * 4));
+        const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             // k-tiles of this half, grouped by scale group

@@ -11,8 +11,7 @@ namespace lbv {
 // Parameters of one few-row verify launch (passed by value to the kernel).
 struct VerifyParams {
     const void* X;          // [M][ldx] fp16 / bf16
-    const uint4* codes;     // codes region of the device layout
-    const uint8_t* side;    // side region
+    const uint8_t* W;       // packed records [tile][chunk] (layout.h)
     float* Y;               // [M][ldy]
     unsigned* err;          // device status word of the plan (bounded waits)
     int ldx, ldy;
@@ -21,6 +20,7 @@ struct VerifyParams {
     int splits;             // K slices == cluster size along grid x
     int cps;                // chunks per slice (the last slice may be shorter)
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
+    unsigned zero;          // always 0 (keeps decode constants in registers)
 };
 
 // Launch shape of the few-row kernel.
@@ -43,8 +43,8 @@ cudaError_t launch_gemv(lbv_format fmt, lbv_dtype xt, int group, const VerifyPar
 cudaError_t launch_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dt,
                            const uint32_t* signs, cudaStream_t st);
 
-cudaError_t launch_dequant(lbv_format fmt, int group, const uint4* codes, const uint8_t* side,
-                           int K, int N, int ntiles, int nchunks, uint16_t* W, cudaStream_t st);
+cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, int N,
+                           int ntiles, int nchunks, uint16_t* W, cudaStream_t st);
 
 }  // namespace lbv
 

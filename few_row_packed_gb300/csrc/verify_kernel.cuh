@@ -73,6 +73,7 @@ struct DecSpec {
     int target;
     uint32_t base;   // 16-bit pattern, replicated into both halves
     int c;
+    int bid;         // index of `base` among the format's distinct bases
 };
 
 // 1-bit sign: value = w + c with w = +-1 (bit 1 -> +1).
@@ -81,27 +82,28 @@ struct DecSpec {
 __host__ __device__ constexpr DecSpec sign1_spec(int xt, int s)
 {
     if (xt == LBV_F16) {
-        const int sh = (s <= 4) ? 5 : (s >= 11 && s <= 13) ? -3 : 0;
+        // left shifts only: slots 0-4 -> 5-9, 11-12 -> 14-15, 13 -> 14
+        const int sh = (s <= 4) ? 5 : (s == 11 || s == 12) ? 3 : (s == 13) ? 1 : 0;
         const int j = s + sh;
-        return j == 15   ? DecSpec{sh, j, 0xBC00u, 0}
-               : j == 14 ? DecSpec{sh, j, 0x0000u, 1}
-               : j == 10 ? DecSpec{sh, j, 0x4000u, 3}
-               : j == 9  ? DecSpec{sh, j, 0x4400u, 5}
-               : j == 8  ? DecSpec{sh, j, 0x4800u, 9}
-               : j == 7  ? DecSpec{sh, j, 0x4C00u, 17}
-               : j == 6  ? DecSpec{sh, j, 0x5000u, 33}
-                         : DecSpec{sh, j, 0x5400u, 65};   // j == 5
+        return j == 15   ? DecSpec{sh, j, 0xBC00u, 0, 0}
+               : j == 14 ? DecSpec{sh, j, 0x0000u, 1, 1}
+               : j == 10 ? DecSpec{sh, j, 0x4000u, 3, 2}
+               : j == 9  ? DecSpec{sh, j, 0x4400u, 5, 3}
+               : j == 8  ? DecSpec{sh, j, 0x4800u, 9, 4}
+               : j == 7  ? DecSpec{sh, j, 0x4C00u, 17, 5}
+               : j == 6  ? DecSpec{sh, j, 0x5000u, 33, 6}
+                         : DecSpec{sh, j, 0x5400u, 65, 7};   // j == 5
     } else {
         const int sh = (s <= 1) ? 5 : (s >= 8 && s <= 13) ? -6 : 0;
         const int j = s + sh;
-        return j == 15   ? DecSpec{sh, j, 0xBF80u, 0}
-               : j == 14 ? DecSpec{sh, j, 0x0000u, 1}
-               : j == 7  ? DecSpec{sh, j, 0x4000u, 3}
-               : j == 6  ? DecSpec{sh, j, 0x4080u, 5}
-               : j == 5  ? DecSpec{sh, j, 0x4100u, 9}
-               : j == 4  ? DecSpec{sh, j, 0x4180u, 17}
-               : j == 3  ? DecSpec{sh, j, 0x4200u, 33}
-                         : DecSpec{sh, j, 0x4280u, 65};   // j == 2
+        return j == 15   ? DecSpec{sh, j, 0xBF80u, 0, 0}
+               : j == 14 ? DecSpec{sh, j, 0x0000u, 1, 1}
+               : j == 7  ? DecSpec{sh, j, 0x4000u, 3, 2}
+               : j == 6  ? DecSpec{sh, j, 0x4080u, 5, 3}
+               : j == 5  ? DecSpec{sh, j, 0x4100u, 9, 4}
+               : j == 4  ? DecSpec{sh, j, 0x4180u, 17, 5}
+               : j == 3  ? DecSpec{sh, j, 0x4200u, 33, 6}
+                         : DecSpec{sh, j, 0x4280u, 65, 7};   // j == 2
     }
 }
 
@@ -113,15 +115,15 @@ __host__ __device__ constexpr DecSpec affine2_spec(int xt, int s)
     if (xt == LBV_F16) {
         const int sh = (s <= 1) ? 4 : (s <= 4) ? 0 : -6;
         const int j = 2 * s + sh;
-        return j == 4 ? DecSpec{sh, j, 0x5400u, 64}
-               : j == 6 ? DecSpec{sh, j, 0x4C00u, 16}
-                        : DecSpec{sh, j, 0x4400u, 4};
+        return j == 4 ? DecSpec{sh, j, 0x5400u, 64, 0}
+               : j == 6 ? DecSpec{sh, j, 0x4C00u, 16, 1}
+                        : DecSpec{sh, j, 0x4400u, 4, 2};
     } else {
         const int sh = (s <= 2) ? 1 : (s <= 5) ? -5 : -11;
         const int j = 2 * s + sh;
-        return j == 1 ? DecSpec{sh, j, 0x4280u, 64}
-               : j == 3 ? DecSpec{sh, j, 0x4180u, 16}
-                        : DecSpec{sh, j, 0x4080u, 4};
+        return j == 1 ? DecSpec{sh, j, 0x4280u, 64, 0}
+               : j == 3 ? DecSpec{sh, j, 0x4180u, 16, 1}
+                        : DecSpec{sh, j, 0x4080u, 4, 2};
     }
 }
 
@@ -129,7 +131,8 @@ __host__ __device__ constexpr DecSpec affine2_spec(int xt, int s)
 //   fp16: target 4, base 64.0, c 64;  bf16: target 3, base 16.0, c 16
 __host__ __device__ constexpr DecSpec q4_0_spec(int xt, int s)
 {
-    return xt == LBV_F16 ? DecSpec{4 - 4 * s, 4, 0x5400u, 64} : DecSpec{3 - 4 * s, 3, 0x4180u, 16};
+    return xt == LBV_F16 ? DecSpec{4 - 4 * s, 4, 0x5400u, 64, 0}
+                         : DecSpec{3 - 4 * s, 3, 0x4180u, 16, 0};
 }
 
 template <int FMT>
@@ -140,18 +143,38 @@ __host__ __device__ constexpr DecSpec dec_spec(int xt, int s)
                                      : q4_0_spec(xt, s);
 }
 
+// Distinct XOR bases of a format (kept in registers: one LOP3 per decode).
+template <int FMT>
+__host__ __device__ constexpr int num_bases()
+{
+    return FMT == LBV_FMT_SIGN1_G128 ? 8 : FMT == LBV_FMT_AFFINE2 ? 3 : 1;
+}
+
+template <int FMT>
+__host__ __device__ constexpr uint32_t base_of(int xt, int bid)
+{
+    uint32_t b = 0;
+    for (int s = 0; s < 16; ++s)
+        if (dec_spec<FMT>(xt, s).bid == bid)
+            b = dec_spec<FMT>(xt, s).base;
+    return b | (b << 16);
+}
+
 template <int FMT, int XT, int S>
-__device__ __forceinline__ uint32_t decode(uint32_t w)
+__device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[num_bases<FMT>()])
 {
     constexpr DecSpec d = dec_spec<FMT>(XT, S);
     constexpr int W = Traits<FMT, FMT == LBV_FMT_SIGN1_G128 ? 128 : FMT == LBV_FMT_Q4_0 ? 32 : 64>::W;
     constexpr uint32_t field = (1u << W) - 1u;
     constexpr uint32_t mask = (field << d.target) | (field << (d.target + 16));
-    constexpr uint32_t base = d.base | (d.base << 16);
     constexpr int shl = d.shift > 0 ? (d.shift > 31 ? 31 : d.shift) : 0;
     constexpr int shr = d.shift < 0 ? (-d.shift > 31 ? 31 : -d.shift) : 0;
     const uint32_t v = shl ? (w << shl) : shr ? (w >> shr) : w;
-    return (v & mask) ^ base;
+    // (v & mask) ^ base as one LOP3 with an immediate mask: written in C, the
+    // compiler splits it into two logic operations.
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(r) : "r"(v), "n"(mask), "r"(bases[d.bid]));
+    return r;
 }
 
 
@@ -216,9 +239,62 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Cluster barrier halves: every CTA arrives once it runs; waiting on that
+// phase guarantees all peers have started before their shared memory is
+// written.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Single-lane issue without divergence: the operation runs only where
+// `pred` is nonzero.
+__device__ __forceinline__ void mbar_expect_tx_if(uint32_t pred, uint32_t bar, uint32_t bytes)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n}\n"
+                 ::"r"(pred), "r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_if(uint32_t pred, uint32_t dst, const void* src,
+                                            uint32_t bytes, uint32_t bar)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%1], [%2], %3, [%4];\n}\n"
+                 ::"r"(pred), "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_if(uint32_t pred)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q fence.proxy.async.shared::cta;\n}\n" ::"r"(pred)
+                 : "memory");
+}
+
+// One try of an mbarrier phase wait (true if the phase has completed).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // Bounded wait for phase `parity` of an mbarrier.  Returns false if it did
@@ -266,11 +342,12 @@ __device__ __forceinline__ float2 f16pair(uint32_t v)
 template <int FMT, int GROUP, int NW, int TPW>
 struct Geometry {
     using T = Traits<FMT, GROUP>;
-    static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (tile, chunk, g)
-    static constexpr int TILE_B = 512 + 8 * SIDE_B;           // bytes per tile and chunk
-    static constexpr int SLOT_B = TPW * TILE_B;               // one ring stage
-    static constexpr int STAGES_RAW = 65536 / (NW * SLOT_B);
-    static constexpr int STAGES = STAGES_RAW < 4 ? 4 : STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (record, g)
+    static constexpr int REC = 512 + 8 * SIDE_B;              // record bytes (tile, chunk)
+    static constexpr int CPS = 2;                             // chunks per ring stage
+    static constexpr int SLOT_B = TPW * CPS * REC;            // one ring stage
+    static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
+    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
     static constexpr size_t BAR_B = (size_t)NW * STAGES * 8;
     // corrections and row sums per group of the slice
@@ -288,7 +365,7 @@ __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int spl
     b += (size_t)cps * T::KT * 256u;
     b += (size_t)cps * T::GPC * 8 * 4 * G::CORR_ARRAYS;
     if (splits > 1)
-        b += (size_t)tiles_max * 512u;
+        b += (size_t)((tiles_max + splits - 1) / splits) * splits * 512u;
     return b;
 }
 
@@ -301,36 +378,55 @@ struct VerifyKernel {
     static constexpr int STAGES = G::STAGES;
     static constexpr int NSET = T::GPC >= 2 ? T::GPC : 2;   // accumulator chains per tile
 
-    // All lanes of a warp track the same cursor; lane 0 issues the copies of
-    // (unit, chunk) into ring stage `slot`.
-    static __device__ __forceinline__ void issue(const VerifyParams& p, int t0, int t1, int unit,
-                                                 int chunk, uint32_t ring_w, uint32_t bars_w,
-                                                 int slot)
+    // Load cursor of a warp: the record of its next (unit, stage), tracked
+    // incrementally by every lane; lane 0 issues.  A stage holds up to CPS
+    // consecutive chunks of each of the unit's tiles.
+    struct Cursor {
+        const uint8_t* rec;     // record (tile0, first chunk of the stage)
+        int nvalid;             // tiles of the unit inside the cluster range
+        int nc;                 // chunks in this stage
+        int unit, stage;
+    };
+
+    static __device__ __forceinline__ void cursor_set(const VerifyParams& p, int t0, int t1,
+                                                      int c0, int nch, Cursor& c)
+    {
+        const int tile0 = t0 + c.unit * TPW;
+        const int ch = c.stage * G::CPS;
+        c.rec = p.W + ((size_t)tile0 * p.nchunks + c0 + ch) * G::REC;
+        c.nvalid = min(TPW, t1 - tile0);
+        c.nc = min(G::CPS, nch - ch);
+    }
+
+    static __device__ __forceinline__ void cursor_next(const VerifyParams& p, int t0, int t1,
+                                                       int c0, int nch, int nstage, Cursor& c)
+    {
+        if (++c.stage == nstage) {
+            c.stage = 0;
+            c.unit += NW;
+        }
+        cursor_set(p, t0, t1, c0, nch, c);
+    }
+
+    static __device__ __forceinline__ void issue(const VerifyParams& p, const Cursor& c,
+                                                 uint32_t leader, uint32_t ring_w,
+                                                 uint32_t bars_w, int slot)
     {
         const uint32_t bar = bars_w + slot * 8;
         const uint32_t dst = ring_w + slot * G::SLOT_B;
-        uint32_t bytes = 0;
+        const uint32_t bytes = (uint32_t)c.nc * G::REC;
+        mbar_expect_tx_if(leader, bar, (uint32_t)c.nvalid * bytes);
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl)
-            if (t0 + unit * TPW + tl < t1)
-                bytes += G::TILE_B;
-        mbar_expect_tx(bar, bytes);
-#pragma unroll
-        for (int tl = 0; tl < TPW; ++tl) {
-            const int tile = t0 + unit * TPW + tl;
-            if (tile < t1) {
-                const size_t tc = (size_t)tile * p.nchunks + chunk;
-                bulk_g2s(dst + tl * 512, p.codes + tc * 32, 512u, bar);
-                bulk_g2s(dst + TPW * 512 + tl * 8 * G::SIDE_B, p.side + tc * 8 * G::SIDE_B,
-                         8u * G::SIDE_B, bar);
-            }
-        }
+            bulk_g2s_if(leader && tl < c.nvalid, dst + tl * G::CPS * G::REC,
+                        c.rec + (size_t)tl * p.nchunks * G::REC, bytes, bar);
     }
 
-    // One k-tile: decode the four A registers (slots 2*ktl, 2*ktl+1 of the
-    // column-g word and the column-(g+8) word of half HALF) and issue the mma.
+    static constexpr int NB = num_bases<FMT>();
+
     template <int HALF, int KTL>
     static __device__ __forceinline__ void ktile(const uint4 (&w)[TPW], uint32_t b0, uint32_t b1,
+                                                 const uint32_t (&bases)[NB],
                                                  float (&acc)[TPW][NSET][4])
     {
         constexpr int kt = HALF * (T::KT / 2) + KTL;
@@ -339,10 +435,10 @@ struct VerifyKernel {
         for (int tl = 0; tl < TPW; ++tl) {
             const uint32_t wa = HALF ? w[tl].z : w[tl].x;
             const uint32_t wb = HALF ? w[tl].w : w[tl].y;
-            const uint32_t a0 = decode<FMT, XT, 2 * KTL>(wa);
-            const uint32_t a1 = decode<FMT, XT, 2 * KTL>(wb);
-            const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa);
-            const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb);
+            const uint32_t a0 = decode<FMT, XT, 2 * KTL>(wa, bases);
+            const uint32_t a1 = decode<FMT, XT, 2 * KTL>(wb, bases);
+            const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa, bases);
+            const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb, bases);
             mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
         }
     }
@@ -352,16 +448,17 @@ struct VerifyKernel {
     template <int... P>
     static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
                                                  const uint4 (&w)[TPW], const uint4* xrow,
-                                                 int lane, float (&acc)[TPW][NSET][4])
+                                                 int lane, const uint32_t (&bases)[NB],
+                                                 float (&acc)[TPW][NSET][4])
     {
         (
             [&] {
                 const uint4 q0 = xrow[(2 * P) / 2 * 32 + lane];
                 const uint4 q1 = xrow[(T::KT / 2 + 2 * P) / 2 * 32 + lane];
-                ktile<0, 2 * P>(w, q0.x, q0.y, acc);
-                ktile<1, 2 * P>(w, q1.x, q1.y, acc);
-                ktile<0, 2 * P + 1>(w, q0.z, q0.w, acc);
-                ktile<1, 2 * P + 1>(w, q1.z, q1.w, acc);
+                ktile<0, 2 * P>(w, q0.x, q0.y, bases, acc);
+                ktile<1, 2 * P>(w, q1.x, q1.y, bases, acc);
+                ktile<0, 2 * P + 1>(w, q0.z, q0.w, bases, acc);
+                ktile<1, 2 * P + 1>(w, q1.z, q1.w, bases, acc);
             }(),
             ...);
     }
@@ -408,6 +505,7 @@ struct VerifyKernel {
                                                          int cl, const uint4* __restrict__ xf,
                                                          const float* __restrict__ corr,
                                                          const float* __restrict__ rsum,
+                                                         const uint32_t (&bases)[NB],
                                                          float (&y)[TPW][4], int lane)
     {
         const int t = lane & 3;
@@ -428,10 +526,13 @@ struct VerifyKernel {
             }
         }
         const uint4* xrow = xf + (size_t)cl * (T::KT / 2) * 32;
-        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xrow, lane, acc);
+        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xrow, lane, bases, acc);
         epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
     }
 
+    // A unit's results: straight to Y (no K split), or into the shared memory
+    // of the cluster CTA that owns the tile (K split).  Tile t0 + i belongs to
+    // rank i % S and lands in its slot [(i / S) * S + my_rank].
     static __device__ __forceinline__ void store_unit(const VerifyParams& p, int t1, int tile0,
                                                       const float (&y)[TPW][4], int g, int t,
                                                       float* part, int tbase, int lane)
@@ -442,9 +543,14 @@ struct VerifyKernel {
             if (tile >= t1)
                 continue;
             if (p.splits > 1) {
+                cg::cluster_group cl = cg::this_cluster();
+                const int S = p.splits;
+                const int i = tile - tbase;
+                float* dst = cl.map_shared_rank(part, (unsigned)(i % S)) +
+                             ((i / S) * S + (int)cl.block_rank()) * 128;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    part[(tile - tbase) * 128 + j * 32 + lane] = y[tl][j];
+                    dst[j * 32 + lane] = y[tl][j];
                 continue;
             }
             const int n0 = tile * 16 + g, n1 = n0 + 8;
@@ -465,32 +571,47 @@ struct VerifyKernel {
     static __device__ __forceinline__ void stage_x(const VerifyParams& p, uint4* xf, int c0,
                                                    int nch)
     {
+        constexpr int B = 4;                       // loads in flight per thread
         const int kb = c0 * T::CHUNK_K;
-        const int p8 = (nch * T::CHUNK_K) / 8;   // 8-element pieces per row
+        const int p8 = (nch * T::CHUNK_K) / 8;     // 8-element pieces per row
+        const int total = 8 * p8;
         uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
         const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
-        for (int i = threadIdx.x; i < 8 * p8; i += NW * 32) {
-            const int m = i / p8;
-            const int k8 = (i - m * p8) * 8;
-            const int kg = kb + k8;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (m < p.M && kg < p.K) {             // K % 8 == 0: all 8 in range
-                const uint16_t* src = X + (size_t)m * p.ldx + kg;
-                if (p.x_vec) {
-                    v = *reinterpret_cast<const uint4*>(src);
-                } else {
-                    v.x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
-                    v.y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
-                    v.z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
-                    v.w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
+        for (int i0 = threadIdx.x; i0 < total; i0 += B * NW * 32) {
+            uint4 v[B];
+            int dst[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = i0 + b * NW * 32;
+                v[b] = make_uint4(0u, 0u, 0u, 0u);
+                dst[b] = -1;
+                if (i < total) {
+                    const int m = i / p8;
+                    const int k8 = (i - m * p8) * 8;
+                    const int kg = kb + k8;
+                    if (m < p.M && kg < p.K) {     // K % 8 == 0: all 8 in range
+                        const uint16_t* src = X + (size_t)m * p.ldx + kg;
+                        if (p.x_vec) {
+                            v[b] = *reinterpret_cast<const uint4*>(src);
+                        } else {
+                            v[b].x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
+                            v[b].y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
+                            v[b].z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
+                            v[b].w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
+                        }
+                    }
+                    const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
+                    dst[b] = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
                 }
             }
-            const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
-            const int base = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
-            xw[base + 0] = v.x;
-            xw[base + 4] = v.y;
-            xw[base + 8] = v.z;
-            xw[base + 12] = v.w;
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                if (dst[b] >= 0) {
+                    xw[dst[b] + 0] = v[b].x;
+                    xw[dst[b] + 4] = v[b].y;
+                    xw[dst[b] + 8] = v[b].z;
+                    xw[dst[b] + 12] = v[b].w;
+                }
         }
     }
 
@@ -568,8 +689,8 @@ struct VerifyKernel {
         const int S = p.splits;
         const int c0 = blockIdx.x * p.cps;
         const int nch = min(p.cps, p.nchunks - c0);          // >= 1 (host guarantees)
-        const int t0 = (int)(((long long)p.ntiles * blockIdx.y) / gridDim.y);
-        const int t1 = (int)(((long long)p.ntiles * (blockIdx.y + 1)) / gridDim.y);
+        const int t0 = (int)(((unsigned)p.ntiles * blockIdx.y) / gridDim.y);
+        const int t1 = (int)(((unsigned)p.ntiles * (blockIdx.y + 1)) / gridDim.y);
 
         unsigned char* ring = smem;
         unsigned char* bars = ring + G::RING_B;
@@ -586,8 +707,9 @@ struct VerifyKernel {
         // this warp's units of TPW tiles within [t0, t1)
         const int nunits = (t1 - t0 + TPW - 1) / TPW;
         const int nu = warp < nunits ? (nunits - 1 - warp) / NW + 1 : 0;
-        const int Q = nu * nch;
 
+        if (S > 1)
+            cluster_arrive_relaxed();
         if (lane == 0) {
 #pragma unroll 1
             for (int s = 0; s < STAGES; ++s)
@@ -596,18 +718,29 @@ struct VerifyKernel {
         }
         __syncwarp();
 
+        // XOR bases in registers: opaque values cannot be folded back into
+        // immediates, so each decode stays one LOP3.
+        uint32_t bases[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+            asm volatile("mov.b32 %0, %1;\n" : "=r"(bases[i]) : "r"(base_of<FMT>(XT, i)));
+
         // Packed weights are read-only: start streaming before waiting on the
         // previous kernel in the stream.
-        int lq = 0, lu = warp, lc = 0;                        // load cursor
+        const int nstage = (nch + G::CPS - 1) / G::CPS;
+        const int Q = nu * nstage;
+        const uint32_t leader = lane == 0;
+        Cursor lcur;
+        lcur.unit = warp;
+        lcur.stage = 0;
+        cursor_set(p, t0, t1, c0, nch, lcur);
+        int lq = 0;
+        const int npre = min(STAGES, Q);
 #pragma unroll 1
-        for (int s = 0; s < STAGES && lq < Q; ++s) {
-            if (lane == 0)
-                issue(p, t0, t1, lu, c0 + lc, ring_w, bars_w, s);
+        for (int st = 0; st < npre; ++st) {
+            issue(p, lcur, leader, ring_w, bars_w, st);
             ++lq;
-            if (++lc == nch) {
-                lc = 0;
-                lu += NW;
-            }
+            cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
 
         griddep_wait();
@@ -615,6 +748,8 @@ struct VerifyKernel {
         __syncthreads();
         corrections(xf, corr, rsum, nch, warp, lane);
         __syncthreads();
+        if (S > 1)
+            cluster_wait();            // all peers run: their partial buffers are live
         griddep_launch_dependents();
 
         float y[TPW][4];
@@ -623,40 +758,46 @@ struct VerifyKernel {
             y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
         int cu = warp, cc = 0;                                // compute cursor
         bool ok = true;
-        int q = 0;
+        int q = 0, slot = 0;
+        uint32_t parity = 0;
 #pragma unroll 1
         for (; q < Q; ++q) {
-            const int slot = q % STAGES;
-            if (!mbar_wait(bars_w + slot * 8, (uint32_t)((q / STAGES) & 1))) {
+            const uint32_t bar = bars_w + slot * 8;
+            if (!mbar_try(bar, parity) && !mbar_wait(bar, parity)) {
                 ok = false;
                 break;
             }
-            uint4 w[TPW];
-            uint32_t sd[TPW][T::SIDE_W];
+            const int nc = min(G::CPS, nch - cc);
+            uint4 w[G::CPS][TPW];
+            uint32_t sd[G::CPS][TPW][T::SIDE_W];
             const unsigned char* src = ring_wp + slot * G::SLOT_B;
 #pragma unroll
-            for (int tl = 0; tl < TPW; ++tl) {
-                w[tl] = reinterpret_cast<const uint4*>(src + tl * 512)[lane];
-                const uint32_t* sp = reinterpret_cast<const uint32_t*>(
-                    src + TPW * 512 + tl * 8 * G::SIDE_B + g * G::SIDE_B);
+            for (int ci = 0; ci < G::CPS; ++ci)
 #pragma unroll
-                for (int i = 0; i < T::SIDE_W; ++i)
-                    sd[tl][i] = sp[i];
-            }
+                for (int tl = 0; tl < TPW; ++tl) {
+                    const unsigned char* r = src + (tl * G::CPS + ci) * G::REC;
+                    w[ci][tl] = reinterpret_cast<const uint4*>(r)[lane];
+                    const uint32_t* sp = reinterpret_cast<const uint32_t*>(r + 512 + g * G::SIDE_B);
+#pragma unroll
+                    for (int i = 0; i < T::SIDE_W; ++i)
+                        sd[ci][tl][i] = sp[i];
+                }
             __syncwarp();
             if (lq < Q) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    issue(p, t0, t1, lu, c0 + lc, ring_w, bars_w, slot);
-                }
+                fence_proxy_async_if(leader);
+                issue(p, lcur, leader, ring_w, bars_w, slot);
                 ++lq;
-                if (++lc == nch) {
-                    lc = 0;
-                    lu += NW;
-                }
+                cursor_next(p, t0, t1, c0, nch, nstage, lcur);
             }
-            process_chunk(w, sd, cc, xf, corr, rsum, y, lane);
-            if (++cc == nch) {
+            if (++slot == STAGES) {
+                slot = 0;
+                parity ^= 1u;
+            }
+            process_chunk(w[0], sd[0], cc, xf, corr, rsum, bases, y, lane);
+            if (nc > 1)
+                process_chunk(w[1], sd[1], cc + 1, xf, corr, rsum, bases, y, lane);
+            cc += nc;
+            if (cc == nch) {
                 store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane);
 #pragma unroll
                 for (int tl = 0; tl < TPW; ++tl)
@@ -677,33 +818,33 @@ struct VerifyKernel {
             cluster_reduce(p, part, t0, t1);
     }
 
-    // Sum the K-slice partials of the cluster's CTAs in rank order 0..S-1 and
-    // write Y; CTA rank r writes the r-th share of the cluster's tiles.
+    // After the cluster barrier each CTA sums, in rank order 0..S-1, the
+    // partials its cluster peers stored for the tiles it owns, and writes Y.
     static __device__ void cluster_reduce(const VerifyParams& p, float* part, int t0, int t1)
     {
         cg::cluster_group cl = cg::this_cluster();
         cl.sync();
         const int S = p.splits;
-        const int E = (t1 - t0) * 128;
         const int rank = (int)cl.block_rank();
-        const int e0 = (int)(((long long)E * rank) / S), e1 = (int)(((long long)E * (rank + 1)) / S);
-        for (int e = e0 + (int)threadIdx.x; e < e1; e += NW * 32) {
+        const int nown = (t1 - t0 - rank + S - 1) / S;        // tiles t0 + rank + S*k
+        for (int e = (int)threadIdx.x; e < nown * 128; e += NW * 32) {
+            const int k = e >> 7, r = e & 127;
+            const float* src = part + (k * S) * 128 + r;
             float acc = 0.f;
-            for (int r = 0; r < S; ++r)
-                acc += cl.map_shared_rank(part, r)[e];
-            const int tile = t0 + (e >> 7);
-            const int j = (e >> 5) & 3, ln = e & 31;
+            for (int q = 0; q < S; ++q)
+                acc += src[q * 128];
+            const int tile = t0 + rank + S * k;
+            const int j = r >> 5, ln = r & 31;
             const int n = tile * 16 + (ln >> 2) + 8 * (j >> 1);
             const int m = 2 * (ln & 3) + (j & 1);
             if (n < p.N && m < p.M)
                 p.Y[(size_t)m * p.ldy + n] = acc;
         }
-        cl.sync();
     }
 };
 
 template <int FMT, int XT, int GROUP, int NW, int TPW>
-__global__ void __launch_bounds__(NW * 32, 2) lbv_verify_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(NW * 32, 1) lbv_verify_kernel(const VerifyParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem);
@@ -715,8 +856,8 @@ __global__ void __launch_bounds__(NW * 32, 2) lbv_verify_kernel(const VerifyPara
 template <int FMT, int XT, int GROUP>
 inline void* kernel_ptr(int warps, int tpw)
 {
-    if (warps == 8 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 1>;
     if (warps == 8 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 2>;
+    if (warps == 8 && tpw == 4) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 4>;
     if (warps == 16 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 1>;
     if (warps == 16 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 2>;
     return nullptr;
@@ -725,8 +866,8 @@ inline void* kernel_ptr(int warps, int tpw)
 template <int FMT, int GROUP>
 inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits)
 {
-    if (warps == 8 && tpw == 1) return smem_bytes_for<FMT, GROUP, 8, 1>(cps, tiles_max, splits);
     if (warps == 8 && tpw == 2) return smem_bytes_for<FMT, GROUP, 8, 2>(cps, tiles_max, splits);
+    if (warps == 8 && tpw == 4) return smem_bytes_for<FMT, GROUP, 8, 4>(cps, tiles_max, splits);
     if (warps == 16 && tpw == 1) return smem_bytes_for<FMT, GROUP, 16, 1>(cps, tiles_max, splits);
     if (warps == 16 && tpw == 2) return smem_bytes_for<FMT, GROUP, 16, 2>(cps, tiles_max, splits);
     return (size_t)1 << 40;

@@ -154,8 +154,8 @@ LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, i
 LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_per_warp, int* splits,
                           int* ctas_n);
 
-/* Overrides the few-row launch shape (warps in {8, 16}, tiles_per_warp in
- * {1, 2}, splits in 1..8, ctas_n = clusters along N >= 1, or 0 for as many
+/* Overrides the few-row launch shape ((warps, tiles_per_warp) in {(8, 2),
+ * (8, 4), (16, 1), (16, 2)}, splits in 1..8, ctas_n = clusters along N >= 1, or 0 for as many
  * as can be resident).  Returns
  * LBV_ERR_UNSUPPORTED if the shape does not fit the device (shared memory).
  * For tuning sweeps; not thread-safe against concurrent verify calls. */

@@ -65,6 +65,7 @@ def test_packed_bytes_identities(L):
     assert lbv.packed_bytes(7, 128, 16, 128) == 0
     # padding: ragged N and K round up to a tile and a chunk
     assert lbv.packed_bytes(lbv.FMT_SIGN1_G128, 384, 20) == 2 * 2 * (512 + 8 * 8)
+    assert lbv.packed_bytes(lbv.FMT_AFFINE2, 96, 17, 32) == 2 * 1 * (512 + 8 * 32)
 
 
 def test_bad_arguments_return_status(L):
@@ -92,22 +93,29 @@ def test_bad_arguments_return_status(L):
 
 # ----------------------------------------------------------------------------
 # The device layout, read back from its written specification (layout.h):
-# codes[tile][chunk][lane][word]; word wi of lane (g, t) is column
+# one record per (tile, chunk) in tile-major order, 512 code bytes
+# [lane][word] then 8 x SB side bytes [g].  Word wi of lane (g, t) is column
 # 16*tile + g + 8*(wi & 1), k-tiles (wi >> 1)*KT/2 + s//2; slot s holds the
 # codes of k0 = 16*kt + 8*(s & 1) + 2*t at bit s*W and of k0+1 at 16 + s*W.
 
-SPEC = {  # chunk_k, W (bits), slots, side halves per g per chunk
+SPEC = {  # chunk_k, W (bits), slots
     lbv.FMT_SIGN1_G128: (256, 1, 16),
     lbv.FMT_AFFINE2: (128, 2, 8),
     lbv.FMT_Q4_0: (64, 4, 4),
 }
 
 
+def side_bytes(fmt, group):
+    return (128 // group) * 8 if fmt == lbv.FMT_AFFINE2 else 8
+
+
 def read_layout(fmt, packed, K, N, group):
     ck, W, slots = SPEC[fmt]
     KT = ck // 16
     ntiles, nch = -(-N // 16), -(-K // ck)
-    codes = packed[:ntiles * nch * 512].view(np.uint32).reshape(ntiles, nch, 32, 4)
+    rec = 512 + 8 * side_bytes(fmt, group)
+    recs = packed.reshape(ntiles, nch, rec)
+    codes = np.ascontiguousarray(recs[:, :, :512]).view(np.uint32).reshape(ntiles, nch, 32, 4)
     out = np.full((ntiles * 16, nch * ck), -1, np.int64)
     mask = (1 << W) - 1
     for lane in range(32):
@@ -120,7 +128,7 @@ def read_layout(fmt, packed, K, N, group):
                     k = np.arange(nch) * ck + 16 * kt + 8 * (s & 1) + 2 * t + h
                     v = (codes[:, :, lane, wi] >> np.uint32(s * W + 16 * h)) & mask
                     out[np.ix_(n, k)] = v
-    side = packed[ntiles * nch * 512:].view(np.uint16).reshape(ntiles, nch, 8, -1)
+    side = np.ascontiguousarray(recs[:, :, 512:]).view(np.uint16).reshape(ntiles, nch, 8, -1)
     return out, side
 
 

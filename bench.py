@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M=1..8 table")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override")
+    ap.add_argument("--shape", default="", help="splits[,ctas] override of the launch shape")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
     ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
@@ -383,8 +383,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
-            "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
-                      "ctas_n": shape[3]},
+            "shape": {"splits": shape[0], "clusters_n": shape[1]},
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "per_M": per_M,

@@ -68,8 +68,8 @@ def lib():
             "lbv_plan_destroy": (st, [P]),
             "lbv_plan_query": (st, [P, I, ctypes.POINTER(I), ctypes.POINTER(I),
                                     ctypes.POINTER(S)]),
-            "lbv_plan_shape": (st, [P] + [ctypes.POINTER(I)] * 4),
-            "lbv_plan_set_shape": (st, [P, I, I, I, I]),
+            "lbv_plan_shape": (st, [P] + [ctypes.POINTER(I)] * 2),
+            "lbv_plan_set_shape": (st, [P, I, I]),
             "lbv_plan_measured": (st, [P, I, ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
             "lbv_plan_device_status": (st, [P]),
@@ -203,12 +203,13 @@ class Plan:
         return k.value, s.value, w.value
 
     def shape(self):
-        v = [ctypes.c_int() for _ in range(4)]
+        """(K splits = cluster size, clusters along N) of the few-row kernel."""
+        v = [ctypes.c_int() for _ in range(2)]
         _check(lib().lbv_plan_shape(self.handle, *[ctypes.byref(x) for x in v]))
         return tuple(x.value for x in v)
 
-    def set_shape(self, warps: int, tiles_per_warp: int, splits: int, ctas_n: int = 0):
-        _check(lib().lbv_plan_set_shape(self.handle, warps, tiles_per_warp, splits, ctas_n))
+    def set_shape(self, splits: int, ctas_n: int = 0):
+        _check(lib().lbv_plan_set_shape(self.handle, splits, ctas_n))
 
     def device_status(self):
         """Raises LbvError(ERR_TIMEOUT) if a kernel of this plan gave up a

@@ -21,11 +21,11 @@ LIB = os.path.join(HERE, "liblbv.so")
 SOURCES = [
     "api.cpp",
     "aux_kernels.cu",
-    "verify_sign1.cu",
-    "verify_affine2_g32.cu",
-    "verify_affine2_g64.cu",
-    "verify_affine2_g128.cu",
-    "verify_q4_0.cu",
+    "tc_sign1.cu",
+    "tc_affine2_g32.cu",
+    "tc_affine2_g64.cu",
+    "tc_affine2_g128.cu",
+    "tc_q4_0.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",

@@ -8,6 +8,9 @@
 
 namespace lbv {
 
+// Decode warpgroups per CTA of the few-row kernel.
+constexpr int kTcWarpgroups = 4;
+
 // Parameters of one few-row verify launch (passed by value to the kernel).
 struct VerifyParams {
     const void* X;          // [M][ldx] fp16 / bf16
@@ -19,16 +22,16 @@ struct VerifyParams {
     int ntiles, nchunks;
     int splits;             // K slices == cluster size along grid x
     int cps;                // chunks per slice (the last slice may be shorter)
+    int wsplit;             // warpgroup split of a slice inside a CTA: 1, 2 or 4
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
     unsigned zero;          // always 0 (keeps decode constants in registers)
 };
 
 // Launch shape of the few-row kernel.
 struct Shape {
-    int warps;              // 8 or 16
-    int tpw;                // column tiles per warp unit, 1 or 2
     int splits;             // K slices (cluster size), 1..8
     int ctas_n;             // clusters along N (grid y); each owns a contiguous tile range
+    int wsplit;             // warpgroups sharing one tile inside a CTA (split of the slice)
     size_t smem;            // dynamic shared memory bytes
 };
 

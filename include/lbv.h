@@ -148,19 +148,15 @@ LBV_API lbv_status lbv_plan_destroy(lbv_plan* plan);
 LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, int* splits,
                           size_t* workspace_bytes);
 
-/* The plan's launch shape for the few-row kernel: warps per CTA, column tiles
- * (16 columns each) per warp, K split and CTAs along N.  For tests and
- * benchmarks; any output may be NULL. */
-LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_per_warp, int* splits,
-                          int* ctas_n);
+/* The plan's launch shape for the few-row kernel: the K split (cluster size)
+ * and the number of clusters along N.  Any output may be NULL. */
+LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* splits, int* ctas_n);
 
-/* Overrides the few-row launch shape ((warps, tiles_per_warp) in {(8, 2),
- * (8, 4), (16, 1), (16, 2)}, splits in 1..8, ctas_n = clusters along N >= 1, or 0 for as many
- * as can be resident).  Returns
- * LBV_ERR_UNSUPPORTED if the shape does not fit the device (shared memory).
- * For tuning sweeps; not thread-safe against concurrent verify calls. */
-LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_warp, int splits,
-                              int ctas_n);
+/* Overrides the few-row launch shape: splits in 1..8, ctas_n = clusters along
+ * N >= 1, or 0 for as many as can be resident.  Returns LBV_ERR_UNSUPPORTED if
+ * the shape does not fit the device.  For tuning sweeps; not thread-safe
+ * against concurrent verify calls on the same plan. */
+LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int splits, int ctas_n);
 
 /* With LBV_PLAN_MEASURE: the measured cold-L2 time (us) of the few-row kernel
  * and of the 1-row path run M times at row count M, and the crossover (the

@@ -101,9 +101,9 @@ bool fit_shape(const lbv_plan* P, lbv::Shape& sh, int cps)
     const int64_t tpc = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
     const int owned = (int)((tpc + sh.splits - 1) / sh.splits);
     int64_t best = -1;
-    for (int sw = 1; sw <= lbv::kTcWarpgroups; sw *= 2) {
-        if (sw > 1 && sw > cps)
-            break;
+    for (int sw = 1; sw <= lbv::kTcWarpgroups; ++sw) {
+        if (lbv::kTcWarpgroups % sw != 0 || (sw > 1 && sw > cps))
+            continue;
         const size_t smem = std::max(ops->smem(cps, owned, sh.splits * sw), kSmemOnePerSm);
         if (smem > kSmemCap)
             continue;

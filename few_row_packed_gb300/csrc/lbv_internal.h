@@ -9,7 +9,7 @@
 namespace lbv {
 
 // Decode warpgroups per CTA of the few-row kernel.
-constexpr int kTcWarpgroups = 4;
+constexpr int kTcWarpgroups = 3;
 
 // Parameters of one few-row verify launch (passed by value to the kernel).
 struct VerifyParams {
@@ -22,7 +22,7 @@ struct VerifyParams {
     int ntiles, nchunks;
     int splits;             // K slices == cluster size along grid x
     int cps;                // chunks per slice (the last slice may be shorter)
-    int wsplit;             // warpgroup split of a slice inside a CTA: 1, 2 or 4
+    int wsplit;             // warpgroup split of a slice inside a CTA (divides kTcWarpgroups)
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
     unsigned zero;          // always 0 (keeps decode constants in registers)
 };

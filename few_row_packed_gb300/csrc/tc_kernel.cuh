@@ -4,18 +4,21 @@
 // Design (GB300, sm_103a):
 //   * Persistent grid of thread-block clusters.  Cluster y owns a contiguous,
 //     balanced range of 128-column tiles; its S CTAs split K into slices.
-//     Inside a CTA, four decode warpgroups (one 128-column tile at a time, one
+//     Inside a CTA, three decode warpgroups (one 128-column tile at a time, one
 //     thread per weight column) take tiles round-robin and, when a CTA has
 //     fewer tiles than warpgroups, also split the slice's chunks (SW ways).
 //     The S * SW partial sums of a tile meet in the owner CTA's shared memory
 //     (distributed shared memory across the cluster) and are added in a fixed
 //     order: deterministic, no global workspace.
 //   * Each warpgroup owns a ring of shared-memory stages filled with 1-D bulk
-//     async copies of packed records (its decode warps take turns issuing the
-//     refills) and one MMA warp of its own that issues the tcgen05.mma of
-//     every A slot from converged code (elect.sync), so four issuers keep the
-//     tensor pipe fed while sixteen warps decode.  All hand-offs are
-//     mbarriers; every wait is bounded, and a wait that gives up sets the
+//     async copies of packed records (its decode warps take turns issuing
+//     the refills) and one MMA warp.  The decode warps announce each stored A
+//     slot with a non-blocking arrival on a hardware named barrier (one per A
+//     slot of the ring); the MMA warp syncs on it and issues the slot's
+//     tcgen05.mma from converged code (elect.sync).  One commit per chunk
+//     tells the decoders that the chunk's A slots are free and its
+//     accumulators ready; the decoders release accumulators through an
+//     mbarrier.  Every wait is bounded, and a wait that gives up sets the
 //     plan's status word and lets the kernel run to its end.
 //   * Decode: each thread turns its column's codes into fp16/bf16 pairs with
 //     one LOP3 per pair, (word_variant & mask) ^ base, placing a code in a
@@ -204,13 +207,20 @@ struct TcGeo {
     static constexpr int THREADS = DEC_THREADS + NWG * 32;   // + one MMA warp per warpgroup
     // ring stages per warpgroup: about 18 KB in flight each
     static constexpr int NST = REC * 8 <= 18432 ? 8 : 18432 / REC;
-    static constexpr int ND = GPC == 2 ? 4 : 2;      // accumulators (16 TMEM columns each)
-    static constexpr int NA = GPC == 2 ? 2 : 3;      // A slots (32 TMEM columns each)
-    static constexpr int TMEM_WG = NA * 32 + ND * 16;
+    static constexpr int LAG = 2;                    // the epilogue trails decode by LAG chunks
+    // accumulators (16 TMEM columns each): the epilogue's LAG chunks, the
+    // chunk being decoded, and (when they fit) one more so the MMA warp can
+    // run ahead
+    static constexpr int ND = GPC == 1 ? LAG + 2 : 2 * (LAG + 1);
+    static constexpr int TMEM_WG = 512 / NWG / 32 * 32;   // tensor-memory columns per warpgroup
+    static constexpr int NA = (TMEM_WG - ND * 16) / 32;   // A slots (32 TMEM columns each)
     static constexpr int TMEM_COLS = 512;            // allocation (>= NWG * TMEM_WG)
-    static_assert(NWG * TMEM_WG <= TMEM_COLS, "tensor memory budget");
+    static_assert(NWG * TMEM_WG <= TMEM_COLS && NA >= 2, "tensor memory budget");
     static_assert((T::CK / 64) % IU == 0, "issue units tile a chunk");
-    static constexpr int NBAR_WG = 2 * NST + 2 * NA + 2 * ND;
+    static constexpr int NCD = LAG + 2;              // chunk-done barriers (ring over chunks)
+    static_assert(IU * 64 == T::CK, "an issue unit is one chunk");
+    static constexpr int NBAR_WG = 2 * NST + NCD + ND;
+    static_assert(1 + NWG * NA <= 16, "named barriers: one per A slot of each warpgroup");
 };
 
 // Shared memory carve-up (bytes), 128-byte aligned pieces:
@@ -306,14 +316,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Bounded wait: false if the phase did not complete within about a second.
+// Bounded wait: false if the phase did not complete within about a second
+// (2^31 SM cycles; the cycle counter is cheap to read, unlike the global
+// timer).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
     if (mbar_try(bar, parity))
         return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (!mbar_try(bar, parity))
-        if (globaltimer_ns() - t0 > 1000000000ull)
+        if (clock64() - t0 > (1ll << 31))
             return false;
     return true;
 }
@@ -335,6 +347,11 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 __device__ __forceinline__ void named_bar_sync(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void cluster_arrive_relaxed()
@@ -389,19 +406,6 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&d)[8])
         d[i] = __uint_as_float(r[i]);
 }
 
-// D[128 x 16] (+)= A[128 x 16] (tensor memory) * B[16 x 16] (shared memory),
-// issued by one elected lane of a converged warp.  elect.sync picks the same
-// lane every time for a full warp, so the commits below track these MMAs.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrives on `bar` once every MMA issued so far by the elected lane has
 // completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -413,44 +417,42 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
         : "memory");
 }
 
-// The four k-steps of one A slot (A columns a, a+8, a+16, a+24; B descriptors
-// b, b+256 B, ...): k-step j accumulates into d0 (j < 2) or d1 (j >= 2) and
-// adds to it when bit j of ACC is set; then NC commits (to c0, c1, c2) -- all
-// issued by one elected lane in a single block.
-#define LBV_UMMA_SLOT_BODY                                                           \
-    "{\n .reg .pred e, p0, p1, p2, p3;\n .reg .b32 a1, a2, a3;\n .reg .b64 b1, b2, b3;\n" \
-    " setp.ne.b32 p0, %8, 0;\n setp.ne.b32 p1, %9, 0;\n"                           \
-    " setp.ne.b32 p2, %10, 0;\n setp.ne.b32 p3, %11, 0;\n"                         \
-    " add.u32 a1, %2, 8;\n add.u32 a2, %2, 16;\n add.u32 a3, %2, 24;\n"            \
-    " add.u64 b1, %3, 16;\n add.u64 b2, %3, 32;\n add.u64 b3, %3, 48;\n"           \
-    " elect.sync _|e, 0xffffffff;\n"                                               \
-    " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %4, p0;\n"              \
-    " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, p1;\n"              \
-    " @e tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, p2;\n"              \
-    " @e tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, p3;\n"
+// The four k-steps of one A slot (A tensor-memory addresses a0..a3, B
+// descriptors b0..b3, all computed by the caller so they stay warp-uniform):
+// k-step j accumulates into d0 (j < 2) or d1 (j >= 2) and adds to it when bit
+// j of ACC is set; then NC commits (to c0, c1, c2) -- all issued by one
+// elected lane in a single block.
+#define LBV_UMMA_SLOT_BODY                                                     \
+    "{\n .reg .pred e, p0, p1, p2, p3;\n"                                      \
+    " setp.ne.b32 p0, %15, 0;\n setp.ne.b32 p1, %16, 0;\n"                     \
+    " setp.ne.b32 p2, %17, 0;\n setp.ne.b32 p3, %18, 0;\n"                     \
+    " elect.sync _|e, 0xffffffff;\n"                                         \
+    " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, p0;\n"       \
+    " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, p1;\n"       \
+    " @e tcgen05.mma.cta_group::1.kind::f16 [%1], [%4], %8, %10, p2;\n"       \
+    " @e tcgen05.mma.cta_group::1.kind::f16 [%1], [%5], %9, %10, p3;\n"
 #define LBV_UMMA_COMMIT(N) \
     " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%" #N "];\n"
+#define LBV_UMMA_SLOT_ARGS                                                              \
+    "r"(d0), "r"(d1), "r"(a), "r"(a + 8u), "r"(a + 16u), "r"(a + 24u), "l"(b), "l"(b + 16u), \
+        "l"(b + 32u), "l"(b + 48u), "r"(idesc), "r"(c0), "r"(c1), "r"(c2), "r"(0u), "r"(f0),  \
+        "r"(f1), "r"(f2), "r"(f3)
 
 template <int ACC, int NC>
 __device__ __forceinline__ void umma_slot(uint32_t d0, uint32_t d1, uint32_t a, uint64_t b,
                                           uint32_t idesc, uint32_t c0, uint32_t c1, uint32_t c2)
 {
     const uint32_t f0 = ACC & 1, f1 = (ACC >> 1) & 1, f2 = (ACC >> 2) & 1, f3 = (ACC >> 3) & 1;
-    if constexpr (NC == 1)
-        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(5) "}\n"
-                     ::"r"(d0), "r"(d1), "r"(a), "l"(b), "r"(idesc), "r"(c0), "r"(c1), "r"(c2),
-                       "r"(f0), "r"(f1), "r"(f2), "r"(f3)
-                     : "memory");
+    if constexpr (NC == 0)
+        asm volatile(LBV_UMMA_SLOT_BODY "}\n" ::LBV_UMMA_SLOT_ARGS : "memory");
+    else if constexpr (NC == 1)
+        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(11) "}\n" ::LBV_UMMA_SLOT_ARGS : "memory");
     else if constexpr (NC == 2)
-        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(5) LBV_UMMA_COMMIT(6) "}\n"
-                     ::"r"(d0), "r"(d1), "r"(a), "l"(b), "r"(idesc), "r"(c0), "r"(c1), "r"(c2),
-                       "r"(f0), "r"(f1), "r"(f2), "r"(f3)
-                     : "memory");
+        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(11) LBV_UMMA_COMMIT(12) "}\n"
+                     ::LBV_UMMA_SLOT_ARGS : "memory");
     else
-        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(5) LBV_UMMA_COMMIT(6) LBV_UMMA_COMMIT(7) "}\n"
-                     ::"r"(d0), "r"(d1), "r"(a), "l"(b), "r"(idesc), "r"(c0), "r"(c1), "r"(c2),
-                       "r"(f0), "r"(f1), "r"(f2), "r"(f3)
-                     : "memory");
+        asm volatile(LBV_UMMA_SLOT_BODY LBV_UMMA_COMMIT(11) LBV_UMMA_COMMIT(12) LBV_UMMA_COMMIT(13)
+                     "}\n" ::LBV_UMMA_SLOT_ARGS : "memory");
 }
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
@@ -510,9 +512,15 @@ struct TcKernel {
         return smem_u32(c.smem + c.lay.bars) + (uint32_t)((wg * G::NBAR_WG + i) * 8);
     }
     // barrier indices within a warpgroup's block
-    static constexpr int B_FULL = 0, B_EMPTY = G::NST, B_AFULL = 2 * G::NST,
-                         B_AEMPTY = 2 * G::NST + G::NA, B_DFULL = 2 * G::NST + 2 * G::NA,
-                         B_DEMPTY = 2 * G::NST + 2 * G::NA + G::ND;
+    static constexpr int B_FULL = 0, B_EMPTY = G::NST, B_CDONE = 2 * G::NST,
+                         B_DEMPTY = 2 * G::NST + G::NCD;
+    // Waits until the MMAs of the warpgroup's chunk number qc have completed.
+    static __device__ __forceinline__ bool wait_chunk(const Ctx& c, int wg, int qc)
+    {
+        return mbar_wait(bar_addr(c, wg, B_CDONE + qc % G::NCD), (uint32_t)((qc / G::NCD) & 1));
+    }
+    // hardware named barrier of A slot a of warpgroup wg (0 is __syncthreads)
+    static __device__ __forceinline__ int abar_id(int wg, int a) { return 1 + wg * G::NA + a; }
 
     // ---- prologue: X slice as the B operand, per-group corrections ----
     static __device__ void stage_x(const Ctx& c, int tid)
@@ -623,8 +631,9 @@ struct TcKernel {
     }
 
     // ---- the MMA warp of warpgroup wg: every A slot, in order ----
-    // Issue unit = IU slots holding whole scale groups, so which k-steps start
-    // a group and which commits follow a slot are compile-time facts.
+    // It loops over issue units (IU slots holding whole scale groups), so
+    // which k-steps start a group and which commits follow a slot are
+    // compile-time facts.
     static __device__ void mma_warp(const Ctx& c, const Work& w, int wg, bool& ok)
     {
         const uint32_t idesc = idesc_f16<XT>();
@@ -634,14 +643,10 @@ struct TcKernel {
                                               (uint32_t)(w.cw0 * G::KSTEPS * 256), 128, 0);
         const int units_per_tile = w.nchw * G::SLOTS / G::IU;
         constexpr int GPU_ = G::IU * 4 / G::KSG;            // groups per unit (1 or 2)
-        int s = 0, a = 0, gi = 0;
+        int s = 0, a = 0, gi = 0, qc = 0;
         for (int u = 0; u < w.nu; ++u) {
-            uint64_t b = xdesc0;                             // k-step 0 of the first chunk
+            uint64_t b = xdesc0;                             // k-step 0 of the tile's first chunk
             for (int j = 0; j < units_per_tile; ++j) {
-                // all slots of the unit stored (arrivals are in order per warp)
-                const int sl = s + G::IU - 1;
-                if (ok && !mbar_wait(bar_addr(c, wg, B_AFULL + sl % G::NA), (uint32_t)((sl / G::NA) & 1)))
-                    ok = false;
                 // the accumulators of the unit's groups have been read
 #pragma unroll
                 for (int g = 0; g < GPU_; ++g) {
@@ -650,44 +655,48 @@ struct TcKernel {
                         !mbar_wait(bar_addr(c, wg, B_DEMPTY + gg % G::ND), (uint32_t)(((gg / G::ND) - 1) & 1)))
                         ok = false;
                 }
-                tc_fence_after();
 #pragma unroll
                 for (int i = 0; i < G::IU; ++i) {
+                    named_bar_sync(abar_id(wg, a), 160);     // the four decode warps stored slot s + i
+                    tc_fence_after();
                     const uint32_t a_t = tm + (uint32_t)(a * 32);
-                    const uint32_t aempty = bar_addr(c, wg, B_AEMPTY + a);
-                    if constexpr (G::KSG == 2) {
-                        const uint32_t d0 = dcol + (uint32_t)((gi % G::ND) * 16);
+                    const uint32_t cdone = bar_addr(c, wg, B_CDONE + qc % G::NCD);
+                    const uint32_t d0 = dcol + (uint32_t)((gi % G::ND) * 16);
+                    // one commit per chunk (= unit), after its last slot
+                    if constexpr (GPU_ == 2) {
                         const uint32_t d1 = dcol + (uint32_t)(((gi + 1) % G::ND) * 16);
-                        umma_slot<0xA, 3>(d0, d1, a_t, b, idesc, bar_addr(c, wg, B_DFULL + gi % G::ND),
-                                          bar_addr(c, wg, B_DFULL + (gi + 1) % G::ND), aempty);
+                        umma_slot<0xA, 1>(d0, d1, a_t, b, idesc, cdone, 0u, 0u);
+                    } else if (i == 0 && i == G::IU - 1) {
+                        umma_slot<0xE, 1>(d0, d0, a_t, b, idesc, cdone, 0u, 0u);
+                    } else if (i == 0) {
+                        umma_slot<0xE, 0>(d0, d0, a_t, b, idesc, 0u, 0u, 0u);
+                    } else if (i == G::IU - 1) {
+                        umma_slot<0xF, 1>(d0, d0, a_t, b, idesc, cdone, 0u, 0u);
                     } else {
-                        const uint32_t d0 = dcol + (uint32_t)((gi % G::ND) * 16);
-                        if (i == 0 && i == G::IU - 1)
-                            umma_slot<0xE, 2>(d0, d0, a_t, b, idesc, bar_addr(c, wg, B_DFULL + gi % G::ND),
-                                              aempty, 0u);
-                        else if (i == 0)
-                            umma_slot<0xE, 1>(d0, d0, a_t, b, idesc, aempty, 0u, 0u);
-                        else if (i == G::IU - 1)
-                            umma_slot<0xF, 2>(d0, d0, a_t, b, idesc, bar_addr(c, wg, B_DFULL + gi % G::ND),
-                                              aempty, 0u);
-                        else
-                            umma_slot<0xF, 1>(d0, d0, a_t, b, idesc, aempty, 0u, 0u);
+                        umma_slot<0xF, 0>(d0, d0, a_t, b, idesc, 0u, 0u, 0u);
                     }
                     b += (uint64_t)(4 * 256 >> 4);
                     a = a + 1 == G::NA ? 0 : a + 1;
                 }
                 s += G::IU;
                 gi += GPU_;
+                ++qc;
             }
         }
-        // the last commit of each A slot is the last arrival any barrier gets:
-        // wait for them before tensor and shared memory go away
-        const int nslots = s;
-        for (int i = 0; i < G::NA && i < nslots; ++i) {
-            const int last = nslots - 1 - i;
-            if (ok && !mbar_wait(bar_addr(c, wg, B_AEMPTY + last % G::NA), (uint32_t)((last / G::NA) & 1)))
+        // the last commits are the last arrivals any barrier gets: wait for
+        // them before tensor and shared memory go away
+        for (int i = 0; i < G::NCD && i < qc; ++i)
+            if (ok && !wait_chunk(c, wg, qc - 1 - i))
                 ok = false;
-        }
+    }
+
+    // Slot s is stored by this warp: once its store is complete, announce it
+    // to the MMA warp (non-blocking).
+    static __device__ __forceinline__ void complete_slot(int wg, int s)
+    {
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_arrive(abar_id(wg, s % G::NA), 160);
     }
 
     // ---- one warp of a decode warpgroup ----
@@ -707,18 +716,22 @@ struct TcKernel {
 
         const int Q = w.nu * w.nchw;
         int q = 0, s = 0, gc = 0;
+        bool pending = false;        // a stored slot not yet completed (named barrier + issue)
         for (int u = 0; u < w.nu; ++u) {
             const int tile = c.t0 + w.tl + w.TL * u;
             float y[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m)
                 y[m] = 0.f;
-            // side values (scale, bias) of the previous chunk's groups
-            float ps[G::GPC], pb[G::GPC];
+            // side values (scale, bias) of the last LAG chunks' groups:
+            // hs[j], hb[j] belong to chunk cl - 1 - j
+            float hs[G::LAG][G::GPC], hb[G::LAG][G::GPC];
 #pragma unroll
-            for (int gi = 0; gi < G::GPC; ++gi)
-                ps[gi] = pb[gi] = 0.f;
-            for (int cl = 0; cl <= w.nchw; ++cl) {
+            for (int j = 0; j < G::LAG; ++j)
+#pragma unroll
+                for (int gi = 0; gi < G::GPC; ++gi)
+                    hs[j][gi] = hb[j][gi] = 0.f;
+            for (int cl = 0; cl < w.nchw + G::LAG; ++cl) {
                 float cs[G::GPC] = {}, cb[G::GPC] = {};
                 if (cl < w.nchw) {
                     const int st = q % G::NST;
@@ -760,32 +773,39 @@ struct TcKernel {
                             cb[gi] = 0.f;
                         }
                     }
-                    // decode and hand over each A slot of the chunk
+                    // decode and store each A slot of the chunk.  A slot's
+                    // store completes while the next slot is decoded: its
+                    // announcement (wait::st, the named-barrier arrival) is
+                    // deferred to just before the next store.
 #pragma unroll
                     for (int si = 0; si < G::SLOTS; ++si) {
                         uint32_t r[32];
                         decode_slot(wv, si, bases, r);
+                        if (pending)
+                            complete_slot(wg, s - 1);
                         const int a = s % G::NA;
-                        if (s >= G::NA && ok &&
-                            !mbar_wait(bar_addr(c, wg, B_AEMPTY + a), (uint32_t)(((s / G::NA) - 1) & 1)))
+                        // the A slot's previous contents were consumed by the
+                        // MMAs of chunk (s - NA) / SLOTS
+                        if (s >= G::NA && ok && !wait_chunk(c, wg, (s - G::NA) / G::SLOTS))
                             ok = false;
                         tc_fence_after();
                         tmem_st32(tm_wg + (uint32_t)(a * 32), r);
-                        tmem_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar_addr(c, wg, B_AFULL + a));
+                        pending = true;
                         ++s;
                     }
                 }
-                // epilogue of the previous chunk's groups (their MMAs ran while
-                // this chunk was decoded)
-                if (cl > 0) {
+                // the last chunk's MMAs need its last slot before its epilogue
+                if (cl >= w.nchw && pending) {
+                    complete_slot(wg, s - 1);
+                    pending = false;
+                }
+                // epilogue of chunk cl - LAG's groups (their MMAs ran while the
+                // later chunks were decoded)
+                if (cl >= G::LAG) {
 #pragma unroll
                     for (int gi = 0; gi < G::GPC; ++gi) {
                         const int d = gc % G::ND;
-                        if (ok && !mbar_wait(bar_addr(c, wg, B_DFULL + d), (uint32_t)((gc / G::ND) & 1)))
+                        if (ok && !wait_chunk(c, wg, gc / G::GPC))
                             ok = false;
                         tc_fence_after();
                         float acc[8];
@@ -795,27 +815,34 @@ struct TcKernel {
                         if (lane == 0)
                             mbar_arrive(bar_addr(c, wg, B_DEMPTY + d));
                         ++gc;
-                        const int gr = (w.cw0 + cl - 1) * G::GPC + gi;   // group within the slice
+                        const int gr = (w.cw0 + cl - G::LAG) * G::GPC + gi;   // group within the slice
                         const float4 c0v = *reinterpret_cast<const float4*>(corr + gr * 8);
                         const float4 c1v = *reinterpret_cast<const float4*>(corr + gr * 8 + 4);
                         const float cv[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
 #pragma unroll
                         for (int m = 0; m < 8; ++m)
-                            y[m] = fmaf(ps[gi], acc[m] - cv[m], y[m]);
+                            y[m] = fmaf(hs[G::LAG - 1][gi], acc[m] - cv[m], y[m]);
                         if constexpr (T::AFFINE) {
                             const float4 r0 = *reinterpret_cast<const float4*>(rsum + gr * 8);
                             const float4 r1 = *reinterpret_cast<const float4*>(rsum + gr * 8 + 4);
                             const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
                             for (int m = 0; m < 8; ++m)
-                                y[m] = fmaf(pb[gi], rv[m], y[m]);
+                                y[m] = fmaf(hb[G::LAG - 1][gi], rv[m], y[m]);
                         }
                     }
                 }
 #pragma unroll
+                for (int j = G::LAG - 1; j > 0; --j)
+#pragma unroll
+                    for (int gi = 0; gi < G::GPC; ++gi) {
+                        hs[j][gi] = hs[j - 1][gi];
+                        hb[j][gi] = hb[j - 1][gi];
+                    }
+#pragma unroll
                 for (int gi = 0; gi < G::GPC; ++gi) {
-                    ps[gi] = cs[gi];
-                    pb[gi] = cb[gi];
+                    hs[0][gi] = cs[gi];
+                    hb[0][gi] = cb[gi];
                 }
             }
             store_tile(c, w, tile, col, y, part);
@@ -933,14 +960,10 @@ struct TcKernel {
                     mbar_init(bar_addr(c, w, B_FULL + i), 1);
                     mbar_init(bar_addr(c, w, B_EMPTY + i), 4);
                 }
-                for (int i = 0; i < G::NA; ++i) {
-                    mbar_init(bar_addr(c, w, B_AFULL + i), 4);
-                    mbar_init(bar_addr(c, w, B_AEMPTY + i), 1);
-                }
-                for (int i = 0; i < G::ND; ++i) {
-                    mbar_init(bar_addr(c, w, B_DFULL + i), 1);
+                for (int i = 0; i < G::NCD; ++i)
+                    mbar_init(bar_addr(c, w, B_CDONE + i), 1);
+                for (int i = 0; i < G::ND; ++i)
                     mbar_init(bar_addr(c, w, B_DEMPTY + i), 4);
-                }
             }
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         } else if (tid >= 64 && tid < 80) {
@@ -956,10 +979,11 @@ struct TcKernel {
         const int wg = is_mma ? warp - G::NWG * 4 : warp / 4, wq = warp % 4;
         const Work w = work_of(c, wg);
         if (is_mma) {
-            // the packed weights start streaming before the previous kernel ends
+            // the packed weights start streaming before the previous kernel
+            // ends; lane l fills stage l
             const int first = min(G::NST, w.nu * w.nchw);
-            for (int q = 0; q < first; ++q)
-                produce(c, w, wg, q, lane);
+            for (int q = lane; q < first; q += 32)
+                produce(c, w, wg, q, 0);
         } else {
             griddep_wait();
             stage_x(c, tid);

@@ -217,7 +217,10 @@ struct TcGeo {
     static constexpr int TMEM_COLS = 512;            // allocation (>= NWG * TMEM_WG)
     static_assert(NWG * TMEM_WG <= TMEM_COLS && NA >= 2, "tensor memory budget");
     static_assert((T::CK / 64) % IU == 0, "issue units tile a chunk");
-    static constexpr int NCD = LAG + 2;              // chunk-done barriers (ring over chunks)
+    // chunk-done barriers (a ring over chunks).  A waiter looks back at most
+    // max(LAG, NA / SLOTS) chunks; two more keep any barrier from completing
+    // two phases past a pending waiter.
+    static constexpr int NCD = (LAG > NA / SLOTS ? LAG : NA / SLOTS) + 2;
     static_assert(IU * 64 == T::CK, "an issue unit is one chunk");
     static constexpr int NBAR_WG = 2 * NST + NCD + ND;
     static_assert(1 + NWG * NA <= 16, "named barriers: one per A slot of each warpgroup");

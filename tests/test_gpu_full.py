@@ -49,6 +49,7 @@ def check_matrix(mat, parts, xb, Ms=range(1, 9), rotate=False):
         Y = torch.full((8, N), -7.0, dtype=torch.float32, device="cuda")
         lbv.verify_gemm(plan, X, M, Wp, Y)
         torch.cuda.synchronize()
+        plan.device_status()          # no bounded wait gave up
         got = Y.cpu().numpy()
         err = np.abs(got[:M][:, cols] - Yref[:M])
         tol = RTOL * A[:M] + ATOL

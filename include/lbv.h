@@ -95,11 +95,12 @@ typedef struct lbv_plan lbv_plan;   /* opaque, library-owned */
 
 /*
  * Size in bytes of the device layout of a K x N matrix, or 0 for an invalid
- * shape.  For N % 16 == 0 and K a multiple of the format's chunk (256 for
- * sign1, 128 for affine2, 64 for Q4_0) it equals the canonical size exactly
- * (1.125, 2 + 32/g and 4.5 bits per weight); otherwise the last column tile
- * and K chunk are padded with zero codes and zero scales, which contribute
- * exactly 0.  `group` is ignored except for LBV_FMT_AFFINE2.
+ * shape.  The layout is one record per (128-column tile, K chunk), tile-major;
+ * the chunk is 128 K for sign1 and affine2 g128, 64 K for affine2 g32/g64 and
+ * Q4_0.  For N % 128 == 0 and K a multiple of the chunk the size equals the
+ * canonical one exactly (1.125, 2 + 32/g and 4.5 bits per weight); otherwise
+ * the last tile and chunk are padded with zero codes and zero scales, which
+ * contribute exactly 0.  `group` is ignored except for LBV_FMT_AFFINE2.
  */
 LBV_API size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group);
 

@@ -49,7 +49,9 @@ def parse_args():
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M=1..8 table")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--shape", default="", help="splits[,ctas] override of the launch shape")
+    ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override of the launch shape")
+    ap.add_argument("--kernel", default="mma", choices=["mma", "tc"],
+                    help="few-row kernel: mma.sync (default plans) or tcgen05 (PLAN_TCGEN05)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
     ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
@@ -137,7 +139,7 @@ class Stack:
     """Distinct packed matrices of a workload resident on the device."""
 
     def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int,
-                 use_graphs: bool = True):
+                 use_graphs: bool = True, kernel: str = "mma"):
         import torch
         self.use_graphs = use_graphs
         self.graphs = {}
@@ -145,7 +147,7 @@ class Stack:
         import few_row_packed_gb300 as lbv
         wl = synth.WORKLOADS[workload]
         self.mats = list(wl.matrices)
-        flags = lbv.PLAN_PDL if pdl else 0
+        flags = (lbv.PLAN_PDL if pdl else 0) | (lbv.PLAN_TCGEN05 if kernel == "tc" else 0)
         self.layers = []
         if len(self.mats) == 1:
             mat = self.mats[0]
@@ -169,7 +171,8 @@ class Stack:
                     plans[key].set_shape(*[int(v) for v in shape.split(",")])
             pid = id(parts[0])
             if pid not in packed_cache:
-                packed_cache[pid] = lbv.pack(FMT_IDS[mat.fmt], parts, mat.K, mat.N, mat.group)
+                packed_cache[pid] = lbv.pack(FMT_IDS[mat.fmt], parts, mat.K, mat.N, mat.group,
+                                             plan=plans[key])
             Wp = torch.from_numpy(packed_cache[pid]).cuda()       # a distinct allocation
             X = torch.from_numpy(xb.view(np.int16)).cuda()
             Xr = torch.zeros_like(X) if mat.rotate else None
@@ -238,13 +241,14 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload, M):
-    """DRAM bytes per verify launch from the committed ncu capture, if it was
-    taken on the current kernel sources."""
+def recorded_traffic(workload, M, kernel):
+    """DRAM bytes per verify launch from the committed ncu capture of this
+    workload and kernel ("mma" or "tc"), if it was taken on the current
+    kernel sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
-        e = t[workload]
+        e = t[f"{workload}/{kernel}"]
         if e.get("kernel_hash") == kernel_hash() and int(e.get("M", -1)) == M:
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -294,7 +298,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     dev = torch.cuda.current_device()
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
-    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M,
+    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
                   use_graphs=not args.no_graph)
     peak, peak_kind = peaks()
     phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
@@ -324,7 +328,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     us_launch = ms_v * 1e3 / (args.steps * stack.calls)
     bytes_launch = bytes_step / stack.calls
     achieved = bytes_launch / (us_launch * 1e-6) / 1e9
-    traffic = recorded_traffic(args.workload, args.M)
+    traffic = recorded_traffic(args.workload, args.M, args.kernel)
 
     per_M = {}
     if not args.no_sweep:
@@ -383,7 +387,9 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
-            "shape": {"splits": shape[0], "clusters_n": shape[1]},
+            "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
+                      "ctas_n": shape[3]},
+            "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "per_M": per_M,
@@ -391,7 +397,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                        if per_M else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_kind": peak_kind, "kernel": "lbv_tc_kernel",
+                     "peak_kind": peak_kind,
+                     "kernel": "lbv_tc_kernel" if args.kernel == "tc" else "lbv_verify_kernel",
                      "bytes_per_launch": bytes_launch, "us_per_launch": round(us_launch, 3)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": args.M * mat0.K * 2,

@@ -24,8 +24,10 @@ PLAN_MEASURE = 0x1
 PLAN_FORCE_FEWROW = 0x2
 PLAN_FORCE_GEMV = 0x4
 PLAN_PDL = 0x8
+PLAN_TCGEN05 = 0x10
 KERNEL_FEWROW = 1
 KERNEL_GEMV = 2
+KERNEL_FEWROW_TC = 3
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
 
@@ -64,12 +66,14 @@ def lib():
             "lbv_pack_sign_g128": (st, [P, P, I, I, P, S]),
             "lbv_pack_affine2": (st, [P, P, P, I, I, I, P, S]),
             "lbv_pack_q4_0": (st, [P, I, I, P, S]),
+            "lbv_plan_packed_bytes": (S, [P]),
+            "lbv_plan_pack": (st, [P, P, P, P, P, S]),
             "lbv_plan_create": (st, [I, I, I, I, I, U, ctypes.POINTER(P)]),
             "lbv_plan_destroy": (st, [P]),
             "lbv_plan_query": (st, [P, I, ctypes.POINTER(I), ctypes.POINTER(I),
                                     ctypes.POINTER(S)]),
-            "lbv_plan_shape": (st, [P] + [ctypes.POINTER(I)] * 2),
-            "lbv_plan_set_shape": (st, [P, I, I]),
+            "lbv_plan_shape": (st, [P] + [ctypes.POINTER(I)] * 4),
+            "lbv_plan_set_shape": (st, [P, I, I, I, I]),
             "lbv_plan_measured": (st, [P, I, ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
             "lbv_plan_device_status": (st, [P]),
@@ -160,8 +164,11 @@ def pack_q4_0(blocks, K: int, N: int) -> np.ndarray:
     return out
 
 
-def pack(fmt: int, parts, K: int, N: int, group: int = 128) -> np.ndarray:
-    """Canonical arrays (as produced for the format) -> device-layout bytes."""
+def pack(fmt: int, parts, K: int, N: int, group: int = 128, plan=None) -> np.ndarray:
+    """Canonical arrays (as produced for the format) -> device-layout bytes: the
+    default layout, or the layout `plan` reads (needed for PLAN_TCGEN05 plans)."""
+    if plan is not None:
+        return plan.pack(parts)
     if fmt == FMT_SIGN1_G128:
         return pack_sign_g128(parts[0], parts[1], K, N)
     if fmt == FMT_AFFINE2:
@@ -194,7 +201,16 @@ class Plan:
 
     @property
     def packed_bytes(self) -> int:
-        return packed_bytes(self.fmt, self.K, self.N, self.group)
+        """Bytes of the device layout this plan's kernels read."""
+        return int(lib().lbv_plan_packed_bytes(self.handle))
+
+    def pack(self, parts) -> np.ndarray:
+        """Canonical arrays of the plan's format -> this plan's device layout."""
+        arrs = [np.ascontiguousarray(a) for a in parts]
+        ptrs = [a.ctypes.data for a in arrs] + [None] * (3 - len(arrs))
+        out = np.zeros(self.packed_bytes, np.uint8)
+        _check(lib().lbv_plan_pack(self.handle, *ptrs[:3], out.ctypes.data, out.size))
+        return out
 
     def query(self, M: int):
         k, s, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
@@ -203,13 +219,12 @@ class Plan:
         return k.value, s.value, w.value
 
     def shape(self):
-        """(K splits = cluster size, clusters along N) of the few-row kernel."""
-        v = [ctypes.c_int() for _ in range(2)]
+        v = [ctypes.c_int() for _ in range(4)]
         _check(lib().lbv_plan_shape(self.handle, *[ctypes.byref(x) for x in v]))
         return tuple(x.value for x in v)
 
-    def set_shape(self, splits: int, ctas_n: int = 0):
-        _check(lib().lbv_plan_set_shape(self.handle, splits, ctas_n))
+    def set_shape(self, warps: int, tiles_per_warp: int, splits: int, ctas_n: int = 0):
+        _check(lib().lbv_plan_set_shape(self.handle, warps, tiles_per_warp, splits, ctas_n))
 
     def device_status(self):
         """Raises LbvError(ERR_TIMEOUT) if a kernel of this plan gave up a

@@ -20,7 +20,14 @@ LIB = os.path.join(HERE, "liblbv.so")
 
 SOURCES = [
     "api.cpp",
+    "tc_api.cpp",
     "aux_kernels.cu",
+    "verify_sign1.cu",
+    "verify_affine2_g32.cu",
+    "verify_affine2_g64.cu",
+    "verify_affine2_g128.cu",
+    "verify_q4_0.cu",
+    "tc_aux.cu",
     "tc_sign1.cu",
     "tc_affine2_g32.cu",
     "tc_affine2_g64.cu",

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "lbv_internal.h"
+#include "tc_api.h"
 #include "verify_ops.h"
 
 namespace {
@@ -85,41 +86,15 @@ constexpr size_t kSmemCap = 220 * 1024;        // per CTA, of 227 KB
 // placing two CTAs of one grid on an SM while other SMs stay empty.
 constexpr size_t kSmemOnePerSm = 116 * 1024;
 
-// Work of the busiest warpgroup, in (tile, chunk) records, for `tpc` tiles
-// per cluster, `cps` chunks per slice and a warpgroup split `sw`.
-int64_t wg_load(int64_t tpc, int cps, int sw)
+// Bytes per (tile, chunk) of the device layout and X bytes per chunk staged.
+size_t tile_chunk_bytes(const lbv_plan* P)
 {
-    const int64_t lanes = lbv::kTcWarpgroups / sw;
-    return ((tpc + lanes - 1) / lanes) * ((cps + sw - 1) / sw);
+    return P->layout.rec_bytes;
 }
 
-// Fills sh.smem and sh.wsplit for sh.splits and sh.ctas_n: the warpgroup
-// split with the least work per warpgroup whose partial buffers fit.
-bool fit_shape(const lbv_plan* P, lbv::Shape& sh, int cps)
-{
-    const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
-    const int64_t tpc = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
-    const int owned = (int)((tpc + sh.splits - 1) / sh.splits);
-    int64_t best = -1;
-    for (int sw = 1; sw <= lbv::kTcWarpgroups; ++sw) {
-        if (lbv::kTcWarpgroups % sw != 0 || (sw > 1 && sw > cps))
-            continue;
-        const size_t smem = std::max(ops->smem(cps, owned, sh.splits * sw), kSmemOnePerSm);
-        if (smem > kSmemCap)
-            continue;
-        const int64_t load = wg_load(tpc, cps, sw);
-        if (best < 0 || load < best) {
-            best = load;
-            sh.wsplit = sw;
-            sh.smem = smem;
-        }
-    }
-    return best >= 0;
-}
-
-// Fills sh.splits (clamped), sh.ctas_n, sh.wsplit and sh.smem for a K split:
-// one cluster of `splits` CTAs per `splits` SMs, as many clusters as can be
-// resident at once, each owning a contiguous range of 128-column tiles.
+// Fills sh.splits (clamped), sh.ctas_n and sh.smem for a (warps, tpw,
+// splits) choice: one cluster of `splits` CTAs per `splits` SMs, as many
+// clusters as can be resident at once, each owning a contiguous tile range.
 // ctas_req > 0 caps the number of clusters.  Returns false if nothing fits.
 bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
 {
@@ -131,9 +106,11 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
     if (ctas_req > 0)
         G = std::min<int64_t>(G, ctas_req);
     for (int it = 0; it < 4; ++it) {
-        sh.ctas_n = (int)G;
-        if (!fit_shape(P, sh, cps))
+        const int tiles_max = (int)((ntiles + G - 1) / G);
+        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits), kSmemOnePerSm);
+        if (sh.smem > kSmemCap)
             return false;
+        sh.ctas_n = (int)G;
         if (ops->prepare(P->xdtype, sh) != cudaSuccess)
             return false;
         const int maxc = ops->max_clusters(P->xdtype, sh);
@@ -143,24 +120,28 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
             return true;
         G = maxc;
     }
+    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits),
+                       kSmemOnePerSm);
     sh.ctas_n = (int)G;
-    return fit_shape(P, sh, cps) && ops->prepare(P->xdtype, sh) == cudaSuccess;
+    return ops->prepare(P->xdtype, sh) == cudaSuccess;
 }
 
-// Default launch shape: the K split that minimises what the busiest decode
-// warpgroup streams (its records) plus half the activation bytes a CTA
-// stages.
+// Default launch shape: 16 warps of two-tile units; the K split that
+// minimises what the busiest warp of a CTA streams (its units times the
+// slice) plus half the activation bytes the CTA stages.
 lbv::Shape default_shape(lbv_plan* P)
 {
-    lbv::Shape best = {1, 0, 1, 0};
+    const int warps = 16, tpw = 2;
+    lbv::Shape best = {warps, tpw, 1, 0, 0};
     double best_cost = 1e300;
     for (int s = 1; s <= 8; ++s) {
-        lbv::Shape sh = {s, 0, 1, 0};
+        lbv::Shape sh = {warps, tpw, s, 0, 0};
         if (!complete_shape(P, sh, 0) || sh.splits != s)
             continue;
         const int cps = shape_cps(sh, P->layout.nchunks);
-        const int64_t tpc = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
-        const double cost = (double)wg_load(tpc, cps, sh.wsplit) * P->layout.rec_bytes +
+        const int64_t tmax = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
+        const int64_t umax = ((tmax + tpw - 1) / tpw + warps - 1) / warps;
+        const double cost = (double)umax * tpw * warps * cps * tile_chunk_bytes(P) +
                             0.5 * (double)cps * P->fi.chunk_k * 16.0;
         if (cost < best_cost * 0.98) {
             best_cost = cost;
@@ -198,56 +179,9 @@ size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group)
     return lbv::make_layout(fi, K, N).total;
 }
 
-}  // extern "C"
-
 // --------------------------------------------------------------------------
-// Host packers.  One routine walks the device layout (layout.h) and fetches
-// the code of weight (k, n) and the side values from the canonical arrays.
-
-namespace {
-
-template <class CodeF, class SideF>
-void pack_records(const lbv::FmtInfo& fi, int K, int N, uint8_t* out, CodeF code, SideF side)
-{
-    const lbv::Layout L = lbv::make_layout(fi, K, N);
-    const int W = fi.code_bits, PPW = 16 / W, NWORD = fi.code_bytes / 4;
-    const int nside = fi.side_bytes / 2;
-    for (int64_t tile = 0; tile < L.ntiles; ++tile)
-        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
-            uint8_t* rec = out + ((size_t)tile * L.nchunks + ch) * L.rec_bytes;
-            for (int c = 0; c < lbv::kTileN; ++c) {
-                const int n = (int)tile * lbv::kTileN + c;
-                for (int j = 0; j < NWORD; ++j) {
-                    uint32_t w = 0;
-                    for (int s = 0; s < PPW; ++s) {
-                        const int k0 = (int)ch * fi.chunk_k + 2 * (PPW * j + s);
-                        w |= code(n, k0) << (s * W);
-                        w |= code(n, k0 + 1) << (16 + s * W);
-                    }
-                    memcpy(rec + (j / 4) * 2048 + c * 16 + (j % 4) * 4, &w, 4);
-                }
-                uint16_t* sd = reinterpret_cast<uint16_t*>(rec + lbv::kTileN * fi.code_bytes +
-                                                           c * fi.side_bytes);
-                for (int i = 0; i < nside; ++i)
-                    sd[i] = n < N ? side(n, (int)ch, i) : (uint16_t)0;
-            }
-        }
-}
-
-lbv_status check_pack(lbv_format fmt, int K, int N, int group, size_t out_bytes, const char* name)
-{
-    const size_t need = lbv_packed_bytes(fmt, K, N, group);
-    if (need == 0)
-        return fail(LBV_ERR_INVALID_ARG, "%s: K=%d N=%d group=%d is not a valid shape", name, K, N,
-                    group);
-    if (out_bytes < need)
-        return fail(LBV_ERR_WORKSPACE, "%s: out_bytes %zu < %zu", name, out_bytes, need);
-    return LBV_OK;
-}
-
-}  // namespace
-
-extern "C" {
+// Host packers.  Each walks the device layout (layout.h) and fetches the
+// code of weight (k, n) from the canonical arrays.
 
 lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int K, int N,
                               void* out, size_t out_bytes)
@@ -255,50 +189,104 @@ lbv_status lbv_pack_sign_g128(const uint32_t* bits, const uint16_t* scales, int 
     g_err.clear();
     if (!bits || !scales || !out)
         return fail(LBV_ERR_INVALID_ARG, "lbv_pack_sign_g128: null pointer");
-    lbv_status st = check_pack(LBV_FMT_SIGN1_G128, K, N, 128, out_bytes, "lbv_pack_sign_g128");
-    if (st != LBV_OK)
-        return st;
+    const size_t need = lbv_packed_bytes(LBV_FMT_SIGN1_G128, K, N, 128);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_sign_g128: K=%d N=%d (need K%%128==0, N>0)", K, N);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_sign_g128: out_bytes %zu < %zu", out_bytes, need);
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_SIGN1_G128, 128, &fi);
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint8_t* base = static_cast<uint8_t*>(out);
     const int wk = K / 32, sk = K / 128;
-    pack_records(
-        fi, K, N, static_cast<uint8_t*>(out),
-        [&](int n, int k) -> uint32_t {
-            if (n >= N || k >= K) return 0u;
-            return (bits[(size_t)n * wk + k / 32] >> (k % 32)) & 1u;
-        },
-        [&](int n, int ch, int) -> uint16_t {
-            return ch < sk ? scales[(size_t)n * sk + ch] : (uint16_t)0;
-        });
+    auto bit = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        return (bits[(size_t)n * wk + k / 32] >> (k % 32)) & 1u;
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 16; ++s) {
+                        const int kt = (wi >> 1) * 8 + (s >> 1);
+                        const int k0 = (int)ch * 256 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= bit(n, k0) << s;
+                        w |= bit(n, k0 + 1) << (16 + s);
+                    }
+                    codes[lane * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 2; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int grp = (int)ch * 2 + j;
+                        const bool ok = n < N && grp < sk;
+                        side[g * 4 + 2 * j + hi] = ok ? scales[(size_t)n * sk + grp] : 0;
+                    }
+        }
     return LBV_OK;
 }
 
-lbv_status lbv_pack_affine2(const uint32_t* codes, const uint16_t* scales,
+lbv_status lbv_pack_affine2(const uint32_t* codes_in, const uint16_t* scales,
                             const uint16_t* biases, int K, int N, int group, void* out,
                             size_t out_bytes)
 {
     g_err.clear();
-    if (!codes || !scales || !biases || !out)
+    if (!codes_in || !scales || !biases || !out)
         return fail(LBV_ERR_INVALID_ARG, "lbv_pack_affine2: null pointer");
     if (group != 32 && group != 64 && group != 128)
         return fail(LBV_ERR_UNSUPPORTED, "lbv_pack_affine2: group %d (supported: 32, 64, 128)", group);
-    lbv_status st = check_pack(LBV_FMT_AFFINE2, K, N, group, out_bytes, "lbv_pack_affine2");
-    if (st != LBV_OK)
-        return st;
+    const size_t need = lbv_packed_bytes(LBV_FMT_AFFINE2, K, N, group);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_affine2: K=%d N=%d group=%d (need K%%group==0)", K, N, group);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_affine2: out_bytes %zu < %zu", out_bytes, need);
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_AFFINE2, group, &fi);
-    const int wk = K / 16, gk = K / group, gpc = fi.chunk_k / group;
-    pack_records(
-        fi, K, N, static_cast<uint8_t*>(out),
-        [&](int n, int k) -> uint32_t {
-            if (n >= N || k >= K) return 0u;
-            return (codes[(size_t)n * wk + k / 16] >> (2 * (k % 16))) & 3u;
-        },
-        [&](int n, int ch, int i) -> uint16_t {
-            const int grp = ch * gpc + i / 2;
-            if (grp >= gk) return 0;
-            return (i % 2 ? biases : scales)[(size_t)n * gk + grp];
-        });
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint8_t* base = static_cast<uint8_t*>(out);
+    const int wk = K / 16, gk = K / group, gpc = 128 / group;
+    auto code = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        return (codes_in[(size_t)n * wk + k / 16] >> (2 * (k % 16))) & 3u;
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 8; ++s) {
+                        const int kt = (wi >> 1) * 4 + (s >> 1);
+                        const int k0 = (int)ch * 128 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= code(n, k0) << (2 * s);
+                        w |= code(n, k0 + 1) << (16 + 2 * s);
+                    }
+                    codes[lane * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < gpc; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int grp = (int)ch * gpc + j;
+                        const bool ok = n < N && grp < gk;
+                        uint16_t* e = side + g * (4 * gpc) + 4 * j;
+                        e[hi] = ok ? scales[(size_t)n * gk + grp] : 0;
+                        e[2 + hi] = ok ? biases[(size_t)n * gk + grp] : 0;
+                    }
+        }
     return LBV_OK;
 }
 
@@ -307,32 +295,56 @@ lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out, size_t 
     g_err.clear();
     if (!blocks || !out)
         return fail(LBV_ERR_INVALID_ARG, "lbv_pack_q4_0: null pointer");
-    lbv_status st = check_pack(LBV_FMT_Q4_0, K, N, 32, out_bytes, "lbv_pack_q4_0");
-    if (st != LBV_OK)
-        return st;
+    const size_t need = lbv_packed_bytes(LBV_FMT_Q4_0, K, N, 32);
+    if (need == 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_pack_q4_0: K=%d N=%d (need K%%32==0)", K, N);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_pack_q4_0: out_bytes %zu < %zu", out_bytes, need);
     lbv::FmtInfo fi;
     lbv::fmt_info(LBV_FMT_Q4_0, 32, &fi);
+    const lbv::Layout L = lbv::make_layout(fi, K, N);
+    uint8_t* base = static_cast<uint8_t*>(out);
     const int nb = K / 32;
-    pack_records(
-        fi, K, N, static_cast<uint8_t*>(out),
-        [&](int n, int k) -> uint32_t {
-            if (n >= N || k >= K) return 0u;
-            const uint8_t* blk = blocks + ((size_t)n * nb + k / 32) * 18;
-            const int j = k % 32;
-            return j < 16 ? (blk[2 + j] & 15u) : (uint32_t)(blk[2 + j - 16] >> 4);
-        },
-        [&](int n, int ch, int i) -> uint16_t {
-            const int b = ch * 2 + i;
-            if (b >= nb) return 0;
-            const uint8_t* blk = blocks + ((size_t)n * nb + b) * 18;
-            return (uint16_t)(blk[0] | (blk[1] << 8));
-        });
+    auto nib = [&](int n, int k) -> uint32_t {
+        if (n >= N || k >= K) return 0u;
+        const uint8_t* blk = blocks + ((size_t)n * nb + k / 32) * 18;
+        const int j = k % 32;
+        return j < 16 ? (blk[2 + j] & 15u) : (uint32_t)(blk[2 + j - 16] >> 4);
+    };
+    for (int64_t tile = 0; tile < L.ntiles; ++tile)
+        for (int64_t ch = 0; ch < L.nchunks; ++ch) {
+            const size_t tc = (size_t)tile * L.nchunks + ch;
+            uint32_t* codes = reinterpret_cast<uint32_t*>(base + tc * L.rec_bytes);
+            uint16_t* side = reinterpret_cast<uint16_t*>(base + tc * L.rec_bytes + 512);
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                for (int wi = 0; wi < 4; ++wi) {
+                    const int n = (int)tile * 16 + g + 8 * (wi & 1);
+                    uint32_t w = 0;
+                    for (int s = 0; s < 4; ++s) {
+                        const int kt = (wi >> 1) * 2 + (s >> 1);
+                        const int k0 = (int)ch * 64 + 16 * kt + 8 * (s & 1) + 2 * t;
+                        w |= nib(n, k0) << (4 * s);
+                        w |= nib(n, k0 + 1) << (16 + 4 * s);
+                    }
+                    codes[lane * 4 + wi] = w;
+                }
+            }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 2; ++j)
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int n = (int)tile * 16 + g + 8 * hi;
+                        const int b = (int)ch * 2 + j;
+                        uint16_t d = 0;
+                        if (n < N && b < nb) {
+                            const uint8_t* blk = blocks + ((size_t)n * nb + b) * 18;
+                            d = (uint16_t)(blk[0] | (blk[1] << 8));
+                        }
+                        side[g * 4 + 2 * j + hi] = d;
+                    }
+        }
     return LBV_OK;
 }
-
-}  // extern "C"
-
-extern "C" {
 
 // --------------------------------------------------------------------------
 // Plans
@@ -356,6 +368,8 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: K=%d N=%d not valid for the format", K, N);
     if ((flags & LBV_PLAN_FORCE_FEWROW) && (flags & LBV_PLAN_FORCE_GEMV))
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: both FORCE flags set");
+    if ((flags & LBV_PLAN_TCGEN05) && (flags & LBV_PLAN_FORCE_GEMV))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: TCGEN05 with FORCE_GEMV");
 
     lbv_plan* P = new (std::nothrow) lbv_plan();
     if (!P)
@@ -389,6 +403,11 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: no launch shape fits K=%d", K);
     }
     P->shape = sh;
+    P->tc = (flags & LBV_PLAN_TCGEN05) ? 1 : 0;
+    if (P->tc && !lbv::tc_plan_setup(P)) {
+        lbv_plan_destroy(P);
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: no tcgen05 launch shape fits K=%d", K);
+    }
     for (int m = 0; m <= 8; ++m)
         P->use_gemv[m] = (flags & LBV_PLAN_FORCE_GEMV) ? 1 : 0;
     P->crossover = (flags & LBV_PLAN_FORCE_GEMV) ? 9 : 1;
@@ -412,6 +431,43 @@ lbv_status lbv_plan_destroy(lbv_plan* plan)
         delete plan;
     }
     return LBV_OK;
+}
+
+size_t lbv_plan_packed_bytes(const lbv_plan* P)
+{
+    if (!P)
+        return 0;
+    return P->tc ? lbv::tc_packed_bytes(P) : P->layout.total;
+}
+
+lbv_status lbv_plan_pack(const lbv_plan* P, const void* part0, const void* part1,
+                         const void* part2, void* out, size_t out_bytes)
+{
+    g_err.clear();
+    if (!P || !part0 || !out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_pack: null argument");
+    if ((P->fmt == LBV_FMT_SIGN1_G128 && !part1) || (P->fmt == LBV_FMT_AFFINE2 && (!part1 || !part2)))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_pack: missing scales or biases");
+    const size_t need = lbv_plan_packed_bytes(P);
+    if (out_bytes < need)
+        return fail(LBV_ERR_WORKSPACE, "lbv_plan_pack: out_bytes %zu < %zu", out_bytes, need);
+    if (P->tc) {
+        lbv::tc_pack(P, part0, part1, part2, static_cast<uint8_t*>(out));
+        return LBV_OK;
+    }
+    switch (P->fmt) {
+    case LBV_FMT_SIGN1_G128:
+        return lbv_pack_sign_g128(static_cast<const uint32_t*>(part0),
+                                  static_cast<const uint16_t*>(part1), P->K, P->N, out, out_bytes);
+    case LBV_FMT_AFFINE2:
+        return lbv_pack_affine2(static_cast<const uint32_t*>(part0),
+                                static_cast<const uint16_t*>(part1),
+                                static_cast<const uint16_t*>(part2), P->K, P->N, P->group, out,
+                                out_bytes);
+    case LBV_FMT_Q4_0:
+        return lbv_pack_q4_0(static_cast<const uint8_t*>(part0), P->K, P->N, out, out_bytes);
+    }
+    return fail(LBV_ERR_INVALID_ARG, "lbv_plan_pack: unknown format");
 }
 
 lbv_status lbv_plan_device_status(const lbv_plan* P)
@@ -439,32 +495,52 @@ lbv_status lbv_plan_query(const lbv_plan* P, int M, int* kernel_id, int* splits,
     if (M < 1 || M > 8)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_query: M=%d outside 1..8", M);
     if (kernel_id)
-        *kernel_id = P->use_gemv[M] ? LBV_KERNEL_GEMV : LBV_KERNEL_FEWROW;
+        *kernel_id = P->tc ? LBV_KERNEL_FEWROW_TC : P->use_gemv[M] ? LBV_KERNEL_GEMV : LBV_KERNEL_FEWROW;
     if (splits)
-        *splits = P->use_gemv[M] ? 1 : P->shape.splits;
+        *splits = P->tc ? P->tc_shape.splits : P->use_gemv[M] ? 1 : P->shape.splits;
     if (workspace_bytes)
         *workspace_bytes = 0;
     return LBV_OK;
 }
 
-lbv_status lbv_plan_shape(const lbv_plan* P, int* splits, int* ctas_n)
+lbv_status lbv_plan_shape(const lbv_plan* P, int* warps, int* tpw, int* splits, int* ctas_n)
 {
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_shape: plan is NULL");
+    if (P->tc) {
+        if (warps) *warps = 0;
+        if (tpw) *tpw = 0;
+        if (splits) *splits = P->tc_shape.splits;
+        if (ctas_n) *ctas_n = P->tc_shape.ctas_n;
+        return LBV_OK;
+    }
+    if (warps) *warps = P->shape.warps;
+    if (tpw) *tpw = P->shape.tpw;
     if (splits) *splits = P->shape.splits;
     if (ctas_n) *ctas_n = P->shape.ctas_n;
     return LBV_OK;
 }
 
-lbv_status lbv_plan_set_shape(lbv_plan* P, int splits, int ctas_n)
+lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int ctas_n)
 {
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: plan is NULL");
-    if (splits < 1 || splits > 8 || ctas_n < 0)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: splits=%d ctas_n=%d", splits, ctas_n);
-    lbv::Shape sh = {splits, 0, 1, 0};
+    if (P->tc) {
+        if (splits < 1 || splits > 8 || ctas_n < 0)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: splits=%d ctas_n=%d", splits, ctas_n);
+        if (!lbv::tc_set_shape(P, splits, ctas_n))
+            return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_set_shape: shape does not fit (smem or occupancy)");
+        return LBV_OK;
+    }
+    const bool shape_ok = (warps == 8 && (tpw == 2 || tpw == 4)) ||
+                          (warps == 16 && (tpw == 1 || tpw == 2));
+    if (!shape_ok || splits < 1 || splits > 8 ||
+        ctas_n < 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: warps=%d tpw=%d splits=%d ctas_n=%d",
+                    warps, tpw, splits, ctas_n);
+    lbv::Shape sh = {warps, tpw, splits, 0, 0};
     if (!complete_shape(P, sh, ctas_n))
         return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_set_shape: shape does not fit (smem or occupancy)");
     P->shape = sh;
@@ -516,7 +592,6 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.nchunks = (int)P->layout.nchunks;
     p.splits = P->shape.splits;
     p.cps = shape_cps(P->shape, P->layout.nchunks);
-    p.wsplit = P->shape.wsplit;
     p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
     p.err = P->dev_err;
     p.zero = 0;
@@ -528,8 +603,14 @@ lbv_status lbv_verify_launch_internal(const lbv_plan* P, const void* X, int M, i
                                       const void* Wp, float* Y, int ldy, bool gemv,
                                       cudaStream_t st)
 {
-    const lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, ldy);
     cudaError_t e;
+    if (P->tc) {
+        e = lbv::tc_verify_launch(P, X, M, ldx, Wp, Y, ldy, (P->flags & LBV_PLAN_PDL) != 0, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "lbv_verify_gemm: launch");
+        return LBV_OK;
+    }
+    const lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, ldy);
     if (gemv) {
         e = cudaSuccess;
         for (int r = 0; r < M && e == cudaSuccess; ++r)
@@ -585,9 +666,11 @@ lbv_status lbv_dequant_fp16(const lbv_plan* P, const void* Wp, uint16_t* W, lbv_
         return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: null argument");
     if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0 || (reinterpret_cast<uintptr_t>(W) & 1u))
         return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: misaligned pointer");
-    cudaError_t e = lbv::launch_dequant(
-        P->fmt, P->group, static_cast<const uint8_t*>(Wp), P->K, P->N,
-        (int)P->layout.ntiles, (int)P->layout.nchunks, W, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        P->tc ? lbv::tc_dequant(P, Wp, W, reinterpret_cast<cudaStream_t>(stream))
+              : lbv::launch_dequant(P->fmt, P->group, static_cast<const uint8_t*>(Wp), P->K, P->N,
+                                    (int)P->layout.ntiles, (int)P->layout.nchunks, W,
+                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "lbv_dequant_fp16: launch");
     return LBV_OK;
@@ -663,36 +746,69 @@ lbv_status lbv_plan_measure_internal(lbv_plan* P)
     int l2 = 0;
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, P->device);
     s.flush_bytes = (size_t)std::max(l2, 1 << 20) * 2;
-    cudaError_t e = cudaMalloc(&s.w, P->layout.total);
+    cudaError_t e = cudaMalloc(&s.w, lbv_plan_packed_bytes(P));
     if (e == cudaSuccess) e = cudaMalloc(&s.x, (size_t)8 * P->K * 2);
     if (e == cudaSuccess) e = cudaMalloc((void**)&s.y, (size_t)8 * P->N * 4);
     if (e == cudaSuccess) e = cudaMalloc(&s.flush, s.flush_bytes);
-    if (e == cudaSuccess) e = cudaMemset(s.w, 0x5A, P->layout.total);
+    if (e == cudaSuccess) e = cudaMemset(s.w, 0x5A, lbv_plan_packed_bytes(P));
     if (e == cudaSuccess) e = cudaMemset(s.x, 0x11, (size_t)8 * P->K * 2);
     if (e != cudaSuccess)
         return cuda_fail(e, "plan measure: scratch");
     cudaStream_t st = nullptr;
     const int reps = 7;
 
-    // 1) few-row launch shape: every K split that fits
+    if (P->tc) {
+        // tcgen05 plans: every K split that fits; the kernel serves every M
+        lbv::TcShape best = P->tc_shape;
+        float best_us = 1e30f;
+        for (int sp = 1; sp <= 8; ++sp) {
+            if (!lbv::tc_set_shape(P, sp, 0) || P->tc_shape.splits != sp)
+                continue;
+            float us = 0.f;
+            lbv_status rc = time_cold(
+                [&] { return lbv_verify_launch_internal(P, s.x, 8, P->K, s.w, s.y, P->N, false, st); },
+                s, st, reps, &us);
+            if (rc != LBV_OK)
+                return rc;
+            if (us < best_us) {
+                best_us = us;
+                best = P->tc_shape;
+            }
+        }
+        lbv::tc_set_shape(P, best.splits, best.ctas_n);
+        for (int m = 1; m <= 8; ++m) {
+            float few = 0.f;
+            lbv_status rc = time_cold(
+                [&] { return lbv_verify_launch_internal(P, s.x, m, P->K, s.w, s.y, P->N, false, st); },
+                s, st, reps, &few);
+            if (rc != LBV_OK)
+                return rc;
+            P->measured_us[m][0] = few;
+        }
+        return LBV_OK;
+    }
+
+    // 1) few-row launch shape
     lbv::Shape best = P->shape;
     float best_us = 1e30f;
-    for (int sp = 1; sp <= 8; ++sp) {
-        lbv::Shape sh = {sp, 0, 1, 0};
-        if (!complete_shape(P, sh, 0) || sh.splits != sp)
-            continue;
-        P->shape = sh;
-        float us = 0.f;
-        lbv_status rc = time_cold(
-            [&] { return lbv_verify_launch_internal(P, s.x, 8, P->K, s.w, s.y, P->N, false, st); },
-            s, st, reps, &us);
-        if (rc != LBV_OK)
-            return rc;
-        if (us < best_us) {
-            best_us = us;
-            best = sh;
-        }
-    }
+    const int shapes_c[][2] = {{8, 2}, {8, 4}, {16, 1}, {16, 2}};
+    for (const auto& wt : shapes_c)
+            for (int sp = 1; sp <= 8; ++sp) {
+                lbv::Shape sh = {wt[0], wt[1], sp, 0, 0};
+                if (!complete_shape(P, sh, 0) || sh.splits != sp)
+                    continue;
+                P->shape = sh;
+                float us = 0.f;
+                lbv_status rc = time_cold(
+                    [&] { return lbv_verify_launch_internal(P, s.x, 8, P->K, s.w, s.y, P->N, false, st); },
+                    s, st, reps, &us);
+                if (rc != LBV_OK)
+                    return rc;
+                if (us < best_us) {
+                    best_us = us;
+                    best = sh;
+                }
+            }
     P->shape = best;
     complete_shape(P, P->shape, 0);
 

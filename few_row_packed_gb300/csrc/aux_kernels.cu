@@ -102,185 +102,222 @@ template <int FMT, int GROUP>
 struct AuxTraits;
 template <>
 struct AuxTraits<LBV_FMT_SIGN1_G128, 128> {
-    static constexpr int CK = 128, CB = 16, SB = 2, W = 1, GK = 128;
+    static constexpr int CK = 256, KT = 16, W = 1, SLOTS = 16, GK = 128, SIDE_W = 2;
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 template <int G>
 struct AuxTraits<LBV_FMT_AFFINE2, G> {
-    static constexpr int CK = G == 128 ? 128 : 64, CB = G == 128 ? 32 : 16, SB = G == 32 ? 8 : 4,
-                         W = 2, GK = G;
+    static constexpr int CK = 128, KT = 8, W = 2, SLOTS = 8, GK = G, SIDE_W = 2 * (128 / G);
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 template <>
 struct AuxTraits<LBV_FMT_Q4_0, 32> {
-    static constexpr int CK = 64, CB = 32, SB = 4, W = 4, GK = 32;
+    static constexpr int CK = 64, KT = 4, W = 4, SLOTS = 4, GK = 32, SIDE_W = 2;
+    static constexpr int REC = 512 + 8 * SIDE_W * 4;
 };
 
-template <int FMT, int GROUP>
-struct AuxGeo {
-    using A = AuxTraits<FMT, GROUP>;
-    static constexpr int PPW = 16 / A::W, NWORD = A::CB / 4, GPC = A::CK / A::GK;
-    static constexpr int REC = 128 * (A::CB + A::SB);
-};
+// fp16 of one scale/bias half of a side word: lo half = column g, hi = g + 8.
+__device__ __forceinline__ uint16_t side_half(uint32_t word, int hi)
+{
+    return hi ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFFu);
+}
 
 __device__ __forceinline__ float h2f(uint16_t b)
 {
     return __half2float(__ushort_as_half(b));
 }
 
-// The codes words and side values of column c (0..127) of one record.
-template <int FMT, int GROUP>
-__device__ __forceinline__ void read_column(const uint8_t* rec, int c,
-                                            uint32_t (&wv)[AuxGeo<FMT, GROUP>::NWORD],
-                                            uint16_t (&sv)[AuxTraits<FMT, GROUP>::SB / 2])
-{
-    using A = AuxTraits<FMT, GROUP>;
-#pragma unroll
-    for (int h = 0; h < A::CB / 16; ++h) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rec + h * 2048 + c * 16);
-        wv[4 * h + 0] = v.x;
-        wv[4 * h + 1] = v.y;
-        wv[4 * h + 2] = v.z;
-        wv[4 * h + 3] = v.w;
-    }
-#pragma unroll
-    for (int i = 0; i < A::SB / 2; ++i)
-        sv[i] = reinterpret_cast<const uint16_t*>(rec + 128 * A::CB + c * A::SB)[i];
-}
-
-// Code of pair-element (p, h) of a column: k = 2p + h within the chunk.
-template <int FMT, int GROUP>
-__device__ __forceinline__ uint32_t code_at(const uint32_t (&wv)[AuxGeo<FMT, GROUP>::NWORD], int p,
-                                            int h)
-{
-    using A = AuxTraits<FMT, GROUP>;
-    using Gm = AuxGeo<FMT, GROUP>;
-    return (wv[p / Gm::PPW] >> ((p % Gm::PPW) * A::W + 16 * h)) & ((1u << A::W) - 1u);
-}
-
 // ---------------------------------------------------------------------------
-// Dense fp16 dequant (test export): one thread per (tile, chunk, column).
+// Dense fp16 dequant (test export): one thread per (tile, chunk, lane).
 // sign1: +-s exactly; affine: s*q + b exact in fp64, rounded once; Q4_0:
 // d*(q-8) exact in fp32, rounded once.
 
 template <int FMT, int GROUP>
-__global__ void __launch_bounds__(128) lbv_dequant_kernel(const uint8_t* Wp, int K, int N,
+__global__ void __launch_bounds__(256) lbv_dequant_kernel(const uint8_t* Wp, int K, int N,
                                                           int ntiles, int nchunks, uint16_t* W)
 {
     using A = AuxTraits<FMT, GROUP>;
-    using Gm = AuxGeo<FMT, GROUP>;
-    const long long tc = blockIdx.x;                     // record index
-    const int c = threadIdx.x;
-    const int tile = (int)(tc / nchunks), chunk = (int)(tc - (long long)tile * nchunks);
-    const int col = tile * 128 + c;
-    if (col >= N)
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long total = (long long)ntiles * nchunks * 32;
+    if (idx >= total)
         return;
-    uint32_t wv[Gm::NWORD];
-    uint16_t sv[A::SB / 2];
-    read_column<FMT, GROUP>(Wp + (size_t)tc * Gm::REC, c, wv, sv);
-    for (int kk = 0; kk < A::CK; ++kk) {
-        const int k = chunk * A::CK + kk;
-        if (k >= K)
-            break;
-        const uint32_t code = code_at<FMT, GROUP>(wv, kk >> 1, kk & 1);
-        const int gi = kk / A::GK;
-        uint16_t out;
-        if constexpr (FMT == LBV_FMT_SIGN1_G128) {
-            out = code ? sv[0] : (uint16_t)(sv[0] ^ 0x8000u);
-        } else if constexpr (FMT == LBV_FMT_AFFINE2) {
-            const double sc = (double)h2f(sv[2 * gi]);
-            const double bi = (double)h2f(sv[2 * gi + 1]);
-            out = __half_as_ushort(__double2half(sc * (double)code + bi));
-        } else {
-            const float d = h2f(sv[gi]);
-            out = __half_as_ushort(__float2half_rn(d * (float)((int)code - 8)));
+    const int lane = (int)(idx & 31);
+    const long long tc = idx >> 5;
+    const int tile = (int)(tc / nchunks), chunk = (int)(tc - (long long)tile * nchunks);
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rec = Wp + (size_t)tc * A::REC;
+    const uint4 q = reinterpret_cast<const uint4*>(rec)[lane];
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
+    for (int wi = 0; wi < 4; ++wi) {
+        const int col = tile * 16 + g + 8 * (wi & 1);
+        const int hi = wi & 1;
+        const int half = wi >> 1;
+        if (col >= N)
+            continue;
+        for (int s = 0; s < A::SLOTS; ++s) {
+            const int kt = half * (A::KT / 2) + (s >> 1);
+            const int k0 = chunk * A::CK + 16 * kt + 8 * (s & 1) + 2 * t;
+            const int gi = (16 * kt) / A::GK;        // group within the chunk
+            for (int h = 0; h < 2; ++h) {
+                const int k = k0 + h;
+                if (k >= K)
+                    continue;
+                const uint32_t code = (wv[wi] >> (s * A::W + 16 * h)) & ((1u << A::W) - 1u);
+                uint16_t out;
+                if constexpr (FMT == LBV_FMT_SIGN1_G128) {
+                    const uint16_t sb = side_half(sw[gi], hi);
+                    out = code ? sb : (uint16_t)(sb ^ 0x8000u);
+                } else if constexpr (FMT == LBV_FMT_AFFINE2) {
+                    const double sc = (double)h2f(side_half(sw[2 * gi], hi));
+                    const double bi = (double)h2f(side_half(sw[2 * gi + 1], hi));
+                    out = __half_as_ushort(__double2half(sc * (double)code + bi));
+                } else {
+                    const float d = h2f(side_half(sw[gi], hi));
+                    out = __half_as_ushort(__float2half_rn(d * (float)((int)code - 8)));
+                }
+                W[(size_t)k * N + col] = out;
+            }
         }
-        W[(size_t)k * N + col] = out;
     }
 }
 
 cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, int N,
                            int ntiles, int nchunks, uint16_t* W, cudaStream_t st)
 {
-    const dim3 grid((unsigned)((long long)ntiles * nchunks));
+    const long long total = (long long)ntiles * nchunks * 32;
+    const dim3 grid((unsigned)((total + 255) / 256));
     switch (fmt) {
     case LBV_FMT_SIGN1_G128:
-        lbv_dequant_kernel<LBV_FMT_SIGN1_G128, 128><<<grid, 128, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
+        lbv_dequant_kernel<LBV_FMT_SIGN1_G128, 128>
+            <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     case LBV_FMT_AFFINE2:
         if (group == 32)
-            lbv_dequant_kernel<LBV_FMT_AFFINE2, 32><<<grid, 128, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 32>
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         else if (group == 64)
-            lbv_dequant_kernel<LBV_FMT_AFFINE2, 64><<<grid, 128, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 64>
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         else
-            lbv_dequant_kernel<LBV_FMT_AFFINE2, 128><<<grid, 128, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
+            lbv_dequant_kernel<LBV_FMT_AFFINE2, 128>
+                <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     case LBV_FMT_Q4_0:
-        lbv_dequant_kernel<LBV_FMT_Q4_0, 32><<<grid, 128, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
+        lbv_dequant_kernel<LBV_FMT_Q4_0, 32>
+            <<<grid, 256, 0, st>>>(Wp, K, N, ntiles, nchunks, W);
         break;
     }
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// 1-row path (the plain decode step): one thread per output column over all
-// of K, fp32 FMAs on the FMA pipe, run once per row.  A warp reads 32
-// consecutive columns' records (coalesced); X is read through the L1 cache.
+// 1-row path (the plain decode step): one warp per 16-column tile over all of
+// K, fp32 FMAs on the FMA pipe, run once per row.  Each lane decodes the same
+// codes the few-row kernel's lane does; the 4 lanes of a column pair reduce
+// by shuffles.
 
 template <int DT>
-__device__ __forceinline__ float x_at(const uint16_t* x, int k)
+__device__ __forceinline__ float2 x_pair(const uint16_t* x, int k)
 {
-    if constexpr (DT == LBV_F16)
-        return __half2float(__ushort_as_half(x[k]));
-    else
-        return __bfloat162float(__ushort_as_bfloat16(x[k]));
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(x + k);   // k even
+    if constexpr (DT == LBV_F16) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&v));
+    } else {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    }
 }
 
 template <int FMT, int DT, int GROUP>
-__global__ void __launch_bounds__(128) lbv_gemv_kernel(const VerifyParams p, int row)
+__global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int row)
 {
     using A = AuxTraits<FMT, GROUP>;
-    using Gm = AuxGeo<FMT, GROUP>;
-    const int tile = blockIdx.x, c = threadIdx.x;
-    const int col = tile * 128 + c;
+    constexpr int KTG = A::GK / 16;                  // k-tiles per scale group
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int tile = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (tile >= p.ntiles)
+        return;
     const uint16_t* x = reinterpret_cast<const uint16_t*>(p.X) + (size_t)row * p.ldx;
-    float y = 0.f;
+    float y0 = 0.f, y1 = 0.f;                        // columns g and g + 8
     for (int chunk = 0; chunk < p.nchunks; ++chunk) {
-        uint32_t wv[Gm::NWORD];
-        uint16_t sv[A::SB / 2];
-        read_column<FMT, GROUP>(p.W + ((size_t)tile * p.nchunks + chunk) * Gm::REC, c, wv, sv);
+        const size_t tc = (size_t)tile * p.nchunks + chunk;
+        const uint8_t* rec = p.W + tc * A::REC;
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
 #pragma unroll
-        for (int gi = 0; gi < Gm::GPC; ++gi) {
-            float a = 0.f, r = 0.f;
-#pragma unroll 8
-            for (int kk = gi * A::GK; kk < (gi + 1) * A::GK; ++kk) {
-                const int k = chunk * A::CK + kk;
-                const float xv = k < p.K ? x_at<DT>(x, k) : 0.f;
-                const uint32_t code = code_at<FMT, GROUP>(wv, kk >> 1, kk & 1);
-                if constexpr (FMT == LBV_FMT_SIGN1_G128)
-                    a += code ? xv : -xv;
-                else if constexpr (FMT == LBV_FMT_AFFINE2) {
-                    a = fmaf((float)code, xv, a);
-                    r += xv;
-                } else
-                    a = fmaf((float)((int)code - 8), xv, a);
+        for (int half = 0; half < 2; ++half) {
+            // k-tiles of this half, grouped by scale group
+#pragma unroll
+            for (int kt0 = 0; kt0 < A::KT / 2; kt0 += (KTG < A::KT / 2 ? KTG : A::KT / 2)) {
+                float a0 = 0.f, a1 = 0.f, r = 0.f;   // column g, column g + 8, row sum
+                constexpr int span = KTG < A::KT / 2 ? KTG : A::KT / 2;
+#pragma unroll
+                for (int kk = 0; kk < span; ++kk) {
+                    const int ktl = kt0 + kk;
+                    const int kt = half * (A::KT / 2) + ktl;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int s = 2 * ktl + rr;
+                        const int k = chunk * A::CK + 16 * kt + 8 * rr + 2 * t;
+                        float2 xv = make_float2(0.f, 0.f);
+                        if (k < p.K)
+                            xv = x_pair<DT>(x, k);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float xs = h ? xv.y : xv.x;
+                            const int sh = s * A::W + 16 * h;
+                            const uint32_t c0 = (wv[2 * half] >> sh) & ((1u << A::W) - 1u);
+                            const uint32_t c1 = (wv[2 * half + 1] >> sh) & ((1u << A::W) - 1u);
+                            if constexpr (FMT == LBV_FMT_SIGN1_G128) {
+                                a0 += c0 ? xs : -xs;
+                                a1 += c1 ? xs : -xs;
+                            } else if constexpr (FMT == LBV_FMT_AFFINE2) {
+                                a0 = fmaf((float)c0, xs, a0);
+                                a1 = fmaf((float)c1, xs, a1);
+                                r += xs;
+                            } else {
+                                a0 = fmaf((float)((int)c0 - 8), xs, a0);
+                                a1 = fmaf((float)((int)c1 - 8), xs, a1);
+                            }
+                        }
+                    }
+                }
+                const int gi = (16 * (half * (A::KT / 2) + kt0)) / A::GK;
+                if constexpr (FMT == LBV_FMT_AFFINE2) {
+                    const uint32_t sc = sw[2 * gi], bi = sw[2 * gi + 1];
+                    y0 = fmaf(h2f(side_half(sc, 0)), a0, fmaf(h2f(side_half(bi, 0)), r, y0));
+                    y1 = fmaf(h2f(side_half(sc, 1)), a1, fmaf(h2f(side_half(bi, 1)), r, y1));
+                } else {
+                    const uint32_t sc = sw[gi];
+                    y0 = fmaf(h2f(side_half(sc, 0)), a0, y0);
+                    y1 = fmaf(h2f(side_half(sc, 1)), a1, y1);
+                }
             }
-            if constexpr (FMT == LBV_FMT_AFFINE2)
-                y = fmaf(h2f(sv[2 * gi]), a, fmaf(h2f(sv[2 * gi + 1]), r, y));
-            else
-                y = fmaf(h2f(sv[gi]), a, y);
         }
     }
-    if (col < p.N)
-        p.Y[(size_t)row * p.ldy + col] = y;
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t == 0) {
+        const int n0 = tile * 16 + g, n1 = n0 + 8;
+        float* yr = p.Y + (size_t)row * p.ldy;
+        if (n0 < p.N)
+            yr[n0] = y0;
+        if (n1 < p.N)
+            yr[n1] = y1;
+    }
 }
 
 template <int FMT, int GROUP>
 static cudaError_t gemv_t(lbv_dtype xt, const VerifyParams& p, int row, cudaStream_t st)
 {
-    const dim3 grid((unsigned)p.ntiles);
+    const dim3 grid((unsigned)((p.ntiles + 7) / 8));
     if (xt == LBV_F16)
-        lbv_gemv_kernel<FMT, LBV_F16, GROUP><<<grid, 128, 0, st>>>(p, row);
+        lbv_gemv_kernel<FMT, LBV_F16, GROUP><<<grid, 256, 0, st>>>(p, row);
     else
-        lbv_gemv_kernel<FMT, LBV_BF16, GROUP><<<grid, 128, 0, st>>>(p, row);
+        lbv_gemv_kernel<FMT, LBV_BF16, GROUP><<<grid, 256, 0, st>>>(p, row);
     return cudaGetLastError();
 }
 

@@ -1,26 +1,31 @@
 // layout.h -- the library's device layout of packed weights, shared by the
-// host packer (api.cpp) and the kernels.  Lossless: the same bits as the
-// canonical file layout, rearranged so that one thread owns one output column
-// and finds a chunk of that column's codes in 16 or 32 contiguous bytes.
+// host packer (pack.cpp) and the kernels.  Lossless: the same bits as the
+// canonical file layout, rearranged so that one 16-byte load per lane gives a
+// warp exactly the mma.sync m16n8k16 A-fragment bits of one 16-column tile.
 //
 // Terms
-//   tile   128 output columns n = 128*tile .. 128*tile+127: the M side of one
-//          tcgen05 MMA (the M <= 8 activation rows are the N side).
-//   chunk  CK consecutive K values of a column: 128 (sign1), 64 (affine2 g32
-//          and g64, Q4_0) or 128 (affine2 g128).  CB = 16 or 32 code bytes.
-//   pair   the two weights k = 2p and 2p + 1 of a column: one 32-bit register
-//          of two fp16/bf16 values in the MMA's A operand.
+//   tile   16 output columns n = 16*tile .. 16*tile+15 (the m16 side of the
+//          tensor-core tile; the M <= 8 activation rows are the n8 side).
+//   chunk  the K range one 16-byte load per lane covers for one tile:
+//          256 K (sign1), 128 K (affine2), 64 K (Q4_0); 512 bytes per tile.
+//   lane   warp lane = 4*g + t, g = lane >> 2 in 0..7, t = lane & 3.
 //
-// Records: one record of REC = 128 * (CB + SB) bytes per (tile, chunk), in
-// tile-major order (record index tile * nchunks + chunk):
-//   codes: [CB / 16][128 columns][16 bytes].  The CB bytes of a column are
-//          CB / 4 little-endian words; word j holds pairs p = PPW*j + s for
-//          s = 0..PPW-1 (PPW = 16 / W pairs per word, W = bits per code): the
-//          code of k = 2p sits at bit s*W of the low half-word and the code of
-//          k = 2p + 1 at bit 16 + s*W.
-//   side:  [128 columns][SB bytes] of fp16 bit patterns, per scale group j of
-//          the chunk: sign1: scale (SB = 2); affine2: scale, bias (4 bytes per
-//          group; SB = 4, or 8 for g32); Q4_0: d (2 bytes per block, SB = 4).
+// Records: one record of REC = 512 + 8 * SB bytes per (tile, chunk), in
+// tile-major order (record index tile * nchunks + chunk), so the chunks of a
+// tile are contiguous.  A record holds
+//   codes: uint4 [32 lanes] (512 bytes).  Word wi (0..3) of lane (g, t)
+//          belongs to column 16*tile + g + 8*(wi & 1) and covers the chunk's
+//          k-tiles (wi >> 1) * KT/2 .. + KT/2 - 1 (KT = chunk / 16).  Slot s
+//          of that word is k-tile ktl = s >> 1 of the half and r = s & 1,
+//          i.e. the two weights k0 = 16*kt + 8*r + 2*t and k0 + 1 -- the
+//          element pair the A-fragment register for (column, kt, r) holds.
+//          The code of k0 sits at bit s*W (W = 1, 2, 4 bits) of the low
+//          half-word and the code of k0 + 1 at bit 16 + s*W.
+//   side:  uint8 [8 g][SB] of fp16 bit patterns:
+//          sign1   : per group j (2 per chunk): scale(col g), scale(col g+8)
+//          affine2 : per group j (128/g per chunk): scale(g), scale(g+8),
+//                    bias(g), bias(g+8)
+//          Q4_0    : per block j (2 per chunk): d(col g), d(col g+8)
 // Padding columns (n >= N) and K positions (k >= K) have zero codes and zero
 // scales, so they contribute exactly 0.
 #pragma once
@@ -32,47 +37,47 @@
 
 namespace lbv {
 
-constexpr int kTileN = 128;
-
 struct FmtInfo {
-    int chunk_k;      // K per chunk (CK)
-    int code_bytes;   // code bytes per column and chunk (CB)
-    int side_bytes;   // side bytes per column and chunk (SB)
-    int code_bits;    // W
+    int chunk_k;      // K per chunk
+    int kt;           // k-tiles (16 K) per chunk
+    int code_bits;    // bits per code
+    int slots;        // slots per 32-bit word
     int group_k;      // K per scale group
+    int groups;       // scale groups per chunk
+    int side_bytes;   // side bytes per (tile, chunk, g)
 };
 
 inline bool fmt_info(lbv_format fmt, int group, FmtInfo* fi)
 {
     switch (fmt) {
     case LBV_FMT_SIGN1_G128:
-        *fi = {128, 16, 2, 1, 128};
+        *fi = {256, 16, 1, 16, 128, 2, 8};
         return true;
     case LBV_FMT_AFFINE2:
-        if (group == 32) { *fi = {64, 16, 8, 2, 32}; return true; }
-        if (group == 64) { *fi = {64, 16, 4, 2, 64}; return true; }
-        if (group == 128) { *fi = {128, 32, 4, 2, 128}; return true; }
-        return false;
+        if (group != 32 && group != 64 && group != 128)
+            return false;
+        *fi = {128, 8, 2, 8, group, 128 / group, (128 / group) * 8};
+        return true;
     case LBV_FMT_Q4_0:
-        *fi = {64, 32, 4, 4, 32};
+        *fi = {64, 4, 4, 4, 32, 2, 8};
         return true;
     }
     return false;
 }
 
 struct Layout {
-    int64_t ntiles;        // ceil(N / 128)
+    int64_t ntiles;        // ceil(N / 16)
     int64_t nchunks;       // ceil(K / chunk_k)
-    size_t rec_bytes;      // 128 * (CB + SB)
+    size_t rec_bytes;      // 512 + 8 * side_bytes
     size_t total;          // ntiles * nchunks * rec_bytes
 };
 
 inline Layout make_layout(const FmtInfo& fi, int K, int N)
 {
     Layout L;
-    L.ntiles = (N + kTileN - 1) / kTileN;
+    L.ntiles = (N + 15) / 16;
     L.nchunks = (K + fi.chunk_k - 1) / fi.chunk_k;
-    L.rec_bytes = (size_t)kTileN * (size_t)(fi.code_bytes + fi.side_bytes);
+    L.rec_bytes = 512u + 8u * (size_t)fi.side_bytes;
     L.total = (size_t)L.ntiles * (size_t)L.nchunks * L.rec_bytes;
     return L;
 }

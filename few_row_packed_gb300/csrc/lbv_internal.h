@@ -5,11 +5,9 @@
 #include <cuda_runtime.h>
 
 #include "layout.h"
+#include "tc_layout.h"
 
 namespace lbv {
-
-// Decode warpgroups per CTA of the few-row kernel.
-constexpr int kTcWarpgroups = 3;
 
 // Parameters of one few-row verify launch (passed by value to the kernel).
 struct VerifyParams {
@@ -22,18 +20,24 @@ struct VerifyParams {
     int ntiles, nchunks;
     int splits;             // K slices == cluster size along grid x
     int cps;                // chunks per slice (the last slice may be shorter)
-    int wsplit;             // warpgroup split of a slice inside a CTA (divides kTcWarpgroups)
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
     unsigned zero;          // always 0 (keeps decode constants in registers)
 };
 
 // Launch shape of the few-row kernel.
 struct Shape {
+    int warps;              // 8 or 16
+    int tpw;                // column tiles per warp unit, 1 or 2
     int splits;             // K slices (cluster size), 1..8
     int ctas_n;             // clusters along N (grid y); each owns a contiguous tile range
-    int wsplit;             // warpgroups sharing one tile inside a CTA (split of the slice)
     size_t smem;            // dynamic shared memory bytes
 };
+
+// Dynamic shared-memory limit set on every few-row kernel function: the
+// largest any plan may request, so plans of one kernel with different shapes
+// never lower each other's limit (the attribute is per function, not per
+// launch).
+constexpr int kMaxDynSmem = 220 * 1024;
 
 struct LaunchOpts {
     bool pdl;               // programmatic dependent launch
@@ -64,4 +68,9 @@ struct lbv_plan {
     int crossover;           // smallest M that uses the few-row kernel
     unsigned* dev_err;       // device status word (set when a bounded wait gives up)
     float measured_us[9][2]; // per M: [few-row, 1-row x M] (LBV_PLAN_MEASURE), else 0
+    // plans created with LBV_PLAN_TCGEN05: the tcgen05 kernel and its layout
+    int tc;
+    lbv::TcFmtInfo tc_fi;
+    lbv::TcLayout tc_layout;
+    lbv::TcShape tc_shape;
 };

@@ -1,5 +1,5 @@
 // tc_kernel.cuh -- the few-row verify kernel on the 5th-generation tensor
-// cores: Y[M,N] = X[M,K] . W[K,N], M <= 8, for the packed formats of layout.h.
+// cores: Y[M,N] = X[M,K] . W[K,N], M <= 8, for the packed formats of tc_layout.h.
 //
 // Design (GB300, sm_103a):
 //   * Persistent grid of thread-block clusters.  Cluster y owns a contiguous,
@@ -46,7 +46,7 @@
 
 #include <utility>
 
-#include "lbv_internal.h"
+#include "tc_internal.h"
 
 namespace lbv {
 
@@ -168,7 +168,7 @@ __device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[n
 }
 
 // ---------------------------------------------------------------------------
-// Per-format constants (see layout.h)
+// Per-format constants (see tc_layout.h)
 
 template <int FMT, int GROUP>
 struct TcTraits;
@@ -484,7 +484,7 @@ struct TcKernel {
     static constexpr int NB = num_bases<FMT>();
 
     struct Ctx {
-        const VerifyParams* p;
+        const TcParams* p;
         unsigned char* smem;
         TcSmem<FMT, GROUP> lay;
         uint32_t tmem;
@@ -528,7 +528,7 @@ struct TcKernel {
     // ---- prologue: X slice as the B operand, per-group corrections ----
     static __device__ void stage_x(const Ctx& c, int tid)
     {
-        const VerifyParams& p = *c.p;
+        const TcParams& p = *c.p;
         const int kb = c.c0 * T::CK;
         const int nks = c.nch * G::KSTEPS;
         const int pieces = nks * 2 * 8;                 // (k-step, core, row) 16-byte pieces
@@ -620,7 +620,7 @@ struct TcKernel {
     static __device__ __forceinline__ void produce(const Ctx& c, const Work& w, int wg, int q,
                                                    int lane)
     {
-        const VerifyParams& p = *c.p;
+        const TcParams& p = *c.p;
         const int u = q / w.nchw, cl = q - u * w.nchw;
         const int tile = c.t0 + w.tl + w.TL * u;
         const uint8_t* src = p.W + ((size_t)tile * p.nchunks + c.c0 + w.cw0 + cl) * G::REC;
@@ -893,7 +893,7 @@ struct TcKernel {
     static __device__ __forceinline__ void store_tile(const Ctx& c, const Work& w, int tile, int col,
                                                       const float (&y)[8], float* part)
     {
-        const VerifyParams& p = *c.p;
+        const TcParams& p = *c.p;
         const int np = c.S * c.SW;
         if (np > 1) {
             const int i = tile - c.t0;
@@ -916,7 +916,7 @@ struct TcKernel {
 
     static __device__ void reduce_parts(const Ctx& c, int tid, int nthreads)
     {
-        const VerifyParams& p = *c.p;
+        const TcParams& p = *c.p;
         const float* part = reinterpret_cast<const float*>(c.smem + c.lay.part);
         const int S = c.S, np = S * c.SW;
         const int nown = (c.t1 - c.t0 - c.rank + S - 1) / S;     // tiles t0 + rank + S*k
@@ -933,7 +933,7 @@ struct TcKernel {
         }
     }
 
-    static __device__ void run(const VerifyParams& p, unsigned char* smem)
+    static __device__ void run(const TcParams& p, unsigned char* smem)
     {
         const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
         Ctx c;
@@ -1025,7 +1025,7 @@ struct TcKernel {
 };
 
 template <int FMT, int XT, int GROUP>
-__global__ void __launch_bounds__(TcGeo<FMT, GROUP>::THREADS, 1) lbv_tc_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(TcGeo<FMT, GROUP>::THREADS, 1) lbv_tc_kernel(const TcParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     TcKernel<FMT, XT, GROUP>::run(p, smem);
@@ -1040,7 +1040,7 @@ inline size_t tc_smem_bytes(int cps, int owned_max, int nparts)
     return TcSmem<FMT, GROUP>(cps, owned_max, nparts).total;
 }
 
-inline void tc_fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const Shape& sh,
+inline void tc_fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const TcShape& sh,
                            int threads, bool pdl, cudaStream_t st)
 {
     cfg = {};
@@ -1066,32 +1066,33 @@ inline void tc_fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[
 }
 
 template <int FMT, int XT, int GROUP>
-inline cudaError_t tc_launch_t(const Shape& sh, const VerifyParams& p, const LaunchOpts& o,
+inline cudaError_t tc_launch_t(const TcShape& sh, const TcParams& p, const LaunchOpts& o,
                                cudaStream_t st)
 {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     tc_fill_config(cfg, attr, sh, TcGeo<FMT, GROUP>::THREADS, o.pdl, st);
-    void* args[] = {const_cast<VerifyParams*>(&p)};
+    void* args[] = {const_cast<TcParams*>(&p)};
     return cudaLaunchKernelExC(&cfg, (void*)lbv_tc_kernel<FMT, XT, GROUP>, args);
 }
 
 template <int FMT, int XT, int GROUP>
-inline cudaError_t tc_prepare_t(const Shape& sh)
+inline cudaError_t tc_prepare_t(const TcShape& sh)
 {
     return cudaFuncSetAttribute((void*)lbv_tc_kernel<FMT, XT, GROUP>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sh.smem > kMaxDynSmem ? (int)sh.smem : kMaxDynSmem);
 }
 
 template <int FMT, int XT, int GROUP>
-inline int tc_max_clusters_t(const Shape& sh)
+inline int tc_max_clusters_t(const TcShape& sh)
 {
     if (tc_prepare_t<FMT, XT, GROUP>(sh) != cudaSuccess)
         return 0;
     void* k = (void*)lbv_tc_kernel<FMT, XT, GROUP>;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    Shape s1 = sh;
+    TcShape s1 = sh;
     s1.ctas_n = 1;
     tc_fill_config(cfg, attr, s1, TcGeo<FMT, GROUP>::THREADS, false, nullptr);
     int n = 0;

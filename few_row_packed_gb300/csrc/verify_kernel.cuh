@@ -1,0 +1,952 @@
+// verify_kernel.cuh -- the few-row verify kernel, Y[M,N] = X[M,K] . W[K,N],
+// M <= 8, for the packed formats of layout.h.
+//
+// Design (GB300, sm_103a):
+//   * Persistent grid of thread-block clusters.  Cluster y owns a contiguous,
+//     balanced range of 16-column tiles; the S CTAs of a cluster split K into
+//     slices, and their partial sums are reduced through distributed shared
+//     memory in rank order (deterministic, no workspace).
+//   * Each CTA stages its K slice of X once, in mma fragment order, with the
+//     per-group corrections (below).  X is read only after griddepcontrol.wait;
+//     the packed weights, which no kernel writes, start streaming before it.
+//   * Each warp streams its tiles' packed codes and scales through a private
+//     ring of shared-memory stages filled by 1-D bulk async copies (TMA engine)
+//     and tracked by mbarriers, so a few tens of KB per SM stay in flight with
+//     no registers held.  Every wait is bounded; a wait that gives up sets the
+//     plan's status word and the warp stops.
+//   * Decode is one LOP3 per A-fragment register: (word_variant & mask) ^ base
+//     places a code in the mantissa/exponent field of an fp16 or bf16 whose
+//     value is  code_value + c  for a small integer c fixed by the bit position
+//     (the "codes turned into exact halves with 0x6400 less 1024" idea of the
+//     Ishizuki README credits, extended to every position of the word); 1-3
+//     shifts per 32-bit word bring the remaining positions into place.
+//   * mma.sync m16n8k16 (fp16 or bf16 in, fp32 accumulate): 16 weight columns
+//     are the M side and the M <= 8 activation rows the N side (rows >= M are
+//     zero), so each decoded weight meets every drafted row at once (Ishizuki
+//     README, "Kernels written for the verify").  The k-tiles of a chunk are
+//     issued alternately from two independent accumulator chains.
+//   * The offsets c enter each group's accumulator as its initial value
+//     -sum_k c_k x_k, computed once per CTA from the staged activations (the
+//     "row-sum prep" of the dflash-mlx-bonsai2 README); the group scale (and
+//     bias * row sum for affine) is applied in fp32 once per group, so every
+//     tensor-core operand is an exact small integer.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <utility>
+
+#include "lbv_internal.h"
+
+namespace lbv {
+
+namespace cg = cooperative_groups;
+
+template <int FMT, int GROUP>
+struct Traits;
+
+template <>
+struct Traits<LBV_FMT_SIGN1_G128, 128> {
+    static constexpr int CHUNK_K = 256, KT = 16, W = 1, GPC = 2, KTG = 8, SIDE_W = 2;
+    static constexpr bool AFFINE = false;
+};
+template <int G>
+struct Traits<LBV_FMT_AFFINE2, G> {
+    static constexpr int CHUNK_K = 128, KT = 8, W = 2, GPC = 128 / G, KTG = G / 16,
+                         SIDE_W = 2 * (128 / G);
+    static constexpr bool AFFINE = true;
+};
+template <>
+struct Traits<LBV_FMT_Q4_0, 32> {
+    static constexpr int CHUNK_K = 64, KT = 4, W = 4, GPC = 2, KTG = 2, SIDE_W = 2;
+    static constexpr bool AFFINE = false;
+};
+
+// ---------------------------------------------------------------------------
+// Decode specification of slot s of a word: shift the word (positive = left),
+// then keep the W-bit field at `target` (and target + 16) and XOR `base`.
+// The resulting fp16/bf16 value is  code_value + c.
+struct DecSpec {
+    int shift;
+    int target;
+    uint32_t base;   // 16-bit pattern, replicated into both halves
+    int c;
+    int bid;         // index of `base` among the format's distinct bases
+};
+
+// 1-bit sign: value = w + c with w = +-1 (bit 1 -> +1).
+//   fp16 targets: 15 (base -1.0, c 0), 14 (0, 1), 10 (2.0, 3), 9..5 (2^(11-j), 2^(11-j)+1)
+//   bf16 targets: 15 (-1.0, 0), 14 (0, 1), 7 (2.0, 3), 6..2 (2^(8-j), 2^(8-j)+1)
+__host__ __device__ constexpr DecSpec sign1_spec(int xt, int s)
+{
+    if (xt == LBV_F16) {
+        // left shifts only: slots 0-4 -> 5-9, 11-12 -> 14-15, 13 -> 14
+        const int sh = (s <= 4) ? 5 : (s == 11 || s == 12) ? 3 : (s == 13) ? 1 : 0;
+        const int j = s + sh;
+        return j == 15   ? DecSpec{sh, j, 0xBC00u, 0, 0}
+               : j == 14 ? DecSpec{sh, j, 0x0000u, 1, 1}
+               : j == 10 ? DecSpec{sh, j, 0x4000u, 3, 2}
+               : j == 9  ? DecSpec{sh, j, 0x4400u, 5, 3}
+               : j == 8  ? DecSpec{sh, j, 0x4800u, 9, 4}
+               : j == 7  ? DecSpec{sh, j, 0x4C00u, 17, 5}
+               : j == 6  ? DecSpec{sh, j, 0x5000u, 33, 6}
+                         : DecSpec{sh, j, 0x5400u, 65, 7};   // j == 5
+    } else {
+        const int sh = (s <= 1) ? 5 : (s >= 8 && s <= 13) ? -6 : 0;
+        const int j = s + sh;
+        return j == 15   ? DecSpec{sh, j, 0xBF80u, 0, 0}
+               : j == 14 ? DecSpec{sh, j, 0x0000u, 1, 1}
+               : j == 7  ? DecSpec{sh, j, 0x4000u, 3, 2}
+               : j == 6  ? DecSpec{sh, j, 0x4080u, 5, 3}
+               : j == 5  ? DecSpec{sh, j, 0x4100u, 9, 4}
+               : j == 4  ? DecSpec{sh, j, 0x4180u, 17, 5}
+               : j == 3  ? DecSpec{sh, j, 0x4200u, 33, 6}
+                         : DecSpec{sh, j, 0x4280u, 65, 7};   // j == 2
+    }
+}
+
+// 2-bit affine code q at bits 2s: value = q + c.
+//   fp16 targets 4 (64.0, c 64), 6 (16.0, 16), 8 (4.0, 4)
+//   bf16 targets 1 (64.0, 64), 3 (16.0, 16), 5 (4.0, 4)
+__host__ __device__ constexpr DecSpec affine2_spec(int xt, int s)
+{
+    if (xt == LBV_F16) {
+        const int sh = (s <= 1) ? 4 : (s <= 4) ? 0 : -6;
+        const int j = 2 * s + sh;
+        return j == 4 ? DecSpec{sh, j, 0x5400u, 64, 0}
+               : j == 6 ? DecSpec{sh, j, 0x4C00u, 16, 1}
+                        : DecSpec{sh, j, 0x4400u, 4, 2};
+    } else {
+        const int sh = (s <= 2) ? 1 : (s <= 5) ? -5 : -11;
+        const int j = 2 * s + sh;
+        return j == 1 ? DecSpec{sh, j, 0x4280u, 64, 0}
+               : j == 3 ? DecSpec{sh, j, 0x4180u, 16, 1}
+                        : DecSpec{sh, j, 0x4080u, 4, 2};
+    }
+}
+
+// Q4_0 nibble q at bits 4s: value = q + c, one target per dtype.
+//   fp16: target 4, base 64.0, c 64;  bf16: target 3, base 16.0, c 16
+__host__ __device__ constexpr DecSpec q4_0_spec(int xt, int s)
+{
+    return xt == LBV_F16 ? DecSpec{4 - 4 * s, 4, 0x5400u, 64, 0}
+                         : DecSpec{3 - 4 * s, 3, 0x4180u, 16, 0};
+}
+
+template <int FMT>
+__host__ __device__ constexpr DecSpec dec_spec(int xt, int s)
+{
+    return FMT == LBV_FMT_SIGN1_G128 ? sign1_spec(xt, s)
+           : FMT == LBV_FMT_AFFINE2  ? affine2_spec(xt, s)
+                                     : q4_0_spec(xt, s);
+}
+
+// Distinct XOR bases of a format (kept in registers: one LOP3 per decode).
+template <int FMT>
+__host__ __device__ constexpr int num_bases()
+{
+    return FMT == LBV_FMT_SIGN1_G128 ? 8 : FMT == LBV_FMT_AFFINE2 ? 3 : 1;
+}
+
+template <int FMT>
+__host__ __device__ constexpr uint32_t base_of(int xt, int bid)
+{
+    uint32_t b = 0;
+    for (int s = 0; s < 16; ++s)
+        if (dec_spec<FMT>(xt, s).bid == bid)
+            b = dec_spec<FMT>(xt, s).base;
+    return b | (b << 16);
+}
+
+template <int FMT, int XT, int S>
+__device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[num_bases<FMT>()])
+{
+    constexpr DecSpec d = dec_spec<FMT>(XT, S);
+    constexpr int W = Traits<FMT, FMT == LBV_FMT_SIGN1_G128 ? 128 : FMT == LBV_FMT_Q4_0 ? 32 : 64>::W;
+    constexpr uint32_t field = (1u << W) - 1u;
+    constexpr uint32_t mask = (field << d.target) | (field << (d.target + 16));
+    constexpr int shl = d.shift > 0 ? (d.shift > 31 ? 31 : d.shift) : 0;
+    constexpr int shr = d.shift < 0 ? (-d.shift > 31 ? 31 : -d.shift) : 0;
+    const uint32_t v = shl ? (w << shl) : shr ? (w >> shr) : w;
+    // (v & mask) ^ base as one LOP3 with an immediate mask: written in C, the
+    // compiler splits it into two logic operations.
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(r) : "r"(v), "n"(mask), "r"(bases[d.bid]));
+    return r;
+}
+
+
+// ---------------------------------------------------------------------------
+// Device helpers
+
+template <int XT>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    if constexpr (XT == LBV_F16) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+            "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+            "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Cluster barrier halves: every CTA arrives once it runs; waiting on that
+// phase guarantees all peers have started before their shared memory is
+// written.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Single-lane issue without divergence: the operation runs only where
+// `pred` is nonzero.
+__device__ __forceinline__ void mbar_expect_tx_if(uint32_t pred, uint32_t bar, uint32_t bytes)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n}\n"
+                 ::"r"(pred), "r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_if(uint32_t pred, uint32_t dst, const void* src,
+                                            uint32_t bytes, uint32_t bar)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%1], [%2], %3, [%4];\n}\n"
+                 ::"r"(pred), "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_if(uint32_t pred)
+{
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+                 " @q fence.proxy.async.shared::cta;\n}\n" ::"r"(pred)
+                 : "memory");
+}
+
+// One try of an mbarrier phase wait (true if the phase has completed).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  Returns false if it did
+// not complete within roughly a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    constexpr uint32_t kSpin = 1u << 12, kLimit = 1u << 20;
+    for (uint32_t i = 0; i < kLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if (i >= kSpin)
+            __nanosleep(1000);
+    }
+    return false;
+}
+
+template <int XT>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t v)
+{
+    if constexpr (XT == LBV_F16) {
+        __half2 h = *reinterpret_cast<__half2*>(&v);
+        return __half22float2(h);
+    } else {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+        return __bfloat1622float2(h);
+    }
+}
+
+__device__ __forceinline__ float2 f16pair(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
+}
+
+// ---------------------------------------------------------------------------
+// Compile-time geometry of one (format, group, warps, tiles-per-warp) kernel.
+
+template <int FMT, int GROUP, int NW, int TPW>
+struct Geometry {
+    using T = Traits<FMT, GROUP>;
+    static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (record, g)
+    static constexpr int REC = 512 + 8 * SIDE_B;              // record bytes (tile, chunk)
+    static constexpr int CPS = 2;                             // chunks per ring stage
+    static constexpr int SLOT_B = TPW * CPS * REC;            // one ring stage
+    static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
+    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
+    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8;
+    // corrections and row sums per group of the slice
+    static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
+};
+
+// Shared memory carve-up (bytes):
+//   ring | mbarriers | xf (X fragments) | corr | rsum (affine) | part (K split)
+template <int FMT, int GROUP, int NW, int TPW>
+__host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
+{
+    using G = Geometry<FMT, GROUP, NW, TPW>;
+    using T = Traits<FMT, GROUP>;
+    size_t b = G::RING_B + G::BAR_B;
+    b += (size_t)cps * T::KT * 256u;
+    b += (size_t)cps * T::GPC * 8 * 4 * G::CORR_ARRAYS;
+    if (splits > 1)
+        b += (size_t)((tiles_max + splits - 1) / splits) * splits * 512u;
+    return b;
+}
+
+// ---------------------------------------------------------------------------
+
+template <int FMT, int XT, int GROUP, int NW, int TPW>
+struct VerifyKernel {
+    using T = Traits<FMT, GROUP>;
+    using G = Geometry<FMT, GROUP, NW, TPW>;
+    static constexpr int STAGES = G::STAGES;
+    static constexpr int NSET = T::GPC >= 2 ? T::GPC : 2;   // accumulator chains per tile
+
+    // Load cursor of a warp: the record of its next (unit, stage), tracked
+    // incrementally by every lane; lane 0 issues.  A stage holds up to CPS
+    // consecutive chunks of each of the unit's tiles.
+    struct Cursor {
+        const uint8_t* rec;     // record (tile0, first chunk of the stage)
+        int nvalid;             // tiles of the unit inside the cluster range
+        int nc;                 // chunks in this stage
+        int unit, stage;
+    };
+
+    static __device__ __forceinline__ void cursor_set(const VerifyParams& p, int t0, int t1,
+                                                      int c0, int nch, Cursor& c)
+    {
+        const int tile0 = t0 + c.unit * TPW;
+        const int ch = c.stage * G::CPS;
+        c.rec = p.W + ((size_t)tile0 * p.nchunks + c0 + ch) * G::REC;
+        c.nvalid = min(TPW, t1 - tile0);
+        c.nc = min(G::CPS, nch - ch);
+    }
+
+    static __device__ __forceinline__ void cursor_next(const VerifyParams& p, int t0, int t1,
+                                                       int c0, int nch, int nstage, Cursor& c)
+    {
+        if (++c.stage == nstage) {
+            c.stage = 0;
+            c.unit += NW;
+        }
+        cursor_set(p, t0, t1, c0, nch, c);
+    }
+
+    static __device__ __forceinline__ void issue(const VerifyParams& p, const Cursor& c,
+                                                 uint32_t leader, uint32_t ring_w,
+                                                 uint32_t bars_w, int slot)
+    {
+        const uint32_t bar = bars_w + slot * 8;
+        const uint32_t dst = ring_w + slot * G::SLOT_B;
+        const uint32_t bytes = (uint32_t)c.nc * G::REC;
+        mbar_expect_tx_if(leader, bar, (uint32_t)c.nvalid * bytes);
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl)
+            bulk_g2s_if(leader && tl < c.nvalid, dst + tl * G::CPS * G::REC,
+                        c.rec + (size_t)tl * p.nchunks * G::REC, bytes, bar);
+    }
+
+    static constexpr int NB = num_bases<FMT>();
+
+    template <int HALF, int KTL>
+    static __device__ __forceinline__ void ktile(const uint4 (&w)[TPW], uint32_t b0, uint32_t b1,
+                                                 const uint32_t (&bases)[NB],
+                                                 float (&acc)[TPW][NSET][4])
+    {
+        constexpr int kt = HALF * (T::KT / 2) + KTL;
+        constexpr int set = T::GPC >= 2 ? kt / T::KTG : HALF;
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl) {
+            const uint32_t wa = HALF ? w[tl].z : w[tl].x;
+            const uint32_t wb = HALF ? w[tl].w : w[tl].y;
+            const uint32_t a0 = decode<FMT, XT, 2 * KTL>(wa, bases);
+            const uint32_t a1 = decode<FMT, XT, 2 * KTL>(wb, bases);
+            const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa, bases);
+            const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb, bases);
+            mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
+        }
+    }
+
+    // k-tile pair P of both halves, alternating between the two halves'
+    // accumulator chains.
+    template <int... P>
+    static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
+                                                 const uint4 (&w)[TPW], const uint4* xrow,
+                                                 int lane, const uint32_t (&bases)[NB],
+                                                 float (&acc)[TPW][NSET][4])
+    {
+        (
+            [&] {
+                const uint4 q0 = xrow[(2 * P) / 2 * 32 + lane];
+                const uint4 q1 = xrow[(T::KT / 2 + 2 * P) / 2 * 32 + lane];
+                ktile<0, 2 * P>(w, q0.x, q0.y, bases, acc);
+                ktile<1, 2 * P>(w, q1.x, q1.y, bases, acc);
+                ktile<0, 2 * P + 1>(w, q0.z, q0.w, bases, acc);
+                ktile<1, 2 * P + 1>(w, q1.z, q1.w, bases, acc);
+            }(),
+            ...);
+    }
+
+    template <int... GI>
+    static __device__ __forceinline__ void epilogue(std::integer_sequence<int, GI...>,
+                                                    const uint32_t (&sd)[TPW][T::SIDE_W],
+                                                    const float* corr_c, const float* rsum_c,
+                                                    float (&acc)[TPW][NSET][4],
+                                                    float (&y)[TPW][4], int t)
+    {
+        (
+            [&] {
+                constexpr int gi = GI;
+#pragma unroll
+                for (int tl = 0; tl < TPW; ++tl) {
+                    float a[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        a[j] = T::GPC >= 2 ? acc[tl][gi][j] : acc[tl][0][j] + acc[tl][1][j];
+                    if constexpr (T::AFFINE) {
+                        const float2 sc = f16pair(sd[tl][2 * gi]);
+                        const float2 bi = f16pair(sd[tl][2 * gi + 1]);
+                        const float2 R = *reinterpret_cast<const float2*>(rsum_c + gi * 8 + 2 * t);
+                        y[tl][0] = fmaf(sc.x, a[0], fmaf(bi.x, R.x, y[tl][0]));
+                        y[tl][1] = fmaf(sc.x, a[1], fmaf(bi.x, R.y, y[tl][1]));
+                        y[tl][2] = fmaf(sc.y, a[2], fmaf(bi.y, R.x, y[tl][2]));
+                        y[tl][3] = fmaf(sc.y, a[3], fmaf(bi.y, R.y, y[tl][3]));
+                    } else {
+                        const float2 sc = f16pair(sd[tl][gi]);
+                        y[tl][0] = fmaf(sc.x, a[0], y[tl][0]);
+                        y[tl][1] = fmaf(sc.x, a[1], y[tl][1]);
+                        y[tl][2] = fmaf(sc.y, a[2], y[tl][2]);
+                        y[tl][3] = fmaf(sc.y, a[3], y[tl][3]);
+                    }
+                }
+            }(),
+            ...);
+    }
+
+    // One chunk (cl = chunk index within the slice) of a warp's unit.
+    static __device__ __forceinline__ void process_chunk(const uint4 (&w)[TPW],
+                                                         const uint32_t (&sd)[TPW][T::SIDE_W],
+                                                         int cl, const uint4* __restrict__ xf,
+                                                         const float* __restrict__ corr,
+                                                         const float* __restrict__ rsum,
+                                                         const uint32_t (&bases)[NB],
+                                                         float (&y)[TPW][4], int lane)
+    {
+        const int t = lane & 3;
+        const float* corr_c = corr + cl * T::GPC * 8;
+        const float* rsum_c = rsum + cl * T::GPC * 8;
+        float acc[TPW][NSET][4];
+#pragma unroll
+        for (int j = 0; j < NSET; ++j) {
+            float2 I = make_float2(0.f, 0.f);
+            if (T::GPC >= 2 || j == 0)
+                I = *reinterpret_cast<const float2*>(corr_c + (T::GPC >= 2 ? j : 0) * 8 + 2 * t);
+#pragma unroll
+            for (int tl = 0; tl < TPW; ++tl) {
+                acc[tl][j][0] = I.x;
+                acc[tl][j][1] = I.y;
+                acc[tl][j][2] = I.x;
+                acc[tl][j][3] = I.y;
+            }
+        }
+        const uint4* xrow = xf + (size_t)cl * (T::KT / 2) * 32;
+        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xrow, lane, bases, acc);
+        epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
+    }
+
+    // A unit's results: straight to Y (no K split), or into the shared memory
+    // of the cluster CTA that owns the tile (K split).  Tile t0 + i belongs to
+    // rank i % S and lands in its slot [(i / S) * S + my_rank].
+    static __device__ __forceinline__ void store_unit(const VerifyParams& p, int t1, int tile0,
+                                                      const float (&y)[TPW][4], int g, int t,
+                                                      float* part, int tbase, int lane)
+    {
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl) {
+            const int tile = tile0 + tl;
+            if (tile >= t1)
+                continue;
+            if (p.splits > 1) {
+                cg::cluster_group cl = cg::this_cluster();
+                const int S = p.splits;
+                const int i = tile - tbase;
+                float* dst = cl.map_shared_rank(part, (unsigned)(i % S)) +
+                             ((i / S) * S + (int)cl.block_rank()) * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j * 32 + lane] = y[tl][j];
+                continue;
+            }
+            const int n0 = tile * 16 + g, n1 = n0 + 8;
+            const int m0 = 2 * t, m1 = 2 * t + 1;
+            if (m0 < p.M) {
+                if (n0 < p.N) p.Y[(size_t)m0 * p.ldy + n0] = y[tl][0];
+                if (n1 < p.N) p.Y[(size_t)m0 * p.ldy + n1] = y[tl][2];
+            }
+            if (m1 < p.M) {
+                if (n0 < p.N) p.Y[(size_t)m1 * p.ldy + n0] = y[tl][1];
+                if (n1 < p.N) p.Y[(size_t)m1 * p.ldy + n1] = y[tl][3];
+            }
+        }
+    }
+
+    // Stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order (rows >= M
+    // and K >= p.K are zero).
+    static __device__ __forceinline__ void stage_x(const VerifyParams& p, uint4* xf, int c0,
+                                                   int nch)
+    {
+        constexpr int B = 4;                       // loads in flight per thread
+        const int kb = c0 * T::CHUNK_K;
+        const int p8 = (nch * T::CHUNK_K) / 8;     // 8-element pieces per row
+        const int total = 8 * p8;
+        uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
+        const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
+        for (int i0 = threadIdx.x; i0 < total; i0 += B * NW * 32) {
+            uint4 v[B];
+            int dst[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = i0 + b * NW * 32;
+                v[b] = make_uint4(0u, 0u, 0u, 0u);
+                dst[b] = -1;
+                if (i < total) {
+                    const int m = i / p8;
+                    const int k8 = (i - m * p8) * 8;
+                    const int kg = kb + k8;
+                    if (m < p.M && kg < p.K) {     // K % 8 == 0: all 8 in range
+                        const uint16_t* src = X + (size_t)m * p.ldx + kg;
+                        if (p.x_vec) {
+                            v[b] = *reinterpret_cast<const uint4*>(src);
+                        } else {
+                            v[b].x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
+                            v[b].y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
+                            v[b].z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
+                            v[b].w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
+                        }
+                    }
+                    const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
+                    dst[b] = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                if (dst[b] >= 0) {
+                    xw[dst[b] + 0] = v[b].x;
+                    xw[dst[b] + 4] = v[b].y;
+                    xw[dst[b] + 8] = v[b].z;
+                    xw[dst[b] + 12] = v[b].w;
+                }
+        }
+    }
+
+    // Per-group corrections of the slice, one warp per chunk:
+    //   corr = -sum_k c_k x_k (Q4_0: -(c + 8) * rowsum), rsum = rowsum.
+    template <int... KP>
+    static __device__ __forceinline__ void corr_pairs(std::integer_sequence<int, KP...>,
+                                                      const uint4* xrow, int lane,
+                                                      float (&cs)[T::GPC], float (&rs)[T::GPC])
+    {
+        (
+            [&] {
+                constexpr int kt0 = 2 * KP;
+                const uint4 q = xrow[KP * 32 + lane];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kt = kt0 + e;                       // folds after unrolling
+                    const float2 f0 = pair_to_float2<XT>(e ? q.z : q.x);
+                    const float2 f1 = pair_to_float2<XT>(e ? q.w : q.y);
+                    const float s0 = f0.x + f0.y, s1 = f1.x + f1.y;
+                    const int ktl = kt % (T::KT / 2);
+                    const int gi = kt / T::KTG;
+                    cs[gi] += coef(2 * ktl) * s0 + coef(2 * ktl + 1) * s1;
+                    rs[gi] += s0 + s1;
+                }
+            }(),
+            ...);
+    }
+
+    static __device__ __forceinline__ float coef(int s)
+    {
+        // s is a constant after unrolling; the chain folds to one value.
+        float c = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i == s)
+                c = (float)dec_spec<FMT>(XT, i).c;
+        return c;
+    }
+
+    static __device__ __forceinline__ void corrections(uint4* xf, float* corr, float* rsum,
+                                                       int nch, int warp, int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        for (int cl = warp; cl < nch; cl += NW) {
+            float cs[T::GPC], rs[T::GPC];
+#pragma unroll
+            for (int i = 0; i < T::GPC; ++i)
+                cs[i] = rs[i] = 0.f;
+            corr_pairs(std::make_integer_sequence<int, T::KT / 2>{},
+                       xf + (size_t)cl * (T::KT / 2) * 32, lane, cs, rs);
+#pragma unroll
+            for (int i = 0; i < T::GPC; ++i) {
+                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 1);
+                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 2);
+                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+                if (t == 0) {
+                    const int gr = cl * T::GPC + i;
+                    if constexpr (FMT == LBV_FMT_Q4_0)
+                        corr[gr * 8 + g] = -(float)(dec_spec<FMT>(XT, 0).c + 8) * rs[i];
+                    else
+                        corr[gr * 8 + g] = -cs[i];
+                    if constexpr (T::AFFINE)
+                        rsum[gr * 8 + g] = rs[i];
+                }
+            }
+        }
+    }
+
+    static __device__ void run(const VerifyParams& p, unsigned char* smem)
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int g = lane >> 2, t = lane & 3;
+        const int S = p.splits;
+        const int c0 = blockIdx.x * p.cps;
+        const int nch = min(p.cps, p.nchunks - c0);          // >= 1 (host guarantees)
+        const int t0 = (int)(((unsigned)p.ntiles * blockIdx.y) / gridDim.y);
+        const int t1 = (int)(((unsigned)p.ntiles * (blockIdx.y + 1)) / gridDim.y);
+
+        unsigned char* ring = smem;
+        unsigned char* bars = ring + G::RING_B;
+        uint4* xf = reinterpret_cast<uint4*>(bars + G::BAR_B);
+        float* corr = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xf) +
+                                               (size_t)p.cps * T::KT * 256u);
+        float* rsum = corr + p.cps * T::GPC * 8;
+        float* part = corr + p.cps * T::GPC * 8 * G::CORR_ARRAYS;
+
+        const uint32_t ring_w = smem_u32(ring) + warp * STAGES * G::SLOT_B;
+        const uint32_t bars_w = smem_u32(bars) + warp * STAGES * 8;
+        const unsigned char* ring_wp = ring + (size_t)warp * STAGES * G::SLOT_B;
+
+        // this warp's units of TPW tiles within [t0, t1)
+        const int nunits = (t1 - t0 + TPW - 1) / TPW;
+        const int nu = warp < nunits ? (nunits - 1 - warp) / NW + 1 : 0;
+
+        if (S > 1)
+            cluster_arrive_relaxed();
+        if (lane == 0) {
+#pragma unroll 1
+            for (int s = 0; s < STAGES; ++s)
+                mbar_init(bars_w + s * 8, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+
+        // XOR bases in registers: opaque values cannot be folded back into
+        // immediates, so each decode stays one LOP3.
+        uint32_t bases[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+            asm volatile("mov.b32 %0, %1;\n" : "=r"(bases[i]) : "r"(base_of<FMT>(XT, i)));
+
+        // Packed weights are read-only: start streaming before waiting on the
+        // previous kernel in the stream.
+        const int nstage = (nch + G::CPS - 1) / G::CPS;
+        const int Q = nu * nstage;
+        const uint32_t leader = lane == 0;
+        Cursor lcur;
+        lcur.unit = warp;
+        lcur.stage = 0;
+        cursor_set(p, t0, t1, c0, nch, lcur);
+        int lq = 0;
+        const int npre = min(STAGES, Q);
+#pragma unroll 1
+        for (int st = 0; st < npre; ++st) {
+            issue(p, lcur, leader, ring_w, bars_w, st);
+            ++lq;
+            cursor_next(p, t0, t1, c0, nch, nstage, lcur);
+        }
+
+        griddep_wait();
+        stage_x(p, xf, c0, nch);
+        __syncthreads();
+        corrections(xf, corr, rsum, nch, warp, lane);
+        __syncthreads();
+        if (S > 1)
+            cluster_wait();            // all peers run: their partial buffers are live
+        griddep_launch_dependents();
+
+        float y[TPW][4];
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl)
+            y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
+        int cu = warp, cc = 0;                                // compute cursor
+        bool ok = true;
+        int q = 0, slot = 0;
+        uint32_t parity = 0;
+#pragma unroll 1
+        for (; q < Q; ++q) {
+            const uint32_t bar = bars_w + slot * 8;
+            if (!mbar_try(bar, parity) && !mbar_wait(bar, parity)) {
+                ok = false;
+                break;
+            }
+            const int nc = min(G::CPS, nch - cc);
+            uint4 w[G::CPS][TPW];
+            uint32_t sd[G::CPS][TPW][T::SIDE_W];
+            const unsigned char* src = ring_wp + slot * G::SLOT_B;
+#pragma unroll
+            for (int ci = 0; ci < G::CPS; ++ci)
+#pragma unroll
+                for (int tl = 0; tl < TPW; ++tl) {
+                    const unsigned char* r = src + (tl * G::CPS + ci) * G::REC;
+                    w[ci][tl] = reinterpret_cast<const uint4*>(r)[lane];
+                    const uint32_t* sp = reinterpret_cast<const uint32_t*>(r + 512 + g * G::SIDE_B);
+#pragma unroll
+                    for (int i = 0; i < T::SIDE_W; ++i)
+                        sd[ci][tl][i] = sp[i];
+                }
+            __syncwarp();
+            if (lq < Q) {
+                fence_proxy_async_if(leader);
+                issue(p, lcur, leader, ring_w, bars_w, slot);
+                ++lq;
+                cursor_next(p, t0, t1, c0, nch, nstage, lcur);
+            }
+            if (++slot == STAGES) {
+                slot = 0;
+                parity ^= 1u;
+            }
+            process_chunk(w[0], sd[0], cc, xf, corr, rsum, bases, y, lane);
+            if (nc > 1)
+                process_chunk(w[1], sd[1], cc + 1, xf, corr, rsum, bases, y, lane);
+            cc += nc;
+            if (cc == nch) {
+                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane);
+#pragma unroll
+                for (int tl = 0; tl < TPW; ++tl)
+                    y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
+                cc = 0;
+                cu += NW;
+            }
+        }
+        if (!ok) {
+            if (lane == 0)
+                atomicOr(p.err, 1u);
+            // let the copies already issued into this warp's ring land
+            for (int r = q; r < lq; ++r)
+                mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
+        }
+
+        if (S > 1)
+            cluster_reduce(p, part, t0, t1);
+    }
+
+    // After the cluster barrier each CTA sums, in rank order 0..S-1, the
+    // partials its cluster peers stored for the tiles it owns, and writes Y.
+    static __device__ void cluster_reduce(const VerifyParams& p, float* part, int t0, int t1)
+    {
+        cg::cluster_group cl = cg::this_cluster();
+        cl.sync();
+        const int S = p.splits;
+        const int rank = (int)cl.block_rank();
+        const int nown = (t1 - t0 - rank + S - 1) / S;        // tiles t0 + rank + S*k
+        for (int e = (int)threadIdx.x; e < nown * 128; e += NW * 32) {
+            const int k = e >> 7, r = e & 127;
+            const float* src = part + (k * S) * 128 + r;
+            float acc = 0.f;
+            for (int q = 0; q < S; ++q)
+                acc += src[q * 128];
+            const int tile = t0 + rank + S * k;
+            const int j = r >> 5, ln = r & 31;
+            const int n = tile * 16 + (ln >> 2) + 8 * (j >> 1);
+            const int m = 2 * (ln & 3) + (j & 1);
+            if (n < p.N && m < p.M)
+                p.Y[(size_t)m * p.ldy + n] = acc;
+        }
+    }
+};
+
+template <int FMT, int XT, int GROUP, int NW, int TPW>
+__global__ void __launch_bounds__(NW * 32, 1) lbv_verify_kernel(const VerifyParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem);
+}
+
+// ---------------------------------------------------------------------------
+// Host side: launch / smem / cluster occupancy for one (FMT, XT, GROUP)
+
+template <int FMT, int XT, int GROUP>
+inline void* kernel_ptr(int warps, int tpw)
+{
+    if (warps == 8 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 2>;
+    if (warps == 8 && tpw == 4) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 4>;
+    if (warps == 16 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 1>;
+    if (warps == 16 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 2>;
+    return nullptr;
+}
+
+template <int FMT, int GROUP>
+inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits)
+{
+    if (warps == 8 && tpw == 2) return smem_bytes_for<FMT, GROUP, 8, 2>(cps, tiles_max, splits);
+    if (warps == 8 && tpw == 4) return smem_bytes_for<FMT, GROUP, 8, 4>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 1) return smem_bytes_for<FMT, GROUP, 16, 1>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 2) return smem_bytes_for<FMT, GROUP, 16, 2>(cps, tiles_max, splits);
+    return (size_t)1 << 40;
+}
+
+inline void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const Shape& sh,
+                        bool pdl, cudaStream_t st)
+{
+    cfg = {};
+    cfg.gridDim = dim3((unsigned)sh.splits, (unsigned)sh.ctas_n, 1u);
+    cfg.blockDim = dim3((unsigned)(sh.warps * 32), 1u, 1u);
+    cfg.dynamicSmemBytes = sh.smem;
+    cfg.stream = st;
+    unsigned na = 0;
+    if (sh.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)sh.splits;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+}
+
+template <int FMT, int XT, int GROUP>
+inline cudaError_t launch_t(const Shape& sh, const VerifyParams& p, const LaunchOpts& o,
+                            cudaStream_t st)
+{
+    void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    if (!k)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_config(cfg, attr, sh, o.pdl, st);
+    void* args[] = {const_cast<VerifyParams*>(&p)};
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+template <int FMT, int XT, int GROUP>
+inline cudaError_t prepare_t(const Shape& sh)
+{
+    void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    if (!k)
+        return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sh.smem > kMaxDynSmem ? (int)sh.smem : kMaxDynSmem);
+}
+
+// Clusters of the shape that can be resident at once (0 if none fits).
+template <int FMT, int XT, int GROUP>
+inline int max_clusters_t(const Shape& sh)
+{
+    void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    if (!k || prepare_t<FMT, XT, GROUP>(sh) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    Shape s1 = sh;
+    s1.ctas_n = 1;
+    fill_config(cfg, attr, s1, false, nullptr);
+    int n = 0;
+    if (sh.splits > 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess)
+            return 0;
+        return n;
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, sh.warps * 32, sh.smem) !=
+        cudaSuccess)
+        return 0;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return n * sms;
+}
+
+}  // namespace lbv

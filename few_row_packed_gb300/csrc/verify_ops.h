@@ -1,5 +1,5 @@
 // verify_ops.h -- per-(format, group) few-row kernel entry points; each
-// translation unit tc_<fmt>.cu instantiates one set.
+// translation unit verify_<fmt>.cu instantiates one set.
 #pragma once
 
 #include "lbv_internal.h"
@@ -11,7 +11,7 @@ struct VerifyOps {
                           const LaunchOpts& o, cudaStream_t st);
     cudaError_t (*prepare)(lbv_dtype xt, const Shape& sh);
     int (*max_clusters)(lbv_dtype xt, const Shape& sh);
-    size_t (*smem)(int cps, int owned_max, int nparts);   // nparts = splits * wsplit
+    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits);
 };
 
 extern const VerifyOps sign1_ops;
@@ -23,29 +23,29 @@ extern const VerifyOps q4_0_ops;
 }  // namespace lbv
 
 // Defines the VerifyOps of one (FMT, GROUP) in a translation unit that
-// includes tc_kernel.cuh.
-#define LBV_DEFINE_VERIFY_OPS(NAME, FMT, GROUP)                                            \
-    namespace lbv {                                                                        \
-    static cudaError_t NAME##_launch(lbv_dtype xt, const Shape& sh, const VerifyParams& p, \
-                                     const LaunchOpts& o, cudaStream_t st)                 \
-    {                                                                                      \
-        return xt == LBV_F16 ? tc_launch_t<FMT, LBV_F16, GROUP>(sh, p, o, st)              \
-                             : tc_launch_t<FMT, LBV_BF16, GROUP>(sh, p, o, st);            \
-    }                                                                                      \
-    static cudaError_t NAME##_prepare(lbv_dtype xt, const Shape& sh)                       \
-    {                                                                                      \
-        return xt == LBV_F16 ? tc_prepare_t<FMT, LBV_F16, GROUP>(sh)                       \
-                             : tc_prepare_t<FMT, LBV_BF16, GROUP>(sh);                     \
-    }                                                                                      \
-    static int NAME##_max_clusters(lbv_dtype xt, const Shape& sh)                          \
-    {                                                                                      \
-        return xt == LBV_F16 ? tc_max_clusters_t<FMT, LBV_F16, GROUP>(sh)                  \
-                             : tc_max_clusters_t<FMT, LBV_BF16, GROUP>(sh);                \
-    }                                                                                      \
-    static size_t NAME##_smem(int cps, int owned_max, int nparts)                          \
-    {                                                                                      \
-        return tc_smem_bytes<FMT, GROUP>(cps, owned_max, nparts);                          \
-    }                                                                                      \
-    const VerifyOps NAME##_ops = {NAME##_launch, NAME##_prepare, NAME##_max_clusters,      \
-                                  NAME##_smem};                                            \
+// includes verify_kernel.cuh.
+#define LBV_DEFINE_VERIFY_OPS(NAME, FMT, GROUP)                                             \
+    namespace lbv {                                                                         \
+    static cudaError_t NAME##_launch(lbv_dtype xt, const Shape& sh, const VerifyParams& p,  \
+                                     const LaunchOpts& o, cudaStream_t st)                  \
+    {                                                                                       \
+        return xt == LBV_F16 ? launch_t<FMT, LBV_F16, GROUP>(sh, p, o, st)                  \
+                             : launch_t<FMT, LBV_BF16, GROUP>(sh, p, o, st);                \
+    }                                                                                       \
+    static cudaError_t NAME##_prepare(lbv_dtype xt, const Shape& sh)                        \
+    {                                                                                       \
+        return xt == LBV_F16 ? prepare_t<FMT, LBV_F16, GROUP>(sh)                           \
+                             : prepare_t<FMT, LBV_BF16, GROUP>(sh);                         \
+    }                                                                                       \
+    static int NAME##_max_clusters(lbv_dtype xt, const Shape& sh)                           \
+    {                                                                                       \
+        return xt == LBV_F16 ? max_clusters_t<FMT, LBV_F16, GROUP>(sh)                      \
+                             : max_clusters_t<FMT, LBV_BF16, GROUP>(sh);                    \
+    }                                                                                       \
+    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits)       \
+    {                                                                                       \
+        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits);                \
+    }                                                                                       \
+    const VerifyOps NAME##_ops = {NAME##_launch, NAME##_prepare, NAME##_max_clusters,       \
+                                  NAME##_smem};                                             \
     }

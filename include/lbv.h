@@ -83,10 +83,17 @@ typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
                                       (X is read and Y written only after it has).
                                       Only valid if the kernel launched just
                                       before on the stream never writes Wp. */
+#define LBV_PLAN_TCGEN05     0x10u /* use the tcgen05 few-row kernel (A operand
+                                      in tensor memory, 128-column tiles) for
+                                      every M.  Such a plan reads its own device
+                                      layout: pack with lbv_plan_pack and size
+                                      buffers with lbv_plan_packed_bytes.  Not
+                                      combinable with LBV_PLAN_FORCE_GEMV. */
 
 /* Kernel ids reported by lbv_plan_query. */
-#define LBV_KERNEL_FEWROW 1
-#define LBV_KERNEL_GEMV   2
+#define LBV_KERNEL_FEWROW    1     /* mma.sync few-row kernel (default)       */
+#define LBV_KERNEL_GEMV      2     /* 1-row path, run once per row           */
+#define LBV_KERNEL_FEWROW_TC 3     /* tcgen05 few-row kernel (LBV_PLAN_TCGEN05) */
 
 typedef struct lbv_plan lbv_plan;   /* opaque, library-owned */
 
@@ -94,13 +101,14 @@ typedef struct lbv_plan lbv_plan;   /* opaque, library-owned */
 /* Packing (host): canonical file layout -> the library's device layout.     */
 
 /*
- * Size in bytes of the device layout of a K x N matrix, or 0 for an invalid
- * shape.  The layout is one record per (128-column tile, K chunk), tile-major;
- * the chunk is 128 K for sign1 and affine2 g128, 64 K for affine2 g32/g64 and
- * Q4_0.  For N % 128 == 0 and K a multiple of the chunk the size equals the
- * canonical one exactly (1.125, 2 + 32/g and 4.5 bits per weight); otherwise
- * the last tile and chunk are padded with zero codes and zero scales, which
- * contribute exactly 0.  `group` is ignored except for LBV_FMT_AFFINE2.
+ * Size in bytes of the default device layout (the one the mma.sync few-row
+ * kernel and the 1-row path read) of a K x N matrix, or 0 for an invalid
+ * shape.  One record per (16-column tile, K chunk), tile-major.  For
+ * N % 16 == 0 and K a multiple of the format's chunk (256 for sign1, 128 for
+ * affine2, 64 for Q4_0) it equals the canonical size exactly
+ * (1.125, 2 + 32/g and 4.5 bits per weight); otherwise the last column tile
+ * and K chunk are padded with zero codes and zero scales, which contribute
+ * exactly 0.  `group` is ignored except for LBV_FMT_AFFINE2.
  */
 LBV_API size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group);
 
@@ -143,21 +151,43 @@ LBV_API lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_
                            unsigned flags, lbv_plan** out);
 LBV_API lbv_status lbv_plan_destroy(lbv_plan* plan);
 
+/* Size in bytes of the device layout the plan's kernels read: equal to
+ * lbv_packed_bytes() of the plan's shape, except for LBV_PLAN_TCGEN05 plans,
+ * whose layout is one record per (128-column tile, K chunk) (128 K for sign1
+ * and affine2 g128, 64 K otherwise), padded with zero codes and scales.
+ * 0 for a NULL plan. */
+LBV_API size_t lbv_plan_packed_bytes(const lbv_plan* plan);
+
+/* Packs canonical host arrays into the plan's device layout (host buffer of
+ * lbv_plan_packed_bytes() bytes).  part0..part2 are the arrays of
+ * lbv_pack_sign_g128 (bits, scales, unused), lbv_pack_affine2 (codes, scales,
+ * biases) or lbv_pack_q4_0 (blocks, unused, unused), laid out as documented
+ * there.  LBV_ERR_WORKSPACE if out_bytes is too small. */
+LBV_API lbv_status lbv_plan_pack(const lbv_plan* plan, const void* part0, const void* part1,
+                                 const void* part2, void* out, size_t out_bytes);
+
 /* For a row count M (1..8): the kernel that lbv_verify_gemm will launch
- * (LBV_KERNEL_FEWROW or LBV_KERNEL_GEMV), its K split (cluster size) and the
+ * (LBV_KERNEL_FEWROW, LBV_KERNEL_GEMV or LBV_KERNEL_FEWROW_TC), its K split (cluster size) and the
  * workspace it needs (always 0 in this build).  Any output may be NULL. */
 LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, int* splits,
                           size_t* workspace_bytes);
 
-/* The plan's launch shape for the few-row kernel: the K split (cluster size)
- * and the number of clusters along N.  Any output may be NULL. */
-LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* splits, int* ctas_n);
+/* The plan's launch shape for the few-row kernel: warps per CTA, column tiles
+ * (16 columns each) per warp, K split and CTAs along N.  For tests and
+ * benchmarks; any output may be NULL. */
+LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_per_warp, int* splits,
+                          int* ctas_n);
 
-/* Overrides the few-row launch shape: splits in 1..8, ctas_n = clusters along
- * N >= 1, or 0 for as many as can be resident.  Returns LBV_ERR_UNSUPPORTED if
- * the shape does not fit the device.  For tuning sweeps; not thread-safe
- * against concurrent verify calls on the same plan. */
-LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int splits, int ctas_n);
+/* Overrides the few-row launch shape ((warps, tiles_per_warp) in {(8, 2),
+ * (8, 4), (16, 1), (16, 2)}, splits in 1..8, ctas_n = clusters along N >= 1, or 0 for as many
+ * as can be resident).  Returns
+ * LBV_ERR_UNSUPPORTED if the shape does not fit the device (shared memory).
+ * For tuning sweeps; not thread-safe against concurrent verify calls.
+ * LBV_PLAN_TCGEN05 plans report warps = tiles_per_warp = 0 and ignore both
+ * on input (their kernel has a fixed CTA: three decode warpgroups and one
+ * MMA warp each). */
+LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_warp, int splits,
+                              int ctas_n);
 
 /* With LBV_PLAN_MEASURE: the measured cold-L2 time (us) of the few-row kernel
  * and of the 1-row path run M times at row count M, and the crossover (the

@@ -64,9 +64,8 @@ def test_packed_bytes_identities(L):
     assert lbv.packed_bytes(lbv.FMT_Q4_0, 48, 16, 32) == 0
     assert lbv.packed_bytes(7, 128, 16, 128) == 0
     # padding: ragged N and K round up to a tile and a chunk
-    assert lbv.packed_bytes(lbv.FMT_SIGN1_G128, 384, 20) == 3 * 128 * (16 + 2)
-    assert lbv.packed_bytes(lbv.FMT_AFFINE2, 96, 17, 32) == 2 * 128 * (16 + 8)
-    assert lbv.packed_bytes(lbv.FMT_Q4_0, 96, 129, 32) == 2 * 2 * 128 * (32 + 4)
+    assert lbv.packed_bytes(lbv.FMT_SIGN1_G128, 384, 20) == 2 * 2 * (512 + 8 * 8)
+    assert lbv.packed_bytes(lbv.FMT_AFFINE2, 96, 17, 32) == 2 * 1 * (512 + 8 * 32)
 
 
 def test_bad_arguments_return_status(L):
@@ -94,38 +93,42 @@ def test_bad_arguments_return_status(L):
 
 # ----------------------------------------------------------------------------
 # The device layout, read back from its written specification (layout.h):
-# one record per (128-column tile, chunk) in tile-major order: codes
-# [CB/16][128 columns][16 bytes], then side [128 columns][SB bytes].  The CB
-# bytes of column c are words j; word j holds pairs p = PPW*j + s: the code of
-# k = 2p at bit s*W and of k = 2p + 1 at bit 16 + s*W.
+# one record per (tile, chunk) in tile-major order, 512 code bytes
+# [lane][word] then 8 x SB side bytes [g].  Word wi of lane (g, t) is column
+# 16*tile + g + 8*(wi & 1), k-tiles (wi >> 1)*KT/2 + s//2; slot s holds the
+# codes of k0 = 16*kt + 8*(s & 1) + 2*t at bit s*W and of k0+1 at 16 + s*W.
 
-SPEC = {  # fmt: group -> (chunk_k, code bytes CB, side bytes SB, bits W)
-    lbv.FMT_SIGN1_G128: {128: (128, 16, 2, 1)},
-    lbv.FMT_AFFINE2: {32: (64, 16, 8, 2), 64: (64, 16, 4, 2), 128: (128, 32, 4, 2)},
-    lbv.FMT_Q4_0: {32: (64, 32, 4, 4)},
+SPEC = {  # chunk_k, W (bits), slots
+    lbv.FMT_SIGN1_G128: (256, 1, 16),
+    lbv.FMT_AFFINE2: (128, 2, 8),
+    lbv.FMT_Q4_0: (64, 4, 4),
 }
 
 
+def side_bytes(fmt, group):
+    return (128 // group) * 8 if fmt == lbv.FMT_AFFINE2 else 8
+
+
 def read_layout(fmt, packed, K, N, group):
-    ck, cb, sb, W = SPEC[fmt][group]
-    ppw = 16 // W
-    ntiles, nch = -(-N // 128), -(-K // ck)
-    rec = 128 * (cb + sb)
+    ck, W, slots = SPEC[fmt]
+    KT = ck // 16
+    ntiles, nch = -(-N // 16), -(-K // ck)
+    rec = 512 + 8 * side_bytes(fmt, group)
     recs = packed.reshape(ntiles, nch, rec)
-    codes = np.ascontiguousarray(recs[:, :, :128 * cb]).reshape(ntiles, nch, cb // 16, 128, 16)
-    words = np.ascontiguousarray(codes.transpose(0, 1, 3, 2, 4)).reshape(
-        ntiles, nch, 128, cb).view(np.uint32)                    # [tile][chunk][col][word]
-    out = np.full((ntiles * 128, nch * ck), -1, np.int64)
+    codes = np.ascontiguousarray(recs[:, :, :512]).view(np.uint32).reshape(ntiles, nch, 32, 4)
+    out = np.full((ntiles * 16, nch * ck), -1, np.int64)
     mask = (1 << W) - 1
-    n = (np.arange(ntiles)[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)
-    for j in range(cb // 4):
-        for s_ in range(ppw):
-            p = ppw * j + s_
-            for h in range(2):
-                v = (words[:, :, :, j] >> np.uint32(s_ * W + 16 * h)) & mask   # [tile][chunk][col]
-                k = np.arange(nch) * ck + 2 * p + h
-                out[np.ix_(n, k)] = v.transpose(0, 2, 1).reshape(ntiles * 128, nch)
-    side = np.ascontiguousarray(recs[:, :, 128 * cb:]).view(np.uint16).reshape(ntiles, nch, 128, -1)
+    for lane in range(32):
+        g, t = lane >> 2, lane & 3
+        for wi in range(4):
+            n = np.arange(ntiles) * 16 + g + 8 * (wi & 1)
+            for s in range(slots):
+                kt = (wi >> 1) * (KT // 2) + (s >> 1)
+                for h in range(2):
+                    k = np.arange(nch) * ck + 16 * kt + 8 * (s & 1) + 2 * t + h
+                    v = (codes[:, :, lane, wi] >> np.uint32(s * W + 16 * h)) & mask
+                    out[np.ix_(n, k)] = v
+    side = np.ascontiguousarray(recs[:, :, 512:]).view(np.uint16).reshape(ntiles, nch, 8, -1)
     return out, side
 
 
@@ -141,8 +144,8 @@ def canonical_codes(fmt, parts, K, N):
 
 
 @pytest.mark.parametrize("fmt,K,N,group", [
-    (lbv.FMT_SIGN1_G128, 512, 48, 128), (lbv.FMT_SIGN1_G128, 384, 150, 128),
-    (lbv.FMT_AFFINE2, 256, 32, 64), (lbv.FMT_AFFINE2, 320, 17, 32), (lbv.FMT_AFFINE2, 384, 140, 128),
+    (lbv.FMT_SIGN1_G128, 512, 48, 128), (lbv.FMT_SIGN1_G128, 384, 21, 128),
+    (lbv.FMT_AFFINE2, 256, 32, 64), (lbv.FMT_AFFINE2, 320, 17, 32), (lbv.FMT_AFFINE2, 384, 40, 128),
     (lbv.FMT_Q4_0, 192, 32, 32), (lbv.FMT_Q4_0, 96, 9, 32)])
 def test_pack_is_lossless(L, fmt, K, N, group):
     name = {0: synth.SIGN1_G128, 1: synth.AFFINE2, 2: synth.Q4_0}[fmt]
@@ -154,23 +157,25 @@ def test_pack_is_lossless(L, fmt, K, N, group):
     ref = canonical_codes(fmt, parts, K, N)
     assert np.array_equal(codes[:N, :K], ref)
     assert np.all(codes[N:, :] == 0) and np.all(codes[:, K:] == 0)
-    ck = SPEC[fmt][group][0]
+    ck = SPEC[fmt][0]
+    # side entries: per group j of a chunk: scale(g), scale(g+8) [, bias(g), bias(g+8)]
     gk = group if fmt == lbv.FMT_AFFINE2 else (128 if fmt == lbv.FMT_SIGN1_G128 else 32)
-    per = 2 if fmt == lbv.FMT_AFFINE2 else 1          # fp16 values per group
-    ntiles, nch = side.shape[0], side.shape[1]
+    per = 4 if fmt == lbv.FMT_AFFINE2 else 2
+    ntiles = side.shape[0]
     for tile in range(ntiles):
-        for ch in range(nch):
-            for c in range(128):
-                n = tile * 128 + c
+        for ch in range(side.shape[1]):
+            for g in range(8):
                 for j in range(ck // gk):
                     grp = ch * (ck // gk) + j
-                    e = side[tile, ch, c, per * j]
-                    if n >= N or grp * gk >= K:
-                        assert e == 0
-                    elif fmt == lbv.FMT_Q4_0:
-                        blk = parts[0][n, grp]
-                        assert e == int(blk[0]) | (int(blk[1]) << 8)
-                    else:
-                        assert e == parts[1][n, grp]
-                        if fmt == lbv.FMT_AFFINE2:
-                            assert side[tile, ch, c, per * j + 1] == parts[2][n, grp]
+                    for hi in range(2):
+                        n = tile * 16 + g + 8 * hi
+                        e = side[tile, ch, g, per * j + hi]
+                        if n >= N or grp * gk >= K:
+                            assert e == 0
+                        elif fmt == lbv.FMT_Q4_0:
+                            blk = parts[0][n, grp]
+                            assert e == int(blk[0]) | (int(blk[1]) << 8)
+                        else:
+                            assert e == parts[1][n, grp]
+                            if fmt == lbv.FMT_AFFINE2:
+                                assert side[tile, ch, g, per * j + 2 + hi] == parts[2][n, grp]

@@ -48,10 +48,11 @@ class Case:
         self.fmt = FMT[fmtname]
         self.K, self.N, self.group, self.xdtype = K, N, group, xdtype
         self.parts, self.xb = synth.gen_matrix(self.mat, seed, rows=8)
-        self.packed = lbv.pack(self.fmt, self.parts, K, N, group)
+        self.plan = lbv.Plan(self.fmt, K, N, group, DT[xdtype], flags)
+        # the layout this plan's kernels read (lbv_plan_pack)
+        self.packed = lbv.pack(self.fmt, self.parts, K, N, group, plan=self.plan)
         self.Wp = dev(self.packed)
         self.X = x_dev(self.xb)
-        self.plan = lbv.Plan(self.fmt, K, N, group, DT[xdtype], flags)
         self.cols = np.arange(N) if cols is None else np.asarray(cols)
         self.Xf = oracle.x_to_f64(self.xb, xdtype)
         self.Yref, self.A = oracle.verify(self.fmt, self.parts, self.Xf, K, N, group,
@@ -97,41 +98,40 @@ def test_parity_small_all_M(fmtname, K, N, group, xdtype):
 
 
 def test_tiny_1bit_seed0_every_shape():
-    """The 512x256 1-bit case under every launch shape (K split, clusters
-    along N): all within tolerance, each shape deterministic."""
+    """The 512x256 1-bit case under every launch shape (warps, tiles per warp,
+    K split): all within tolerance, each shape deterministic."""
     c = Case(synth.SIGN1_G128, 512, 256, 128, "f16", seed=0)
     seen = 0
-    for splits in (1, 2, 4):
-        for ctas in (0, 1, 2):
-            c.plan.set_shape(splits, ctas)
-            assert c.plan.shape()[0] == splits
+    for warps, tpw in ((8, 2), (8, 4), (16, 1), (16, 2)):
+        for splits in (1, 2):
+            c.plan.set_shape(warps, tpw, splits)
+            assert c.plan.shape()[:3] == (warps, tpw, splits)
             for M in (1, 5, 8):
                 Y1, Y2 = c.run(M), c.run(M)
                 assert np.array_equal(Y1, Y2)
                 c.check(Y1, M)
             seen += 1
-    assert seen == 9
+    assert seen == 8
 
 
 @pytest.mark.parametrize("fmtname,K,N,group,xdtype", [
-    (synth.SIGN1_G128, 2048, 400, 128, "f16"),
-    (synth.AFFINE2, 1536, 300, 64, "bf16"),
-    (synth.AFFINE2, 1280, 260, 128, "f16"),
-    (synth.AFFINE2, 640, 200, 32, "bf16"),
-    (synth.Q4_0, 1280, 270, 32, "f16")])
+    (synth.SIGN1_G128, 2048, 160, 128, "f16"),
+    (synth.AFFINE2, 1536, 96, 64, "bf16"),
+    (synth.Q4_0, 1280, 80, 32, "f16")])
 def test_split_k_shapes(fmtname, K, N, group, xdtype):
     c = Case(fmtname, K, N, group, xdtype, seed=3)
     tried = 0
     for splits in (1, 2, 3, 4, 5, 8):
-        for ctas in (0, 1, 2):
-            try:
-                c.plan.set_shape(splits, ctas)
-            except lbv.LbvError:
-                continue
-            tried += 1
-            for M in (2, 8):
-                c.check(c.run(M), M)
-    assert tried >= 9
+        for ctas in (0, 1, 3):
+            for warps, tpw in ((16, 1), (8, 4), (16, 2)):
+                try:
+                    c.plan.set_shape(warps, tpw, splits, ctas)
+                except lbv.LbvError:
+                    continue
+                tried += 1
+                for M in (2, 8):
+                    c.check(c.run(M), M)
+    assert tried >= 20
 
 
 def test_row_and_M_independence_bitwise():
@@ -263,6 +263,6 @@ def test_error_codes_on_device():
     with pytest.raises(lbv.LbvError):
         lbv.verify_gemm(c.plan, c.X, 2, c.Wp.view(torch.uint8)[2:], Y)   # misaligned Wp
     with pytest.raises(lbv.LbvError) as e:
-        c.plan.set_shape(9, 0)
+        c.plan.set_shape(3, 1, 1)
     assert e.value.status == lbv.ERR_INVALID_ARG
     assert c.plan.query(3)[2] == 0                # no workspace

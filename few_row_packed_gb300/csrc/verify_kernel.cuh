@@ -568,10 +568,14 @@ struct VerifyKernel {
 
     // Stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order (rows >= M
     // and K >= p.K are zero).
+    // `after_first_loads` runs once, after the first round of loads is issued
+    // and before any of it is stored: the weight prefetch goes there, so X is
+    // not queued behind it.
+    template <class F>
     static __device__ __forceinline__ void stage_x(const VerifyParams& p, uint4* xf, int c0,
-                                                   int nch)
+                                                   int nch, F&& after_first_loads)
     {
-        constexpr int B = 4;                       // loads in flight per thread
+        constexpr int B = 8;                       // loads in flight per thread
         const int kb = c0 * T::CHUNK_K;
         const int p8 = (nch * T::CHUNK_K) / 8;     // 8-element pieces per row
         const int total = 8 * p8;
@@ -604,6 +608,8 @@ struct VerifyKernel {
                     dst[b] = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
                 }
             }
+            if (i0 == (int)threadIdx.x)
+                after_first_loads();
 #pragma unroll
             for (int b = 0; b < B; ++b)
                 if (dst[b] >= 0) {
@@ -736,15 +742,25 @@ struct VerifyKernel {
         cursor_set(p, t0, t1, c0, nch, lcur);
         int lq = 0;
         const int npre = min(STAGES, Q);
+        // two stages before the wait on the previous kernel (they overlap its
+        // tail); the rest after this CTA's activation loads are in flight
+        const int nearly = min(2, npre);
 #pragma unroll 1
-        for (int st = 0; st < npre; ++st) {
-            issue(p, lcur, leader, ring_w, bars_w, st);
-            ++lq;
+        for (; lq < nearly; ++lq) {
+            issue(p, lcur, leader, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
 
         griddep_wait();
-        stage_x(p, xf, c0, nch);
+        auto prefetch_rest = [&]() {
+#pragma unroll 1
+            for (; lq < npre; ++lq) {
+                issue(p, lcur, leader, ring_w, bars_w, lq);
+                cursor_next(p, t0, t1, c0, nch, nstage, lcur);
+            }
+        };
+        stage_x(p, xf, c0, nch, prefetch_rest);
+        prefetch_rest();           // threads with no activation piece to load
         __syncthreads();
         corrections(xf, corr, rsum, nch, warp, lane);
         __syncthreads();

@@ -6,9 +6,11 @@
 //     balanced range of 16-column tiles; the S CTAs of a cluster split K into
 //     slices, and their partial sums are reduced through distributed shared
 //     memory in rank order (deterministic, no workspace).
-//   * Each CTA stages its K slice of X once, in mma fragment order, with the
-//     per-group corrections (below).  X is read only after griddepcontrol.wait;
-//     the packed weights, which no kernel writes, start streaming before it.
+//   * Each CTA stages its K slice of X once, row-major, with one 1-D bulk copy
+//     per row (padded rows, so ldmatrix reads the B fragments without bank
+//     conflicts), then computes the per-group corrections (below).  X is read
+//     only after griddepcontrol.wait; the packed weights, which no kernel
+//     writes, start streaming before it.
 //   * Each warp streams its tiles' packed codes and scales through a private
 //     ring of shared-memory stages filled by 1-D bulk async copies (TMA engine)
 //     and tracked by mbarriers, so a few tens of KB per SM stay in flight with
@@ -213,6 +215,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Four 8x8 b16 matrices from shared memory (row addresses from lanes 8i..8i+7
+// for matrix i): thread (g, t) receives row g, elements 2t and 2t + 1 of each.
+__device__ __forceinline__ uint4 ldsm_x4(uint32_t addr)
+{
+    uint4 r;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
@@ -349,20 +362,28 @@ struct Geometry {
     static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
-    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8;
+    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16;   // + the X barrier
     // corrections and row sums per group of the slice
     static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
 };
 
+// Bytes between X rows in shared memory: the slice plus 16 bytes, so the 8
+// row addresses of an ldmatrix hit distinct bank groups.
+template <int FMT, int GROUP>
+__host__ __device__ constexpr int x_row_stride(int cps)
+{
+    return cps * Traits<FMT, GROUP>::CHUNK_K * 2 + 16;
+}
+
 // Shared memory carve-up (bytes):
-//   ring | mbarriers | xf (X fragments) | corr | rsum (affine) | part (K split)
+//   ring | mbarriers (+ X barrier) | xs (X rows) | corr | rsum (affine) | part (K split)
 template <int FMT, int GROUP, int NW, int TPW>
 __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
 {
     using G = Geometry<FMT, GROUP, NW, TPW>;
     using T = Traits<FMT, GROUP>;
     size_t b = G::RING_B + G::BAR_B;
-    b += (size_t)cps * T::KT * 256u;
+    b += 8 * x_row_stride<FMT, GROUP>(cps);
     b += (size_t)cps * T::GPC * 8 * 4 * G::CORR_ARRAYS;
     if (splits > 1)
         b += (size_t)((tiles_max + splits - 1) / splits) * splits * 512u;
@@ -447,14 +468,14 @@ struct VerifyKernel {
     // accumulator chains.
     template <int... P>
     static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
-                                                 const uint4 (&w)[TPW], const uint4* xrow,
-                                                 int lane, const uint32_t (&bases)[NB],
+                                                 const uint4 (&w)[TPW], uint32_t xa,
+                                                 const uint32_t (&bases)[NB],
                                                  float (&acc)[TPW][NSET][4])
     {
         (
             [&] {
-                const uint4 q0 = xrow[(2 * P) / 2 * 32 + lane];
-                const uint4 q1 = xrow[(T::KT / 2 + 2 * P) / 2 * 32 + lane];
+                const uint4 q0 = ldsm_x4(xa + P * 64);                    // k-tiles 2P, 2P + 1
+                const uint4 q1 = ldsm_x4(xa + (T::KT / 4 + P) * 64);      // the second half's
                 ktile<0, 2 * P>(w, q0.x, q0.y, bases, acc);
                 ktile<1, 2 * P>(w, q1.x, q1.y, bases, acc);
                 ktile<0, 2 * P + 1>(w, q0.z, q0.w, bases, acc);
@@ -502,7 +523,7 @@ struct VerifyKernel {
     // One chunk (cl = chunk index within the slice) of a warp's unit.
     static __device__ __forceinline__ void process_chunk(const uint4 (&w)[TPW],
                                                          const uint32_t (&sd)[TPW][T::SIDE_W],
-                                                         int cl, const uint4* __restrict__ xf,
+                                                         int cl, uint32_t xa,
                                                          const float* __restrict__ corr,
                                                          const float* __restrict__ rsum,
                                                          const uint32_t (&bases)[NB],
@@ -525,8 +546,7 @@ struct VerifyKernel {
                 acc[tl][j][3] = I.y;
             }
         }
-        const uint4* xrow = xf + (size_t)cl * (T::KT / 2) * 32;
-        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xrow, lane, bases, acc);
+        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xa + cl * T::CHUNK_K * 2, bases, acc);
         epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
     }
 
@@ -568,70 +588,58 @@ struct VerifyKernel {
 
     // Stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order (rows >= M
     // and K >= p.K are zero).
-    // `after_first_loads` runs once, after the first round of loads is issued
-    // and before any of it is stored: the weight prefetch goes there, so X is
-    // not queued behind it.
-    template <class F>
-    static __device__ __forceinline__ void stage_x(const VerifyParams& p, uint4* xf, int c0,
-                                                   int nch, F&& after_first_loads)
+    // X slice [kb, kb + nch * CHUNK_K) of rows m < M, row-major at xs + m * RS.
+    // Aligned X: thread 0 issues one bulk copy per row (completing on xbar);
+    // the others zero what lies past K in the last chunk.  Otherwise all
+    // threads copy it with plain loads.  Rows >= M are left as they are: they
+    // only reach output columns >= M, which are never stored.
+    static __device__ __forceinline__ bool stage_x(const VerifyParams& p, unsigned char* xs, int RS,
+                                                   uint32_t xbar, int c0, int nch)
     {
-        constexpr int B = 8;                       // loads in flight per thread
         const int kb = c0 * T::CHUNK_K;
-        const int p8 = (nch * T::CHUNK_K) / 8;     // 8-element pieces per row
-        const int total = 8 * p8;
-        uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
+        const int span = nch * T::CHUNK_K;                   // elements per row slice
+        const int have = min(span, p.K - kb);                // elements inside K (K % 16 == 0)
         const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
-        for (int i0 = threadIdx.x; i0 < total; i0 += B * NW * 32) {
-            uint4 v[B];
-            int dst[B];
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                const int i = i0 + b * NW * 32;
-                v[b] = make_uint4(0u, 0u, 0u, 0u);
-                dst[b] = -1;
-                if (i < total) {
-                    const int m = i / p8;
-                    const int k8 = (i - m * p8) * 8;
-                    const int kg = kb + k8;
-                    if (m < p.M && kg < p.K) {     // K % 8 == 0: all 8 in range
-                        const uint16_t* src = X + (size_t)m * p.ldx + kg;
-                        if (p.x_vec) {
-                            v[b] = *reinterpret_cast<const uint4*>(src);
-                        } else {
-                            v[b].x = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
-                            v[b].y = (uint32_t)src[2] | ((uint32_t)src[3] << 16);
-                            v[b].z = (uint32_t)src[4] | ((uint32_t)src[5] << 16);
-                            v[b].w = (uint32_t)src[6] | ((uint32_t)src[7] << 16);
-                        }
-                    }
-                    const int kt = k8 >> 4, hi = (k8 >> 3) & 1;
-                    dst[b] = (((kt >> 1) * 32 + 4 * m) * 4) + (kt & 1) * 2 + hi;
-                }
+        if (p.x_vec) {
+            if (threadIdx.x == 0) {
+                mbar_expect_tx(xbar, (uint32_t)(p.M * have * 2));
+                for (int m = 0; m < p.M; ++m)
+                    bulk_g2s_if(1u, smem_u32(xs + (size_t)m * RS), X + (size_t)m * p.ldx + kb,
+                                (uint32_t)(have * 2), xbar);
             }
-            if (i0 == (int)threadIdx.x)
-                after_first_loads();
-#pragma unroll
-            for (int b = 0; b < B; ++b)
-                if (dst[b] >= 0) {
-                    xw[dst[b] + 0] = v[b].x;
-                    xw[dst[b] + 4] = v[b].y;
-                    xw[dst[b] + 8] = v[b].z;
-                    xw[dst[b] + 12] = v[b].w;
-                }
+            const int tail = (span - have) / 8;              // 16-byte pieces past K, per row
+            for (int i = threadIdx.x; i < p.M * tail; i += NW * 32) {
+                const int m = i / tail, k8 = have + (i - m * tail) * 8;
+                *reinterpret_cast<uint4*>(xs + (size_t)m * RS + k8 * 2) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            return true;
         }
+        for (int i = threadIdx.x; i < p.M * span; i += NW * 32) {
+            const int m = i / span, k = i - m * span;
+            reinterpret_cast<uint16_t*>(xs + (size_t)m * RS)[k] =
+                k < have ? X[(size_t)m * p.ldx + kb + k] : (uint16_t)0;
+        }
+        return false;
+    }
+
+    // This lane's ldmatrix row address offset within the X rows: lanes 8i..8i+7
+    // give the rows of matrix i, which covers K elements 8i..8i+7 of a k-tile pair.
+    static __device__ __forceinline__ uint32_t ldsm_lane_offset(int RS, int lane)
+    {
+        return (uint32_t)((lane & 7) * RS + (lane >> 3) * 16);
     }
 
     // Per-group corrections of the slice, one warp per chunk:
     //   corr = -sum_k c_k x_k (Q4_0: -(c + 8) * rowsum), rsum = rowsum.
     template <int... KP>
     static __device__ __forceinline__ void corr_pairs(std::integer_sequence<int, KP...>,
-                                                      const uint4* xrow, int lane,
-                                                      float (&cs)[T::GPC], float (&rs)[T::GPC])
+                                                      uint32_t xa, float (&cs)[T::GPC],
+                                                      float (&rs)[T::GPC])
     {
         (
             [&] {
                 constexpr int kt0 = 2 * KP;
-                const uint4 q = xrow[KP * 32 + lane];
+                const uint4 q = ldsm_x4(xa + KP * 64);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int kt = kt0 + e;                       // folds after unrolling
@@ -658,7 +666,7 @@ struct VerifyKernel {
         return c;
     }
 
-    static __device__ __forceinline__ void corrections(uint4* xf, float* corr, float* rsum,
+    static __device__ __forceinline__ void corrections(uint32_t xs_a, int RS, float* corr, float* rsum,
                                                        int nch, int warp, int lane)
     {
         const int g = lane >> 2, t = lane & 3;
@@ -668,7 +676,7 @@ struct VerifyKernel {
             for (int i = 0; i < T::GPC; ++i)
                 cs[i] = rs[i] = 0.f;
             corr_pairs(std::make_integer_sequence<int, T::KT / 2>{},
-                       xf + (size_t)cl * (T::KT / 2) * 32, lane, cs, rs);
+                       xs_a + ldsm_lane_offset(RS, lane) + cl * T::CHUNK_K * 2, cs, rs);
 #pragma unroll
             for (int i = 0; i < T::GPC; ++i) {
                 cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 1);
@@ -700,9 +708,10 @@ struct VerifyKernel {
 
         unsigned char* ring = smem;
         unsigned char* bars = ring + G::RING_B;
-        uint4* xf = reinterpret_cast<uint4*>(bars + G::BAR_B);
-        float* corr = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xf) +
-                                               (size_t)p.cps * T::KT * 256u);
+        unsigned char* xs = bars + G::BAR_B;
+        const int RS = x_row_stride<FMT, GROUP>(p.cps);
+        const uint32_t xbar = smem_u32(bars) + (uint32_t)(NW * STAGES * 8);
+        float* corr = reinterpret_cast<float*>(xs + (size_t)8 * RS);
         float* rsum = corr + p.cps * T::GPC * 8;
         float* part = corr + p.cps * T::GPC * 8 * G::CORR_ARRAYS;
 
@@ -720,6 +729,8 @@ struct VerifyKernel {
 #pragma unroll 1
             for (int s = 0; s < STAGES; ++s)
                 mbar_init(bars_w + s * 8, 1);
+            if (warp == 0)
+                mbar_init(xbar, 1);
             mbar_init_fence();
         }
         __syncwarp();
@@ -752,17 +763,18 @@ struct VerifyKernel {
         }
 
         griddep_wait();
-        auto prefetch_rest = [&]() {
+        const bool x_async = stage_x(p, xs, RS, xbar, c0, nch);
 #pragma unroll 1
-            for (; lq < npre; ++lq) {
-                issue(p, lcur, leader, ring_w, bars_w, lq);
-                cursor_next(p, t0, t1, c0, nch, nstage, lcur);
-            }
-        };
-        stage_x(p, xf, c0, nch, prefetch_rest);
-        prefetch_rest();           // threads with no activation piece to load
-        __syncthreads();
-        corrections(xf, corr, rsum, nch, warp, lane);
+        for (; lq < npre; ++lq) {
+            issue(p, lcur, leader, ring_w, bars_w, lq);
+            cursor_next(p, t0, t1, c0, nch, nstage, lcur);
+        }
+        __syncthreads();               // X barrier initialised, tails zeroed (or X copied)
+        bool x_ok = true;
+        if (x_async && !mbar_try(xbar, 0) && !mbar_wait(xbar, 0))
+            x_ok = false;
+        const uint32_t xs_a = smem_u32(xs);
+        corrections(xs_a, RS, corr, rsum, nch, warp, lane);
         __syncthreads();
         if (S > 1)
             cluster_wait();            // all peers run: their partial buffers are live
@@ -773,7 +785,8 @@ struct VerifyKernel {
         for (int tl = 0; tl < TPW; ++tl)
             y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
         int cu = warp, cc = 0;                                // compute cursor
-        bool ok = true;
+        const uint32_t xa_lane = xs_a + ldsm_lane_offset(RS, lane);
+        bool ok = x_ok;
         int q = 0, slot = 0;
         uint32_t parity = 0;
 #pragma unroll 1
@@ -809,9 +822,9 @@ struct VerifyKernel {
                 slot = 0;
                 parity ^= 1u;
             }
-            process_chunk(w[0], sd[0], cc, xf, corr, rsum, bases, y, lane);
+            process_chunk(w[0], sd[0], cc, xa_lane, corr, rsum, bases, y, lane);
             if (nc > 1)
-                process_chunk(w[1], sd[1], cc + 1, xf, corr, rsum, bases, y, lane);
+                process_chunk(w[1], sd[1], cc + 1, xa_lane, corr, rsum, bases, y, lane);
             cc += nc;
             if (cc == nch) {
                 store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane);
@@ -825,9 +838,11 @@ struct VerifyKernel {
         if (!ok) {
             if (lane == 0)
                 atomicOr(p.err, 1u);
-            // let the copies already issued into this warp's ring land
+            // let the copies already issued into this warp's ring (and X) land
             for (int r = q; r < lq; ++r)
                 mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
+            if (x_async && !x_ok)
+                mbar_wait(xbar, 0);
         }
 
         if (S > 1)

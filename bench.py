@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override of the launch shape")
     ap.add_argument("--kernel", default="mma", choices=["mma", "tc"],
                     help="few-row kernel: mma.sync (default plans) or tcgen05 (PLAN_TCGEN05)")
+    ap.add_argument("--head", default="fused", choices=["fused", "two-call", "greedy"],
+                    help="rotated head: rotation fused into the verify launch (default), "
+                         "lbv_fwht128 then lbv_verify_gemm, or fused rotation and per-row "
+                         "argmax without writing the logits")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
     ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
@@ -68,10 +72,13 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def call_bytes(mat, M):
+def call_bytes(mat, M, head="fused"):
+    """Algorithmic bytes of one call: packed weights, X, and Y (or, for the
+    greedy head, the argmax column and logit of each row)."""
     import few_row_packed_gb300 as lbv
     fmt = FMT_IDS[mat.fmt]
-    return lbv.packed_bytes(fmt, mat.K, mat.N, mat.group) + M * mat.K * 2 + M * mat.N * 4
+    out = M * 8 if (mat.rotate and head == "greedy") else M * mat.N * 4
+    return lbv.packed_bytes(fmt, mat.K, mat.N, mat.group) + M * mat.K * 2 + out
 
 
 # ---------------------------------------------------------------------------
@@ -139,10 +146,11 @@ class Stack:
     """Distinct packed matrices of a workload resident on the device."""
 
     def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int,
-                 use_graphs: bool = True, kernel: str = "mma"):
+                 use_graphs: bool = True, kernel: str = "mma", head: str = "fused"):
         import torch
         self.use_graphs = use_graphs
         self.graphs = {}
+        self.head = head
 
         import few_row_packed_gb300 as lbv
         wl = synth.WORKLOADS[workload]
@@ -179,9 +187,15 @@ class Stack:
             Y = torch.zeros((8, mat.N), dtype=torch.float32, device="cuda")
             self.layers.append((mat, plans[key], Wp, X, Xr, Y))
         self.plans = plans
-        self.bytes_per_step = {m: sum(call_bytes(l[0], m) for l in self.layers) for m in range(1, 9)}
+        self.bytes_per_step = {m: sum(call_bytes(l[0], m, head) for l in self.layers)
+                               for m in range(1, 9)}
         self.calls = len(self.layers)
-        self.launches_per_step = sum(2 if l[0].rotate else 1 for l in self.layers)
+        self.launches_per_step = sum(2 if (l[0].rotate and head == "two-call") else 1
+                                     for l in self.layers)
+        # greedy head: argmax outputs and the (zeroed) workspace the calls share
+        self.idx = torch.zeros(8, dtype=torch.int32, device="cuda")
+        self.val = torch.zeros(8, dtype=torch.float32, device="cuda")
+        self.ws = torch.zeros(lbv.fused_workspace_bytes(), dtype=torch.uint8, device="cuda")
 
     def graph(self, M, verify_only=False):
         """A CUDA graph of one step (launches captured through the C ABI)."""
@@ -209,11 +223,16 @@ class Stack:
     def step(self, M, verify_only=False):
         import few_row_packed_gb300 as lbv
         for mat, plan, Wp, X, Xr, Y in self.layers:
-            if mat.rotate and not verify_only:
+            if not mat.rotate or verify_only:
+                lbv.verify_gemm(plan, X, M, Wp, Y)
+            elif self.head == "two-call":
                 lbv.fwht128(X, Xr, M, mat.K, lbv.DTYPE_BY_NAME[mat.xdtype])
                 lbv.verify_gemm(plan, Xr, M, Wp, Y)
+            elif self.head == "fused":
+                lbv.verify_fused(plan, X, M, Wp, lbv.FUSED_ROTATE, Y=Y)
             else:
-                lbv.verify_gemm(plan, X, M, Wp, Y)
+                lbv.verify_fused(plan, X, M, Wp, lbv.FUSED_ROTATE | lbv.FUSED_ARGMAX,
+                                 idx=self.idx, val=self.val, workspace=self.ws)
 
 
 def timed(torch, fn, steps, warmup, barrier):
@@ -256,7 +275,7 @@ def recorded_traffic(workload, M, kernel):
     return None
 
 
-def cpu_baseline(workload, M, budget_s=10.0):
+def cpu_baseline(workload, M, budget_s=10.0, head="fused"):
     """The fp64 oracle as it stands, single-threaded on the host: verify calls
     on full matrices of the workload until about budget_s has passed."""
     import oracle
@@ -277,14 +296,14 @@ def cpu_baseline(workload, M, budget_s=10.0):
         oracle.verify(FMT_IDS[mat.fmt], parts, Xf, mat.K, mat.N, mat.group, cols=cols)
         dt = time.perf_counter() - t0
         frac = ncols / mat.N
-        done_bytes += call_bytes(mat, M) * frac
+        done_bytes += call_bytes(mat, M, head) * frac
         t_total += dt
         cols_done += ncols
         calls += 1
         i += 1
     gbs = done_bytes / t_total / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "us_per_call": t_total / (done_bytes / call_bytes(wl.matrices[0], M)) * 1e6,
+            "us_per_call": t_total / (done_bytes / call_bytes(wl.matrices[0], M, head)) * 1e6,
             "sample": f"{calls} oracle verify call(s), {cols_done} output columns x {M} rows "
                       f"of {workload}, {t_total:.1f} s single-threaded; GB/s of the sample's "
                       "algorithmic bytes"}
@@ -299,7 +318,9 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
-                  use_graphs=not args.no_graph)
+                  use_graphs=not args.no_graph, head=args.head)
+    rotated = any(l[0].rotate for l in stack.layers)
+    greedy = rotated and args.head == "greedy"
     peak, peak_kind = peaks()
     phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
 
@@ -319,8 +340,9 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     bytes_step = stack.bytes_per_step[args.M]
     value = replica_value(bytes_step, world, ms_per_step)
 
-    # dominant kernel: the verify launch, timed alone (verify-only loop)
-    if any(l[0].rotate for l in stack.layers):
+    # dominant kernel: the verify launch, timed alone (verify-only loop) when
+    # the step also launches the separate rotation
+    if rotated and args.head == "two-call":
         ms_v = reduce_max(timed(torch, lambda: stack.run(args.M, verify_only=True), args.steps,
                                 args.warmup, barrier))
     else:
@@ -344,14 +366,20 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     # pinned host memory to the device, the verify stack, the last Y back
     mat0 = stack.layers[0][0]
     x_host = torch.from_numpy(stack.layers[0][3].cpu().numpy()).pin_memory()
-    y_host = torch.zeros((args.M, stack.layers[-1][0].N), dtype=torch.float32).pin_memory()
     X_dev = stack.layers[0][3]
-    Y_last = stack.layers[-1][5]
+    if greedy:       # the result of a greedy step: each row's column and logit
+        outs = [(stack.idx, torch.zeros(8, dtype=torch.int32).pin_memory()),
+                (stack.val, torch.zeros(8, dtype=torch.float32).pin_memory())]
+    else:
+        outs = [(stack.layers[-1][5], torch.zeros((args.M, stack.layers[-1][0].N),
+                                                  dtype=torch.float32).pin_memory())]
+    d2h = sum(h[:args.M].numel() * h.element_size() for _, h in outs)
 
     def e2e_step():
         X_dev[:args.M].copy_(x_host[:args.M], non_blocking=True)
         stack.run(args.M)
-        y_host.copy_(Y_last[:args.M], non_blocking=True)
+        for d, h in outs:
+            h[:args.M].copy_(d[:args.M], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(args.warmup):
@@ -390,6 +418,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
                       "ctas_n": shape[3]},
             "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
+            "head": args.head if rotated else None,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "per_M": per_M,
@@ -402,12 +431,12 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                      "bytes_per_launch": bytes_launch, "us_per_launch": round(us_launch, 3)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": args.M * mat0.K * 2,
-                "d2h_bytes_per_step": args.M * stack.layers[-1][0].N * 4},
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * stack.launches_per_step,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.M)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.M, head=args.head)
     return line
 
 
@@ -432,7 +461,7 @@ def run_reference(args):
     for _ in range(args.steps):
         oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
     dt = time.perf_counter() - t0
-    sample_bytes = call_bytes(mat, M) * ncols / mat.N
+    sample_bytes = call_bytes(mat, M, args.head) * ncols / mat.N
     gbs = sample_bytes * args.steps / dt / 1e9
     sample = (f"{ncols} of {mat.N} output columns x {M} rows of {args.workload} per step, "
               "fp64 oracle, single-threaded")

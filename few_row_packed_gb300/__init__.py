@@ -28,6 +28,8 @@ PLAN_TCGEN05 = 0x10
 KERNEL_FEWROW = 1
 KERNEL_GEMV = 2
 KERNEL_FEWROW_TC = 3
+FUSED_ROTATE = 0x1
+FUSED_ARGMAX = 0x2
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
 
@@ -79,6 +81,9 @@ def lib():
             "lbv_plan_device_status": (st, [P]),
             "lbv_verify_gemm": (st, [P, P, I, I, P, P, I, P, S, P]),
             "lbv_fwht128": (st, [P, P, I, I, I, P, P]),
+            "lbv_fused_workspace_bytes": (S, []),
+            "lbv_fused_rotation": (st, [P, P, I, I, I, P, P]),
+            "lbv_verify_fused": (st, [P, P, I, I, P, U, P, P, I, P, P, P, S, P]),
             "lbv_dequant_fp16": (st, [P, P, P, P]),
             "lbv_last_error": (ctypes.c_char_p, []),
             "lbv_version": (ctypes.c_char_p, []),
@@ -256,6 +261,30 @@ def verify_gemm_host(plan: Plan, x_host, M: int, Wp, y_host, x_dev, y_dev, strea
     x_dev[:M].copy_(x_host[:M], non_blocking=True)
     verify_gemm(plan, x_dev, M, Wp, y_dev, stream=stream)
     y_host[:M].copy_(y_dev[:M], non_blocking=True)
+
+
+def fused_workspace_bytes() -> int:
+    return int(lib().lbv_fused_workspace_bytes())
+
+
+def verify_fused(plan: Plan, X, M: int, Wp, ops: int, Y=None, idx=None, val=None,
+                 workspace=None, signs=None, ldx: int | None = None, ldy: int | None = None,
+                 stream=None):
+    """Fused head: Y = rot(X) . W with FUSED_ROTATE, and with FUSED_ARGMAX the
+    per-row argmax column (idx, int32 [M]) and logit (val, fp32 [M] or None);
+    Y may be None then.  workspace: device bytes, zeroed once by the caller."""
+    ldx = plan.K if ldx is None else ldx
+    ldy = plan.N if ldy is None else ldy
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().lbv_verify_fused(plan.handle, _ptr(X), M, ldx, _ptr(Wp), ops, _ptr(signs),
+                                  _ptr(Y), ldy, _ptr(idx), _ptr(val), _ptr(workspace), ws,
+                                  _stream(stream)))
+
+
+def fused_rotation(X, Xr, M: int, K: int, dtype: int = F16, signs=None, stream=None):
+    """Test export: the rotation exactly as the fused head computes it."""
+    _check(lib().lbv_fused_rotation(_ptr(X), _ptr(Xr), M, K, dtype, _ptr(signs),
+                                    _stream(stream)))
 
 
 def fwht128(X, Xr, M: int, K: int, dtype: int = F16, signs=None, stream=None):

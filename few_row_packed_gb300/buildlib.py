@@ -27,6 +27,7 @@ SOURCES = [
     "verify_affine2_g64.cu",
     "verify_affine2_g128.cu",
     "verify_q4_0.cu",
+    "fused_aux.cu",
     "tc_aux.cu",
     "tc_sign1.cu",
     "tc_affine2_g32.cu",

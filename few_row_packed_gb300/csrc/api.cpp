@@ -69,16 +69,26 @@ int k_quantum(lbv_format fmt, int group)
     return 0;
 }
 
-// Shape bookkeeping: clamp the split so every slice has >= 1 chunk.
-void finish_shape(lbv::Shape& sh, int64_t nchunks)
+// K slices of a split start at multiples of `step` chunks: whole 128-element
+// blocks whenever K allows it, so the fused head can rotate each slice on its
+// own (only Q4_0's 64-element chunks are shorter than a block).
+int slice_step(const lbv_plan* P)
 {
-    int cps = (int)((nchunks + sh.splits - 1) / sh.splits);
-    sh.splits = (int)((nchunks + cps - 1) / cps);
+    return (P->K % 128 == 0 && P->fi.chunk_k < 128) ? 128 / P->fi.chunk_k : 1;
 }
 
-int shape_cps(const lbv::Shape& sh, int64_t nchunks)
+int shape_cps(const lbv::Shape& sh, int64_t nchunks, int step)
 {
-    return (int)((nchunks + sh.splits - 1) / sh.splits);
+    const int cps = (int)((nchunks + sh.splits - 1) / sh.splits);
+    return (cps + step - 1) / step * step;
+}
+
+// Shape bookkeeping: clamp the split so every slice has >= 1 chunk (a fixed
+// point: shape_cps of the result equals the cps it was derived from).
+void finish_shape(lbv::Shape& sh, int64_t nchunks, int step)
+{
+    const int cps = shape_cps(sh, nchunks, step);
+    sh.splits = (int)((nchunks + cps - 1) / cps);
 }
 
 constexpr size_t kSmemCap = 220 * 1024;        // per CTA, of 227 KB
@@ -99,8 +109,8 @@ size_t tile_chunk_bytes(const lbv_plan* P)
 bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
 {
     const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
-    finish_shape(sh, P->layout.nchunks);
-    const int cps = shape_cps(sh, P->layout.nchunks);
+    finish_shape(sh, P->layout.nchunks, slice_step(P));
+    const int cps = shape_cps(sh, P->layout.nchunks, slice_step(P));
     const int64_t ntiles = P->layout.ntiles;
     int64_t G = std::max<int64_t>(1, std::min<int64_t>(ntiles, P->sms / sh.splits));
     if (ctas_req > 0)
@@ -138,7 +148,7 @@ lbv::Shape default_shape(lbv_plan* P)
         lbv::Shape sh = {warps, tpw, s, 0, 0};
         if (!complete_shape(P, sh, 0) || sh.splits != s)
             continue;
-        const int cps = shape_cps(sh, P->layout.nchunks);
+        const int cps = shape_cps(sh, P->layout.nchunks, slice_step(P));
         const int64_t tmax = (P->layout.ntiles + sh.ctas_n - 1) / sh.ctas_n;
         const int64_t umax = ((tmax + tpw - 1) / tpw + warps - 1) / warps;
         const double cost = (double)umax * tpw * warps * cps * tile_chunk_bytes(P) +
@@ -550,28 +560,28 @@ lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int c
 // --------------------------------------------------------------------------
 // Verify
 
-static lbv_status check_verify_args(const lbv_plan* P, const void* X, int M, int ldx,
-                                    const void* Wp, const float* Y, int ldy,
+static lbv_status check_verify_args(const char* fn, const lbv_plan* P, const void* X, int M,
+                                    int ldx, const void* Wp, const float* Y, int ldy,
                                     const void* workspace, size_t workspace_bytes)
 {
     if (!P)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: plan is NULL");
+        return fail(LBV_ERR_INVALID_ARG, "%s: plan is NULL", fn);
     if (M < 1 || M > 8)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: M=%d outside 1..8", M);
+        return fail(LBV_ERR_INVALID_ARG, "%s: M=%d outside 1..8", fn, M);
     if (!X || !Wp || !Y)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: null X, Wp or Y");
+        return fail(LBV_ERR_INVALID_ARG, "%s: null X, Wp or Y", fn);
     if (ldx < P->K || ldy < P->N)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: ldx=%d < K=%d or ldy=%d < N=%d", ldx,
+        return fail(LBV_ERR_INVALID_ARG, "%s: ldx=%d < K=%d or ldy=%d < N=%d", fn, ldx,
                     P->K, ldy, P->N);
     if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: Wp not 16-byte aligned");
+        return fail(LBV_ERR_INVALID_ARG, "%s: Wp not 16-byte aligned", fn);
     if ((reinterpret_cast<uintptr_t>(X) & 1u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 3u) != 0)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: X or Y misaligned for its element type");
+        return fail(LBV_ERR_INVALID_ARG, "%s: X or Y misaligned for its element type", fn);
     if (workspace_bytes != 0 && !workspace)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: workspace_bytes without workspace");
+        return fail(LBV_ERR_INVALID_ARG, "%s: workspace_bytes without workspace", fn);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_gemm: current device %d is not the plan's %d",
+        return fail(LBV_ERR_INVALID_ARG, "%s: current device %d is not the plan's %d", fn,
                     dev, P->device);
     return LBV_OK;
 }
@@ -591,10 +601,17 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.ntiles = (int)P->layout.ntiles;
     p.nchunks = (int)P->layout.nchunks;
     p.splits = P->shape.splits;
-    p.cps = shape_cps(P->shape, P->layout.nchunks);
+    p.cps = shape_cps(P->shape, P->layout.nchunks, slice_step(P));
     p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
     p.err = P->dev_err;
     p.zero = 0;
+    p.rot = 0;
+    p.store_y = 1;
+    p.signs = nullptr;
+    p.amax_keys = nullptr;
+    p.amax_done = nullptr;
+    p.amax_idx = nullptr;
+    p.amax_val = nullptr;
     return p;
 }
 
@@ -630,11 +647,111 @@ lbv_status lbv_verify_gemm(const lbv_plan* P, const void* X, int M, int ldx, con
                            lbv_stream stream)
 {
     g_err.clear();
-    lbv_status st = check_verify_args(P, X, M, ldx, Wp, Y, ldy, workspace, workspace_bytes);
+    lbv_status st = check_verify_args("lbv_verify_gemm", P, X, M, ldx, Wp, Y, ldy, workspace,
+                                      workspace_bytes);
     if (st != LBV_OK)
         return st;
     return lbv_verify_launch_internal(P, X, M, ldx, Wp, Y, ldy, P->use_gemv[M] != 0,
                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+// --------------------------------------------------------------------------
+// Fused head
+
+// Argmax keys (8 x 8 bytes) and the count of finished CTAs, padded.
+static constexpr size_t kFusedWorkspace = 128;
+
+size_t lbv_fused_workspace_bytes(void)
+{
+    return kFusedWorkspace;
+}
+
+lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, const void* Wp,
+                            unsigned ops, const uint32_t* signs, float* Y, int ldy,
+                            int32_t* argmax_idx, float* argmax_val, void* workspace,
+                            size_t workspace_bytes, lbv_stream stream)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: plan is NULL");
+    if (ops & ~(LBV_FUSED_ROTATE | LBV_FUSED_ARGMAX))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: unknown ops bits 0x%x", ops);
+    const bool argmax = (ops & LBV_FUSED_ARGMAX) != 0, rotate = (ops & LBV_FUSED_ROTATE) != 0;
+    if (!Y && !argmax)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: no output (Y NULL without argmax)");
+    // the checks of lbv_verify_gemm, with Y optional
+    float dummy_y[1];
+    lbv_status st = check_verify_args("lbv_verify_fused", P, X, M, ldx, Wp, Y ? Y : dummy_y,
+                                      Y ? ldy : P->N, nullptr, 0);
+    if (st != LBV_OK)
+        return st;
+    if (P->tc)
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_verify_fused: not available on LBV_PLAN_TCGEN05 plans");
+    if (rotate) {
+        if (P->K % 128 != 0)
+            return fail(LBV_ERR_UNSUPPORTED, "lbv_verify_fused: rotation needs K %% 128 == 0 (K=%d)",
+                        P->K);
+        const int cps = shape_cps(P->shape, P->layout.nchunks, slice_step(P));
+        if (P->shape.splits > 1 && (cps * P->fi.chunk_k) % 128 != 0)
+            return fail(LBV_ERR_UNSUPPORTED,
+                        "lbv_verify_fused: the plan's K slices (%d elements) are not whole "
+                        "128-element blocks", cps * P->fi.chunk_k);
+        if (reinterpret_cast<uintptr_t>(signs) & 3u)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: signs not 4-byte aligned");
+    }
+    if (argmax) {
+        if (!argmax_idx)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: argmax without argmax_idx");
+        if ((reinterpret_cast<uintptr_t>(argmax_idx) & 3u) ||
+            (reinterpret_cast<uintptr_t>(argmax_val) & 3u))
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused: argmax outputs misaligned");
+        if (!workspace || workspace_bytes < kFusedWorkspace ||
+            (reinterpret_cast<uintptr_t>(workspace) & 15u))
+            return fail(LBV_ERR_WORKSPACE,
+                        "lbv_verify_fused: argmax needs a 16-byte aligned, zero-initialised "
+                        "workspace of %zu bytes", kFusedWorkspace);
+    }
+    lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, Y ? ldy : P->N);
+    p.rot = rotate ? 1 : 0;
+    p.signs = rotate ? signs : nullptr;
+    p.store_y = Y ? 1 : 0;
+    if (argmax) {
+        p.amax_keys = static_cast<unsigned long long*>(workspace);
+        p.amax_done = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(workspace) + 64);
+        p.amax_idx = argmax_idx;
+        p.amax_val = argmax_val;
+    }
+    lbv::LaunchOpts o;
+    o.pdl = (P->flags & LBV_PLAN_PDL) != 0;
+    const cudaError_t e = ops_for(P->fmt, P->group)
+                              ->launch(P->xdtype, P->shape, p, o,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_verify_fused: launch");
+    return LBV_OK;
+}
+
+lbv_status lbv_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
+                              const uint32_t* signs, lbv_stream stream)
+{
+    g_err.clear();
+    if (!X || !Xr)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fused_rotation: null X or Xr");
+    if (M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fused_rotation: M=%d outside 1..8", M);
+    if (K <= 0 || K % 128 != 0)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fused_rotation: K=%d not a positive multiple of 128",
+                    K);
+    if (dtype != LBV_F16 && dtype != LBV_BF16)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fused_rotation: unknown dtype %d", (int)dtype);
+    if ((reinterpret_cast<uintptr_t>(X) & 1u) || (reinterpret_cast<uintptr_t>(Xr) & 1u) ||
+        (reinterpret_cast<uintptr_t>(signs) & 3u))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_fused_rotation: misaligned pointer");
+    cudaError_t e = lbv::launch_fused_rotation(X, Xr, M, K, dtype, signs,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_fused_rotation: launch");
+    return LBV_OK;
 }
 
 lbv_status lbv_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dtype,

@@ -22,6 +22,15 @@ struct VerifyParams {
     int cps;                // chunks per slice (the last slice may be shorter)
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
     unsigned zero;          // always 0 (keeps decode constants in registers)
+    // fused head (lbv_verify_fused); lbv_verify_gemm leaves rot = 0,
+    // amax_keys = NULL and store_y = 1
+    int rot;                // 1: rotate the staged X blockwise (FWHT-128) first
+    int store_y;            // 0: the logits Y are not written
+    const uint32_t* signs;  // rotation: optional K-bit +-1 mask (NULL: none)
+    unsigned long long* amax_keys;  // workspace [8]: running argmax keys (NULL: no argmax)
+    unsigned* amax_done;    // workspace: CTAs finished with their keys
+    int* amax_idx;          // [M] argmax column of each row
+    float* amax_val;        // [M] its logit (NULL: not written)
 };
 
 // Launch shape of the few-row kernel.
@@ -49,6 +58,10 @@ cudaError_t launch_gemv(lbv_format fmt, lbv_dtype xt, int group, const VerifyPar
 
 cudaError_t launch_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dt,
                            const uint32_t* signs, cudaStream_t st);
+
+// Test export: the fused head's rotation on its own (fused_aux.cu).
+cudaError_t launch_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dtype dt,
+                                  const uint32_t* signs, cudaStream_t st);
 
 cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, int N,
                            int ntiles, int nchunks, uint16_t* W, cudaStream_t st);

@@ -349,6 +349,143 @@ __device__ __forceinline__ float2 f16pair(uint32_t v)
     return __half22float2(h);
 }
 
+// One fp32 value rounded to nearest even in the X dtype (bit pattern).
+template <int XT>
+__device__ __forceinline__ uint16_t round_x(float v)
+{
+    if constexpr (XT == LBV_F16)
+        return __half_as_ushort(__float2half_rn(v));
+    else
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// Two entries (i, j), (i, j + 1) of the 16-point Sylvester Hadamard matrix,
+// H16[i][j] = (-1)^popcount(i & j), as a packed pair of the X dtype.
+template <int XT>
+__device__ __forceinline__ uint32_t h16_pair(int i, int j)
+{
+    constexpr uint32_t one = XT == LBV_F16 ? 0x3C00u : 0x3F80u;   // +1.0
+    const uint32_t lo = one | ((uint32_t)(__popc(i & j) & 1) << 15);
+    const uint32_t hi = one | ((uint32_t)(__popc(i & (j + 1)) & 1) << 15);
+    return lo | (hi << 16);
+}
+
+// Argmax key of (logit v, column n): keys compare like the logits, and among
+// equal logits the smaller column has the larger key.  -0 counts as +0, any
+// NaN ranks above every number (the first NaN wins), and no key is 0, so 0
+// stands for "no column yet".
+__device__ __forceinline__ unsigned long long amax_key(float v, int n)
+{
+    uint32_t u = __float_as_uint(v);
+    if ((u << 1) == 0u)
+        u = 0u;
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (v != v)
+        u = 0xffffffffu;
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xffffffffu - (uint32_t)n);
+}
+
+__device__ __forceinline__ float amax_key_value(unsigned long long k)
+{
+    const uint32_t u = (uint32_t)(k >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// Largest key among the 8 lanes of a warp that share lane & 3 (the lanes
+// holding the same rows of an m16n8 accumulator).
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k)
+{
+#pragma unroll
+    for (int s = 4; s <= 16; s <<= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, s);
+        k = o > k ? o : k;
+    }
+    return k;
+}
+
+// ---------------------------------------------------------------------------
+// Fused head prologue, on X rows staged row-major in shared memory (row m at
+// xs + m * RS bytes, RS % 16 == 0, RS / 4 = 4 mod 8 for conflict-free rows).
+
+// ldmatrix row address of this lane within the X rows: lanes 8i..8i+7 give the
+// rows of matrix i, which covers K elements 8i..8i+7 of a 32-element span.
+__device__ __forceinline__ uint32_t ldsm_lane_offset(int RS, int lane)
+{
+    return (uint32_t)((lane & 7) * RS + (lane >> 3) * 16);
+}
+
+// Flips the sign of X[m][k] (rows m < M, k < have; have % 32 == 0) where bit
+// kb + k of `signs` is set.  Threads tid = 0, nthreads, ... share the work.
+__device__ __forceinline__ void flip_signs(const uint32_t* signs, unsigned char* xs, int RS, int M,
+                                           int kb, int have, int tid, int nthreads)
+{
+    const int words = have / 32;                       // mask words per row
+    for (int i = tid; i < M * words; i += nthreads) {
+        const int m = i / words, wi = i - m * words;
+        const uint32_t sg = signs[(kb >> 5) + wi];
+        uint32_t* e = reinterpret_cast<uint32_t*>(xs + (size_t)m * RS + wi * 64);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            e[j] ^= (((sg >> (2 * j)) & 1u) << 15) | (((sg >> (2 * j + 1)) & 1u) << 31);
+    }
+}
+
+// Rotates blocks 0..nblk-1 of the 8 staged rows in place (warps warp,
+// warp + nwarps, ... take one block each in turn):
+//   x'_b = H128 x_b / sqrt(128),  H[i][j] = (-1)^popcount(i & j)  (Sylvester).
+// H128 = H8 (x) H16, so with the block split into sub-blocks J of 16 elements
+//   U_J = H16 x_J                  one m16n8k16 MMA per sub-block: H16 is the A
+//                                  operand, the sub-block's X fragment (as the
+//                                  verify main loop reads it) is B;
+//   x'_(16 I + i) = sum_J H8[I][J] U_J[i]   an 8-point butterfly across the
+//                                  eight accumulators each lane holds.
+// fp32 sums, one multiplication by the fp32 value of 1/sqrt(128), one rounding
+// to the X dtype.  A warp reads its whole block before writing it back.  All 8
+// rows are rotated; a row's results depend on that row alone.
+template <int XT>
+__device__ __forceinline__ void rotate_x(uint32_t xs_a, unsigned char* xs, int RS, int nblk,
+                                         int warp, int nwarps, int lane)
+{
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t h0 = h16_pair<XT>(g, 2 * t), h1 = h16_pair<XT>(g + 8, 2 * t);
+    const uint32_t h2 = h16_pair<XT>(g, 2 * t + 8), h3 = h16_pair<XT>(g + 8, 2 * t + 8);
+    const uint32_t xa = xs_a + ldsm_lane_offset(RS, lane);
+    constexpr float kInvSqrt128 = 0.08838834764831845f;
+#pragma unroll 1
+    for (int b = warp; b < nblk; b += nwarps) {
+        float u[8][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 r = ldsm_x4(xa + b * 256 + q * 64);     // sub-blocks 2q, 2q + 1
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                u[2 * q][e] = u[2 * q + 1][e] = 0.f;
+            mma16816<XT>(u[2 * q], h0, h1, h2, h3, r.x, r.y);
+            mma16816<XT>(u[2 * q + 1], h0, h1, h2, h3, r.z, r.w);
+        }
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+            for (int J = 0; J < 8; ++J)
+                if (!(J & h))
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = u[J][e], c = u[J + h][e];
+                        u[J][e] = a + c;
+                        u[J + h][e] = a - c;
+                    }
+        // u[I][e] is element 16 I + g + 8 (e >> 1) of row 2 t + (e & 1)
+#pragma unroll
+        for (int I = 0; I < 8; ++I)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 2 * t + (e & 1), i = 16 * I + g + 8 * (e >> 1);
+                *reinterpret_cast<uint16_t*>(xs + (size_t)m * RS + (b * 128 + i) * 2) =
+                    round_x<XT>(u[I][e] * kInvSqrt128);
+            }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Compile-time geometry of one (format, group, warps, tiles-per-warp) kernel.
 
@@ -362,7 +499,8 @@ struct Geometry {
     static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
-    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16;   // + the X barrier
+    // + the X barrier (16) + the CTA's argmax keys of the fused head (64)
+    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16 + 64;
     // corrections and row sums per group of the slice
     static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
 };
@@ -376,7 +514,8 @@ __host__ __device__ constexpr int x_row_stride(int cps)
 }
 
 // Shared memory carve-up (bytes):
-//   ring | mbarriers (+ X barrier) | xs (X rows) | corr | rsum (affine) | part (K split)
+//   ring | mbarriers (+ X barrier, argmax keys) | xs (X rows) | corr | rsum (affine) |
+//   part (K split)
 template <int FMT, int GROUP, int NW, int TPW>
 __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
 {
@@ -553,9 +692,12 @@ struct VerifyKernel {
     // A unit's results: straight to Y (no K split), or into the shared memory
     // of the cluster CTA that owns the tile (K split).  Tile t0 + i belongs to
     // rank i % S and lands in its slot [(i / S) * S + my_rank].
+    // With an argmax (fused head, no K split) the unit's best column of each
+    // row also goes into the CTA's keys.
     static __device__ __forceinline__ void store_unit(const VerifyParams& p, int t1, int tile0,
                                                       const float (&y)[TPW][4], int g, int t,
-                                                      float* part, int tbase, int lane)
+                                                      float* part, int tbase, int lane,
+                                                      unsigned long long* akeys)
     {
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
@@ -573,6 +715,8 @@ struct VerifyKernel {
                     dst[j * 32 + lane] = y[tl][j];
                 continue;
             }
+            if (!p.store_y)
+                continue;
             const int n0 = tile * 16 + g, n1 = n0 + 8;
             const int m0 = 2 * t, m1 = 2 * t + 1;
             if (m0 < p.M) {
@@ -582,6 +726,32 @@ struct VerifyKernel {
             if (m1 < p.M) {
                 if (n0 < p.N) p.Y[(size_t)m1 * p.ldy + n0] = y[tl][1];
                 if (n1 < p.N) p.Y[(size_t)m1 * p.ldy + n1] = y[tl][3];
+            }
+        }
+        if (p.splits == 1 && p.amax_keys) {
+            unsigned long long k0 = 0ull, k1 = 0ull;           // rows 2t, 2t + 1
+#pragma unroll
+            for (int tl = 0; tl < TPW; ++tl) {
+                const int tile = tile0 + tl;
+                const int n0 = tile * 16 + g, n1 = n0 + 8;
+                if (tile >= t1)
+                    continue;
+                if (n0 < p.N) {
+                    k0 = max(k0, amax_key(y[tl][0], n0));
+                    k1 = max(k1, amax_key(y[tl][1], n0));
+                }
+                if (n1 < p.N) {
+                    k0 = max(k0, amax_key(y[tl][2], n1));
+                    k1 = max(k1, amax_key(y[tl][3], n1));
+                }
+            }
+            k0 = warp_max_key(k0);
+            k1 = warp_max_key(k1);
+            if (g == 0) {
+                if (2 * t < p.M && k0)
+                    atomicMax(akeys + 2 * t, k0);
+                if (2 * t + 1 < p.M && k1)
+                    atomicMax(akeys + 2 * t + 1, k1);
             }
         }
     }
@@ -620,13 +790,6 @@ struct VerifyKernel {
                 k < have ? X[(size_t)m * p.ldx + kb + k] : (uint16_t)0;
         }
         return false;
-    }
-
-    // This lane's ldmatrix row address offset within the X rows: lanes 8i..8i+7
-    // give the rows of matrix i, which covers K elements 8i..8i+7 of a k-tile pair.
-    static __device__ __forceinline__ uint32_t ldsm_lane_offset(int RS, int lane)
-    {
-        return (uint32_t)((lane & 7) * RS + (lane >> 3) * 16);
     }
 
     // Per-group corrections of the slice, one warp per chunk:
@@ -696,6 +859,34 @@ struct VerifyKernel {
         }
     }
 
+    // Fused head epilogue: the CTA's keys go to the workspace; the CTA that
+    // finishes last turns the keys into the rows' argmax columns and logits
+    // and leaves the workspace zeroed for the next call.
+    static __device__ void amax_finish(const VerifyParams& p, const unsigned long long* akeys)
+    {
+        __syncthreads();
+        if ((int)threadIdx.x < p.M) {
+            const unsigned long long k = akeys[threadIdx.x];
+            if (k)
+                atomicMax(p.amax_keys + threadIdx.x, k);
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned total = gridDim.x * gridDim.y;
+            if (atomicAdd(p.amax_done, 1u) == total - 1u) {
+                __threadfence();
+                for (int m = 0; m < p.M; ++m) {
+                    const unsigned long long k = atomicExch(p.amax_keys + m, 0ull);
+                    p.amax_idx[m] = (int)(0xffffffffu - (uint32_t)k);   // -1: no column
+                    if (p.amax_val)
+                        p.amax_val[m] = amax_key_value(k);
+                }
+                atomicExch(p.amax_done, 0u);
+            }
+        }
+    }
+
     static __device__ void run(const VerifyParams& p, unsigned char* smem)
     {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -718,6 +909,10 @@ struct VerifyKernel {
         const uint32_t ring_w = smem_u32(ring) + warp * STAGES * G::SLOT_B;
         const uint32_t bars_w = smem_u32(bars) + warp * STAGES * 8;
         const unsigned char* ring_wp = ring + (size_t)warp * STAGES * G::SLOT_B;
+        unsigned long long* akeys =
+            reinterpret_cast<unsigned long long*>(bars + NW * STAGES * 8 + 16);
+        if (threadIdx.x < 8)
+            akeys[threadIdx.x] = 0ull;
 
         // this warp's units of TPW tiles within [t0, t1)
         const int nunits = (t1 - t0 + TPW - 1) / TPW;
@@ -774,6 +969,18 @@ struct VerifyKernel {
         if (x_async && !mbar_try(xbar, 0) && !mbar_wait(xbar, 0))
             x_ok = false;
         const uint32_t xs_a = smem_u32(xs);
+        if (p.rot) {
+            // every thread's wait on X has ended before X is rewritten
+            const int kb = c0 * T::CHUNK_K, have = min(nch * T::CHUNK_K, p.K - kb);
+            if (__syncthreads_and(x_ok)) {
+                if (p.signs) {
+                    flip_signs(p.signs, xs, RS, p.M, kb, have, threadIdx.x, NW * 32);
+                    __syncthreads();
+                }
+                rotate_x<XT>(xs_a, xs, RS, have / 128, warp, NW, lane);
+            }
+            __syncthreads();
+        }
         corrections(xs_a, RS, corr, rsum, nch, warp, lane);
         __syncthreads();
         if (S > 1)
@@ -792,7 +999,9 @@ struct VerifyKernel {
 #pragma unroll 1
         for (; q < Q; ++q) {
             const uint32_t bar = bars_w + slot * 8;
-            if (!mbar_try(bar, parity) && !mbar_wait(bar, parity)) {
+            // the whole warp leaves together (the unit store below shuffles)
+            const bool landed = mbar_try(bar, parity) || mbar_wait(bar, parity);
+            if (!__all_sync(0xffffffffu, landed)) {
                 ok = false;
                 break;
             }
@@ -827,7 +1036,7 @@ struct VerifyKernel {
                 process_chunk(w[1], sd[1], cc + 1, xa_lane, corr, rsum, bases, y, lane);
             cc += nc;
             if (cc == nch) {
-                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane);
+                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane, akeys);
 #pragma unroll
                 for (int tl = 0; tl < TPW; ++tl)
                     y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
@@ -846,18 +1055,25 @@ struct VerifyKernel {
         }
 
         if (S > 1)
-            cluster_reduce(p, part, t0, t1);
+            cluster_reduce(p, part, t0, t1, akeys);
+        if (p.amax_keys)
+            amax_finish(p, akeys);
     }
 
     // After the cluster barrier each CTA sums, in rank order 0..S-1, the
     // partials its cluster peers stored for the tiles it owns, and writes Y.
-    static __device__ void cluster_reduce(const VerifyParams& p, float* part, int t0, int t1)
+    // With an argmax each thread's elements lie in one row (the stride NW * 32
+    // is a multiple of 128), so its best key needs only a warp reduction.
+    static __device__ void cluster_reduce(const VerifyParams& p, float* part, int t0, int t1,
+                                          unsigned long long* akeys)
     {
+        static_assert((NW * 32) % 128 == 0, "one row per thread in the reduction");
         cg::cluster_group cl = cg::this_cluster();
         cl.sync();
         const int S = p.splits;
         const int rank = (int)cl.block_rank();
         const int nown = (t1 - t0 - rank + S - 1) / S;        // tiles t0 + rank + S*k
+        unsigned long long best = 0ull;
         for (int e = (int)threadIdx.x; e < nown * 128; e += NW * 32) {
             const int k = e >> 7, r = e & 127;
             const float* src = part + (k * S) * 128 + r;
@@ -868,8 +1084,19 @@ struct VerifyKernel {
             const int j = r >> 5, ln = r & 31;
             const int n = tile * 16 + (ln >> 2) + 8 * (j >> 1);
             const int m = 2 * (ln & 3) + (j & 1);
-            if (n < p.N && m < p.M)
-                p.Y[(size_t)m * p.ldy + n] = acc;
+            if (n < p.N && m < p.M) {
+                if (p.store_y)
+                    p.Y[(size_t)m * p.ldy + n] = acc;
+                if (p.amax_keys)
+                    best = max(best, amax_key(acc, n));
+            }
+        }
+        if (p.amax_keys) {
+            best = warp_max_key(best);
+            const int lane = threadIdx.x & 31;
+            const int m = 2 * (lane & 3) + ((threadIdx.x >> 5) & 1);
+            if (lane < 4 && m < p.M && best)
+                atomicMax(akeys + m, best);
         }
     }
 };

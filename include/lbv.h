@@ -14,7 +14,7 @@
  *   - Plain C ABI: pointers and sizes only.  "dev" pointers are CUDA device
  *     memory of the current device, "host" pointers are host memory.
  *   - The caller owns every buffer.  The library never allocates in
- *     lbv_verify_gemm, lbv_fwht128 or lbv_dequant_fp16.  Plans are created and
+ *     lbv_verify_gemm, lbv_verify_fused, lbv_fwht128 or lbv_dequant_fp16.  Plans are created and
  *     destroyed by the caller and are immutable in between (safe to share
  *     between host threads).
  *   - Device work is asynchronous on the given stream; a status of LBV_OK
@@ -232,6 +232,63 @@ LBV_API lbv_status lbv_verify_gemm(const lbv_plan* plan, const void* X, int M, i
  */
 LBV_API lbv_status lbv_fwht128(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
                        const uint32_t* signs, lbv_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused head: the rotation as the verify's prologue and a greedy argmax as  */
+/* its epilogue, in one launch of the few-row kernel.                        */
+
+#define LBV_FUSED_ROTATE 0x1u  /* rotate X blockwise before the product        */
+#define LBV_FUSED_ARGMAX 0x2u  /* per-row argmax over the N logits              */
+
+/* Bytes of the workspace an argmax call needs (128). */
+LBV_API size_t lbv_fused_workspace_bytes(void);
+
+/*
+ * Y[m][:] = X'[m][:] . dequant(Wp) for rows m < M, with in the same kernel:
+ *   LBV_FUSED_ROTATE: X' is the blockwise rotation of lbv_fwht128 (signs
+ *     optional, dev uint32 [K/32] or NULL), computed per CTA from the staged
+ *     X tile and kept in shared memory.  Its arithmetic differs from
+ *     lbv_fwht128's: fp32 sums (the 16-point stages on the tensor cores), one
+ *     fp32 multiplication by 1/sqrt(128), one rounding to the dtype; a
+ *     rotated element can differ from the correctly rounded one by a unit in
+ *     the last place.  Without it X' = X.  Needs K % 128 == 0.
+ *   LBV_FUSED_ARGMAX: argmax_idx[m] (dev int32 [M]) = the column of the
+ *     largest fp32 logit of row m, the smallest such column on ties, -0 equal
+ *     to +0, the first NaN if any; argmax_val[m] (dev fp32 [M], or NULL) =
+ *     that logit, bit for bit the value Y would hold.  The logits need not be
+ *     written: Y may then be NULL (ldy ignored).
+ * dflash-mlx-bonsai2 README, "What this fork adds" (the verify GEMM with a
+ * fused sign, Hadamard and row-sum prep) and "What it does to the numbers"
+ * (greedy decoding; acceptance decided by the argmax, up to fp16 ties).
+ *
+ * The other arguments and rules are those of lbv_verify_gemm, except that
+ * the few-row kernel is used at every M (never the 1-row path).
+ * workspace: dev, 16-byte aligned, >= lbv_fused_workspace_bytes(), needed
+ * with LBV_FUSED_ARGMAX (else ignored; LBV_ERR_WORKSPACE when missing or
+ * short).  The caller zeroes it once before its first use; every call leaves
+ * it zeroed when its kernel completes.  Calls that may run at the same time
+ * (other streams) need distinct workspaces; calls in one stream can share one.
+ * Errors: LBV_ERR_INVALID_ARG as lbv_verify_gemm, for unknown ops bits, for
+ * no output (Y NULL without LBV_FUSED_ARGMAX), for argmax_idx NULL with
+ * LBV_FUSED_ARGMAX and for misaligned signs, argmax_idx or argmax_val;
+ * LBV_ERR_UNSUPPORTED for LBV_PLAN_TCGEN05 plans, for the rotation with
+ * K % 128 != 0 or with K slices of the plan's launch shape that are not
+ * whole 128-element blocks.  If a bounded wait in the kernel gives up, the
+ * plan's device status records it (lbv_plan_device_status) and argmax_idx
+ * may be -1.
+ */
+LBV_API lbv_status lbv_verify_fused(const lbv_plan* plan, const void* X, int M, int ldx,
+                                    const void* Wp, unsigned ops, const uint32_t* signs,
+                                    float* Y, int ldy, int32_t* argmax_idx, float* argmax_val,
+                                    void* workspace, size_t workspace_bytes, lbv_stream stream);
+
+/*
+ * Test export: X' exactly as lbv_verify_fused with LBV_FUSED_ROTATE computes
+ * it inside the verify kernel (the same device code, run on its own), for
+ * element-by-element checks.  Arguments as lbv_fwht128 (in place allowed).
+ */
+LBV_API lbv_status lbv_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
+                                      const uint32_t* signs, lbv_stream stream);
 
 /*
  * Test export: the dense fp16 dequantized matrix, W[k][n] (dev, [K][N]

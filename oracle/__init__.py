@@ -203,3 +203,17 @@ def fwht128(x, signs=None) -> np.ndarray:
         _load().orc_fwht128(_ptr(row), L, _ptr(s), _ptr(o))
         out[r] = o
     return out.reshape(shape)
+
+
+def argmax_rows(Y) -> np.ndarray:
+    """Greedy choice per row (dflash-mlx-bonsai2 README, "What it does to the
+    numbers": greedy decoding, acceptance by the argmax): the first column
+    holding the row's largest value; -0 equals +0 and a NaN counts as the
+    largest (the first NaN wins)."""
+    Y = np.asarray(Y, np.float64)
+    out = np.empty(Y.shape[0], np.int64)
+    for m in range(Y.shape[0]):
+        row = Y[m]
+        nan = np.flatnonzero(np.isnan(row))
+        out[m] = nan[0] if nan.size else int(np.argmax(row))
+    return out

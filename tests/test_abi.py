@@ -83,6 +83,15 @@ def test_bad_arguments_return_status(L):
     x = np.zeros(256, np.uint16)
     assert L.lbv_fwht128(x.ctypes.data, x.ctypes.data, 1, 100, 0, None, None) == lbv.ERR_INVALID_ARG
     assert L.lbv_fwht128(x.ctypes.data, x.ctypes.data, 9, 128, 0, None, None) == lbv.ERR_INVALID_ARG
+    assert L.lbv_fused_rotation(None, None, 1, 128, 0, None, None) == lbv.ERR_INVALID_ARG
+    assert L.lbv_fused_rotation(x.ctypes.data, x.ctypes.data, 1, 96, 0, None, None) == \
+        lbv.ERR_INVALID_ARG
+    assert L.lbv_fused_rotation(x.ctypes.data, x.ctypes.data, 0, 128, 0, None, None) == \
+        lbv.ERR_INVALID_ARG
+    assert L.lbv_verify_fused(None, None, 1, 1, None, lbv.FUSED_ARGMAX, None, None, 1, None,
+                              None, None, 0, None) == lbv.ERR_INVALID_ARG
+    assert "lbv_verify_fused" in lbv.last_error()
+    assert lbv.fused_workspace_bytes() == 128
     h = P()
     assert L.lbv_plan_create(1, 128, 16, 48, 0, 0, ctypes.byref(h)) == lbv.ERR_UNSUPPORTED
     assert h.value is None

@@ -322,3 +322,31 @@ def test_fwht_exact_sum_then_one_rounding(oracle_lib):
     for i in range(0, 128, 9):
         s = sum(Fraction(float(x[j])) * int(H[i, j]) for j in range(128))
         assert float(s) / np.sqrt(128.0) == y[i]
+
+
+# ----------------------------------------------------------------------------
+# Greedy argmax (fused head epilogue)
+
+def test_argmax_rows_hand_cases(oracle_lib):
+    """Hand-made rows: first of tied maxima, -0 equal to +0, negative rows,
+    the first NaN, a single column."""
+    nan, inf = float("nan"), float("inf")
+    Y = [[1.0, 3.0, 3.0, 2.0],
+         [-1.0, -0.0, 0.0, -2.0],
+         [-5.0, -3.0, -4.0, -3.0],
+         [1.0, nan, 5.0, nan],
+         [-inf, -inf, -inf, -inf],
+         [2.0, 1.0, inf, 0.5]]
+    assert oracle_lib.argmax_rows(np.array(Y)).tolist() == [1, 1, 1, 1, 0, 2]
+    assert oracle_lib.argmax_rows(np.array([[7.0]])).tolist() == [0]
+
+
+def test_argmax_rows_brute_force(oracle_lib):
+    """Against a pairwise-comparison definition on small random rows with
+    many ties (values drawn from a handful of levels)."""
+    rng = np.random.default_rng(11)
+    Y = rng.integers(-3, 4, size=(50, 9)).astype(np.float64)
+    got = oracle_lib.argmax_rows(Y)
+    for m in range(Y.shape[0]):
+        best = [n for n in range(9) if all(Y[m, n] >= Y[m, j] for j in range(9))]
+        assert got[m] == best[0]

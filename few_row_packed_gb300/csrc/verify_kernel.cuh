@@ -499,7 +499,8 @@ struct Geometry {
     static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
-    // + the X barrier (16) + the CTA's argmax keys of the fused head (64)
+    // + the X barrier and a flag word (16), the CTA's argmax keys of the fused
+    // head (64)
     static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16 + 64;
     // corrections and row sums per group of the slice
     static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
@@ -514,8 +515,8 @@ __host__ __device__ constexpr int x_row_stride(int cps)
 }
 
 // Shared memory carve-up (bytes):
-//   ring | mbarriers (+ X barrier, argmax keys) | xs (X rows) | corr | rsum (affine) |
-//   part (K split)
+//   ring | mbarriers (+ X barrier, flag, argmax keys) | xs (X rows) | corr |
+//   rsum (affine) | part (K split)
 template <int FMT, int GROUP, int NW, int TPW>
 __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
 {
@@ -692,12 +693,12 @@ struct VerifyKernel {
     // A unit's results: straight to Y (no K split), or into the shared memory
     // of the cluster CTA that owns the tile (K split).  Tile t0 + i belongs to
     // rank i % S and lands in its slot [(i / S) * S + my_rank].
-    // With an argmax (fused head, no K split) the unit's best column of each
-    // row also goes into the CTA's keys.
+    // With an argmax (fused head, no K split) the unit's best column of rows
+    // 2t and 2t + 1 also updates this lane's running keys ak.
     static __device__ __forceinline__ void store_unit(const VerifyParams& p, int t1, int tile0,
                                                       const float (&y)[TPW][4], int g, int t,
                                                       float* part, int tbase, int lane,
-                                                      unsigned long long* akeys)
+                                                      unsigned long long (&ak)[2])
     {
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
@@ -729,7 +730,6 @@ struct VerifyKernel {
             }
         }
         if (p.splits == 1 && p.amax_keys) {
-            unsigned long long k0 = 0ull, k1 = 0ull;           // rows 2t, 2t + 1
 #pragma unroll
             for (int tl = 0; tl < TPW; ++tl) {
                 const int tile = tile0 + tl;
@@ -737,21 +737,13 @@ struct VerifyKernel {
                 if (tile >= t1)
                     continue;
                 if (n0 < p.N) {
-                    k0 = max(k0, amax_key(y[tl][0], n0));
-                    k1 = max(k1, amax_key(y[tl][1], n0));
+                    ak[0] = max(ak[0], amax_key(y[tl][0], n0));
+                    ak[1] = max(ak[1], amax_key(y[tl][1], n0));
                 }
                 if (n1 < p.N) {
-                    k0 = max(k0, amax_key(y[tl][2], n1));
-                    k1 = max(k1, amax_key(y[tl][3], n1));
+                    ak[0] = max(ak[0], amax_key(y[tl][2], n1));
+                    ak[1] = max(ak[1], amax_key(y[tl][3], n1));
                 }
-            }
-            k0 = warp_max_key(k0);
-            k1 = warp_max_key(k1);
-            if (g == 0) {
-                if (2 * t < p.M && k0)
-                    atomicMax(akeys + 2 * t, k0);
-                if (2 * t + 1 < p.M && k1)
-                    atomicMax(akeys + 2 * t + 1, k1);
             }
         }
     }
@@ -861,29 +853,37 @@ struct VerifyKernel {
 
     // Fused head epilogue: the CTA's keys go to the workspace; the CTA that
     // finishes last turns the keys into the rows' argmax columns and logits
-    // and leaves the workspace zeroed for the next call.
-    static __device__ void amax_finish(const VerifyParams& p, const unsigned long long* akeys)
+    // and leaves the workspace zeroed for the next call.  One thread per row
+    // on every step, so the last CTA's tail is three round trips to L2: the
+    // fence after the key reductions, the ticket, the exchange of the keys.
+    // `last` is a shared flag word.
+    static __device__ void amax_finish(const VerifyParams& p, const unsigned long long* akeys,
+                                       unsigned* last)
     {
         __syncthreads();
-        if ((int)threadIdx.x < p.M) {
-            const unsigned long long k = akeys[threadIdx.x];
+        const int tid = (int)threadIdx.x;
+        if (tid < p.M) {                        // warp 0
+            const unsigned long long k = akeys[tid];
             if (k)
-                atomicMax(p.amax_keys + threadIdx.x, k);
+                atomicMax(p.amax_keys + tid, k);
+            __threadfence();                    // the CTA's reductions before its ticket
         }
-        __threadfence();
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             const unsigned total = gridDim.x * gridDim.y;
-            if (atomicAdd(p.amax_done, 1u) == total - 1u) {
-                __threadfence();
-                for (int m = 0; m < p.M; ++m) {
-                    const unsigned long long k = atomicExch(p.amax_keys + m, 0ull);
-                    p.amax_idx[m] = (int)(0xffffffffu - (uint32_t)k);   // -1: no column
-                    if (p.amax_val)
-                        p.amax_val[m] = amax_key_value(k);
-                }
-                atomicExch(p.amax_done, 0u);
+            *last = atomicAdd(p.amax_done, 1u) == total - 1u;
+        }
+        __syncthreads();
+        if (*last) {
+            __threadfence();                    // every CTA's reductions before the reads
+            if (tid < p.M) {
+                const unsigned long long k = atomicExch(p.amax_keys + tid, 0ull);
+                p.amax_idx[tid] = (int)(0xffffffffu - (uint32_t)k);   // -1: no column
+                if (p.amax_val)
+                    p.amax_val[tid] = amax_key_value(k);
             }
+            if (tid == 0)
+                atomicExch(p.amax_done, 0u);
         }
     }
 
@@ -991,6 +991,7 @@ struct VerifyKernel {
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl)
             y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
+        unsigned long long ak[2] = {0ull, 0ull};              // argmax keys, rows 2t, 2t + 1
         int cu = warp, cc = 0;                                // compute cursor
         const uint32_t xa_lane = xs_a + ldsm_lane_offset(RS, lane);
         bool ok = x_ok;
@@ -1036,7 +1037,7 @@ struct VerifyKernel {
                 process_chunk(w[1], sd[1], cc + 1, xa_lane, corr, rsum, bases, y, lane);
             cc += nc;
             if (cc == nch) {
-                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane, akeys);
+                store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane, ak);
 #pragma unroll
                 for (int tl = 0; tl < TPW; ++tl)
                     y[tl][0] = y[tl][1] = y[tl][2] = y[tl][3] = 0.f;
@@ -1054,10 +1055,20 @@ struct VerifyKernel {
                 mbar_wait(xbar, 0);
         }
 
+        if (S == 1 && p.amax_keys) {                          // the warp's keys into the CTA's
+            ak[0] = warp_max_key(ak[0]);
+            ak[1] = warp_max_key(ak[1]);
+            if (g == 0) {
+                if (2 * t < p.M && ak[0])
+                    atomicMax(akeys + 2 * t, ak[0]);
+                if (2 * t + 1 < p.M && ak[1])
+                    atomicMax(akeys + 2 * t + 1, ak[1]);
+            }
+        }
         if (S > 1)
             cluster_reduce(p, part, t0, t1, akeys);
         if (p.amax_keys)
-            amax_finish(p, akeys);
+            amax_finish(p, akeys, reinterpret_cast<unsigned*>(bars + NW * STAGES * 8 + 8));
     }
 
     // After the cluster barrier each CTA sums, in rank order 0..S-1, the

@@ -56,6 +56,9 @@ def parse_args():
                     help="rotated head: rotation fused into the verify launch (default), "
                          "lbv_fwht128 then lbv_verify_gemm, or fused rotation and per-row "
                          "argmax without writing the logits")
+    ap.add_argument("--stack", default="grouped", choices=["grouped", "calls"],
+                    help="multi-matrix workloads: every matrix in one grouped launch "
+                         "(default) or one verify call per matrix")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
     ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
@@ -146,7 +149,8 @@ class Stack:
     """Distinct packed matrices of a workload resident on the device."""
 
     def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int,
-                 use_graphs: bool = True, kernel: str = "mma", head: str = "fused"):
+                 use_graphs: bool = True, kernel: str = "mma", head: str = "fused",
+                 stack: str = "grouped"):
         import torch
         self.use_graphs = use_graphs
         self.graphs = {}
@@ -175,7 +179,7 @@ class Stack:
             if key not in plans:
                 plans[key] = lbv.Plan(FMT_IDS[mat.fmt], mat.K, mat.N, mat.group,
                                       lbv.DTYPE_BY_NAME[mat.xdtype], flags)
-                if shape:
+                if shape and (len(self.mats) == 1 or stack != "grouped"):
                     plans[key].set_shape(*[int(v) for v in shape.split(",")])
             pid = id(parts[0])
             if pid not in packed_cache:
@@ -192,6 +196,15 @@ class Stack:
         self.calls = len(self.layers)
         self.launches_per_step = sum(2 if (l[0].rotate and head == "two-call") else 1
                                      for l in self.layers)
+        # a model's matrices in one grouped launch
+        self.group = None
+        if len(self.mats) > 1 and stack == "grouped" and kernel == "mma":
+            m0 = self.mats[0]
+            self.group = lbv.Group(FMT_IDS[m0.fmt], m0.group, lbv.DTYPE_BY_NAME[m0.xdtype],
+                                   [(m.K, m.N) for m in mats], flags)
+            if shape:
+                self.group.set_shape(*[int(v) for v in shape.split(",")])
+            self.launches_per_step = 1
         # greedy head: argmax outputs and the (zeroed) workspace the calls share
         self.idx = torch.zeros(8, dtype=torch.int32, device="cuda")
         self.val = torch.zeros(8, dtype=torch.float32, device="cuda")
@@ -222,6 +235,9 @@ class Stack:
 
     def step(self, M, verify_only=False):
         import few_row_packed_gb300 as lbv
+        if self.group is not None:
+            lbv.verify_grouped(self.group, [(X, M, Wp, Y) for _, _, Wp, X, _, Y in self.layers])
+            return
         for mat, plan, Wp, X, Xr, Y in self.layers:
             if not mat.rotate or verify_only:
                 lbv.verify_gemm(plan, X, M, Wp, Y)
@@ -318,7 +334,9 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
-                  use_graphs=not args.no_graph, head=args.head)
+                  use_graphs=not args.no_graph, head=args.head, stack=args.stack)
+    grouped = stack.group is not None
+    kernel_key = "grouped" if grouped else args.kernel
     rotated = any(l[0].rotate for l in stack.layers)
     greedy = rotated and args.head == "greedy"
     peak, peak_kind = peaks()
@@ -347,10 +365,11 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                                 args.warmup, barrier))
     else:
         ms_v = ms
-    us_launch = ms_v * 1e3 / (args.steps * stack.calls)
-    bytes_launch = bytes_step / stack.calls
+    verify_launches = 1 if grouped else stack.calls
+    us_launch = ms_v * 1e3 / (args.steps * verify_launches)
+    bytes_launch = bytes_step / verify_launches
     achieved = bytes_launch / (us_launch * 1e-6) / 1e9
-    traffic = recorded_traffic(args.workload, args.M, args.kernel)
+    traffic = recorded_traffic(args.workload, args.M, kernel_key)
 
     per_M = {}
     if not args.no_sweep:
@@ -415,10 +434,16 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
-            "shape": {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
-                      "ctas_n": shape[3]},
+            "shape": ({"warps": 16, "tiles_per_warp": stack.group.shape()[0],
+                       "splits": stack.group.shape()[1], "cluster_rows": stack.group.shape()[2]}
+                      if grouped else
+                      {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
+                       "ctas_n": shape[3]}),
             "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
             "head": args.head if rotated else None,
+            "stack": (("grouped: every matrix in one launch" if grouped else
+                       "one verify call per matrix") if len(stack.mats) > 1 else None),
+            "us_per_step": round(ms_per_step * 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "per_M": per_M,
@@ -427,7 +452,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
-                     "kernel": "lbv_tc_kernel" if args.kernel == "tc" else "lbv_verify_kernel",
+                     "kernel": ("lbv_verify_grouped_kernel" if grouped else
+                                "lbv_tc_kernel" if args.kernel == "tc" else "lbv_verify_kernel"),
                      "bytes_per_launch": bytes_launch, "us_per_launch": round(us_launch, 3)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": args.M * mat0.K * 2,

@@ -41,6 +41,12 @@ FMT_BY_NAME = {"sign1_g128": FMT_SIGN1_G128, "affine2": FMT_AFFINE2, "q4_0": FMT
 DTYPE_BY_NAME = {"f16": F16, "bf16": BF16}
 
 
+class Problem(ctypes.Structure):
+    """One problem of a grouped call (lbv_problem)."""
+    _fields_ = [("X", ctypes.c_void_p), ("M", ctypes.c_int), ("ldx", ctypes.c_int),
+                ("Wp", ctypes.c_void_p), ("Y", ctypes.c_void_p), ("ldy", ctypes.c_int)]
+
+
 class LbvError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"lbv status {status}: {msg}")
@@ -82,6 +88,12 @@ def lib():
             "lbv_verify_gemm": (st, [P, P, I, I, P, P, I, P, S, P]),
             "lbv_fwht128": (st, [P, P, I, I, I, P, P]),
             "lbv_fused_workspace_bytes": (S, []),
+            "lbv_group_create": (st, [I, I, I, I, P, P, U, ctypes.POINTER(P)]),
+            "lbv_group_destroy": (st, [P]),
+            "lbv_group_shape": (st, [P] + [ctypes.POINTER(I)] * 3),
+            "lbv_group_set_shape": (st, [P, I, I, I]),
+            "lbv_group_device_status": (st, [P]),
+            "lbv_verify_grouped": (st, [P, P, P]),
             "lbv_fused_rotation": (st, [P, P, I, I, I, P, P]),
             "lbv_verify_fused": (st, [P, P, I, I, P, U, P, P, I, P, P, P, S, P]),
             "lbv_dequant_fp16": (st, [P, P, P, P]),
@@ -241,6 +253,57 @@ class Plan:
         _check(lib().lbv_plan_measured(self.handle, M, ctypes.byref(f), ctypes.byref(g),
                                        ctypes.byref(c)))
         return f.value, g.value, c.value
+
+
+class Group:
+    """A grouped-verify plan: problems of shapes K[i] x N[i], one format."""
+
+    def __init__(self, fmt: int, group: int, xdtype: int, shapes, flags: int = 0):
+        shapes = list(shapes)
+        self.count = len(shapes)
+        self.K = (ctypes.c_int * self.count)(*[int(k) for k, _ in shapes])
+        self.N = (ctypes.c_int * self.count)(*[int(n) for _, n in shapes])
+        h = ctypes.c_void_p()
+        _check(lib().lbv_group_create(fmt, group, xdtype, self.count, self.K, self.N, flags,
+                                      ctypes.byref(h)))
+        self.handle = h
+        self.fmt, self.group, self.xdtype, self.flags = fmt, group, xdtype, flags
+        self.shapes = shapes
+
+    def close(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.lbv_group_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def shape(self):
+        v = [ctypes.c_int() for _ in range(3)]
+        _check(lib().lbv_group_shape(self.handle, *[ctypes.byref(x) for x in v]))
+        return tuple(x.value for x in v)
+
+    def set_shape(self, tpw: int, splits: int, rows: int):
+        _check(lib().lbv_group_set_shape(self.handle, tpw, splits, rows))
+
+    def device_status(self):
+        _check(lib().lbv_group_device_status(self.handle))
+
+
+def verify_grouped(group: Group, problems, stream=None):
+    """problems: one (X, M, Wp, Y) or (X, M, Wp, Y, ldx, ldy) per shape of the
+    group (device tensors; M = 0 skips the problem)."""
+    arr = (Problem * group.count)()
+    for i, pr in enumerate(problems):
+        X, M, Wp, Y = pr[:4]
+        K, N = group.shapes[i]
+        ldx = pr[4] if len(pr) > 4 else K
+        ldy = pr[5] if len(pr) > 5 else N
+        arr[i] = Problem(_ptr(X), int(M), int(ldx), _ptr(Wp), _ptr(Y), int(ldy))
+    _check(lib().lbv_verify_grouped(group.handle, arr, _stream(stream)))
 
 
 # --- device calls ------------------------------------------------------------------

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -964,5 +965,337 @@ extern "C" lbv_status lbv_plan_measured(const lbv_plan* P, int M, float* fewrow_
     if (fewrow_us) *fewrow_us = P->measured_us[M][0];
     if (gemv_us) *gemv_us = P->measured_us[M][1];
     if (crossover) *crossover = P->crossover;
+    return LBV_OK;
+}
+
+// --------------------------------------------------------------------------
+// Grouped verify: independent problems of one format in one launch
+
+namespace {
+
+// Chunks per K slice of a problem under the group's split: whole 128-element
+// blocks where K allows it (as for plans); 0 if the problem would not have
+// exactly `splits` slices.
+int group_problem_cps(const lbv_group* G, int i, int splits)
+{
+    const int step = (G->K[i] % 128 == 0 && G->fi.chunk_k < 128) ? 128 / G->fi.chunk_k : 1;
+    lbv::Shape sh = {16, 2, splits, 0, 0};
+    const int cps = shape_cps(sh, G->nchunks[i], step);
+    return (G->nchunks[i] + cps - 1) / cps == splits ? cps : 0;
+}
+
+// Cluster rows of each problem for about R rows in all: in proportion to its
+// packed bytes, at least 1 and at most its tiles; problems with active[i] == 0
+// get none.  Returns the total.
+int divide_rows(const lbv_group* G, int R, const int* M, int* rows)
+{
+    double B = 0.0;
+    for (int i = 0; i < G->count; ++i)
+        if (!M || M[i] > 0)
+            B += G->bytes[i];
+    int total = 0;
+    for (int i = 0; i < G->count; ++i) {
+        rows[i] = 0;
+        if (M && M[i] == 0)
+            continue;
+        const long r = std::lround((double)R * G->bytes[i] / B);
+        rows[i] = (int)std::max<long>(1, std::min<long>(r, G->ntiles[i]));
+        total += rows[i];
+    }
+    return total;
+}
+
+int group_tiles_max(const lbv_group* G, const int* rows)
+{
+    int t = 1;
+    for (int i = 0; i < G->count; ++i)
+        if (rows[i] > 0)
+            t = std::max(t, (G->ntiles[i] + rows[i] - 1) / rows[i]);
+    return t;
+}
+
+// Launch shape for (tpw, splits) with about R cluster rows; false if the K
+// split does not suit every problem, or shared memory or occupancy rule it out.
+bool group_fit(lbv_group* G, int tpw, int splits, int R, lbv::Shape* out, int* resident,
+               int* tiles_max)
+{
+    const lbv::VerifyOps* ops = ops_for(G->fmt, G->group);
+    int cps_max = 0;
+    for (int i = 0; i < G->count; ++i) {
+        const int c = group_problem_cps(G, i, splits);
+        if (c == 0)
+            return false;
+        cps_max = std::max(cps_max, c);
+    }
+    std::vector<int> rows(G->count);
+    lbv::Shape sh = {16, tpw, splits, 0, 0};
+    sh.ctas_n = divide_rows(G, R, nullptr, rows.data());
+    const int tmax = group_tiles_max(G, rows.data());
+    sh.smem = std::max(ops->smem(16, tpw, cps_max, tmax, splits), kSmemOnePerSm);
+    if (sh.smem > kSmemCap)
+        return false;
+    const int res = ops->max_clusters_grouped(G->xdtype, sh);
+    if (res < 1)
+        return false;
+    *out = sh;
+    *resident = res;
+    *tiles_max = tmax;
+    return true;
+}
+
+// Takes a fitted shape: a call divides its rows from the same R, so no
+// cluster row of a call gets more tiles than tiles_max (fewer active problems
+// only give each one more rows).
+void group_take(lbv_group* G, const lbv::Shape& sh, int R, int res, int tmax)
+{
+    G->shape = sh;
+    G->rows_target = R;
+    G->resident = res;
+    G->tiles_max = tmax;
+    for (int i = 0; i < G->count; ++i)
+        G->cps[i] = group_problem_cps(G, i, sh.splits);
+}
+
+// The smallest R (from R0, growing) whose shape fits for (tpw, splits).
+bool group_fit_rows(lbv_group* G, int tpw, int splits, int R0, lbv::Shape* out, int* resident,
+                    int* tiles_max, int* R_out)
+{
+    int tiles = 0;
+    for (int i = 0; i < G->count; ++i)
+        tiles += G->ntiles[i];
+    for (int R = std::max(1, R0);; R = R + std::max(1, R / 4)) {
+        *R_out = std::min(R, tiles);
+        if (group_fit(G, tpw, splits, *R_out, out, resident, tiles_max))
+            return true;
+        if (R >= tiles)
+            return false;
+    }
+}
+
+// Default shape: two tiles per unit; the K split (1..8) that needs the fewest
+// CTAs in all (each CTA pays the prologue once), with at least two waves of
+// resident clusters for the hardware to balance.
+bool group_default_shape(lbv_group* G)
+{
+    bool found = false;
+    long best_ctas = 0;
+    for (int s = 1; s <= 8; ++s) {
+        lbv::Shape sh;
+        int res = 0, tmax = 0, R = 0;
+        if (!group_fit_rows(G, 2, s, 2 * std::max(1, G->sms / s), &sh, &res, &tmax, &R))
+            continue;
+        if (sh.ctas_n < 2 * res && !group_fit_rows(G, 2, s, 2 * res, &sh, &res, &tmax, &R))
+            continue;
+        const long ctas = (long)sh.ctas_n * s;
+        if (!found || ctas < best_ctas) {
+            found = true;
+            best_ctas = ctas;
+            group_take(G, sh, R, res, tmax);
+        }
+    }
+    return found;
+}
+
+}  // namespace
+
+lbv_status lbv_group_create(lbv_format fmt, int group, lbv_dtype xdtype, int count, const int* K,
+                            const int* N, unsigned flags, lbv_group** out)
+{
+    g_err.clear();
+    if (!out)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: out is NULL");
+    *out = nullptr;
+    if (!valid_fmt(fmt))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: unknown format %d", (int)fmt);
+    if (xdtype != LBV_F16 && xdtype != LBV_BF16)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: unknown dtype %d", (int)xdtype);
+    if (fmt == LBV_FMT_AFFINE2 && group != 32 && group != 64 && group != 128)
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_group_create: affine group %d (supported: 32, 64, 128)",
+                    group);
+    if (fmt != LBV_FMT_AFFINE2)
+        group = fmt == LBV_FMT_SIGN1_G128 ? 128 : 32;
+    if (count < 1 || count > lbv::kMaxGroup || !K || !N)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: count=%d outside 1..%d or no shapes",
+                    count, lbv::kMaxGroup);
+    if (flags & ~LBV_PLAN_PDL)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: flags 0x%x (only LBV_PLAN_PDL)", flags);
+    for (int i = 0; i < count; ++i)
+        if (K[i] <= 0 || N[i] <= 0 || K[i] % k_quantum(fmt, group) != 0)
+            return fail(LBV_ERR_INVALID_ARG,
+                        "lbv_group_create: problem %d: K=%d N=%d not valid for the format", i,
+                        K[i], N[i]);
+    lbv_group* G = new (std::nothrow) lbv_group();
+    if (!G)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: out of host memory");
+    G->fmt = fmt;
+    G->xdtype = xdtype;
+    G->group = group;
+    G->flags = flags;
+    G->count = count;
+    lbv::fmt_info(fmt, group, &G->fi);
+    for (int i = 0; i < count; ++i) {
+        const lbv::Layout L = lbv::make_layout(G->fi, K[i], N[i]);
+        G->K[i] = K[i];
+        G->N[i] = N[i];
+        G->ntiles[i] = (int)L.ntiles;
+        G->nchunks[i] = (int)L.nchunks;
+        G->bytes[i] = (double)L.total;
+    }
+    cudaError_t e = cudaGetDevice(&G->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&G->sms, cudaDevAttrMultiProcessorCount, G->device);
+    if (e == cudaSuccess)
+        e = cudaMalloc((void**)&G->dev_err, 256);
+    if (e == cudaSuccess)
+        e = cudaMemset(G->dev_err, 0, 256);
+    if (e != cudaSuccess) {
+        cudaFree(G->dev_err);
+        delete G;
+        return cuda_fail(e, "lbv_group_create: device set-up");
+    }
+    if (!group_default_shape(G)) {
+        lbv_group_destroy(G);
+        return fail(LBV_ERR_UNSUPPORTED,
+                    "lbv_group_create: no K split of 1..8 suits every problem in shared memory");
+    }
+    *out = G;
+    return LBV_OK;
+}
+
+lbv_status lbv_group_destroy(lbv_group* G)
+{
+    if (G) {
+        cudaFree(G->dev_err);
+        delete G;
+    }
+    return LBV_OK;
+}
+
+lbv_status lbv_group_shape(const lbv_group* G, int* tpw, int* splits, int* rows)
+{
+    g_err.clear();
+    if (!G)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_shape: group is NULL");
+    if (tpw)
+        *tpw = G->shape.tpw;
+    if (splits)
+        *splits = G->shape.splits;
+    if (rows)
+        *rows = G->shape.ctas_n;
+    return LBV_OK;
+}
+
+lbv_status lbv_group_set_shape(lbv_group* G, int tpw, int splits, int rows)
+{
+    g_err.clear();
+    if (!G)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_set_shape: group is NULL");
+    if ((tpw != 1 && tpw != 2) || splits < 1 || splits > 8 || rows < 1)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_set_shape: tpw=%d splits=%d rows=%d", tpw,
+                    splits, rows);
+    lbv::Shape sh;
+    int res = 0, tmax = 0;
+    if (!group_fit(G, tpw, splits, rows, &sh, &res, &tmax))
+        return fail(LBV_ERR_UNSUPPORTED,
+                    "lbv_group_set_shape: the split does not suit every problem, or the shape "
+                    "does not fit (shared memory or occupancy)");
+    group_take(G, sh, rows, res, tmax);
+    return LBV_OK;
+}
+
+lbv_status lbv_group_device_status(const lbv_group* G)
+{
+    g_err.clear();
+    if (!G)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_device_status: group is NULL");
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpy(&v, G->dev_err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_group_device_status");
+    if (v) {
+        cudaMemset(G->dev_err, 0, sizeof v);
+        return fail(LBV_ERR_TIMEOUT, "a grouped verify kernel gave up waiting for its weight copies");
+    }
+    return LBV_OK;
+}
+
+lbv_status lbv_verify_grouped(const lbv_group* G, const lbv_problem* problems, lbv_stream stream)
+{
+    g_err.clear();
+    if (!G || !problems)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: NULL group or problems");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != G->device)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: current device %d is not the group's %d",
+                    dev, G->device);
+    int M[lbv::kMaxGroup];
+    int active = 0;
+    for (int i = 0; i < G->count; ++i) {
+        const lbv_problem& q = problems[i];
+        if (q.M < 0 || q.M > 8)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: problem %d: M=%d outside 0..8", i,
+                        q.M);
+        M[i] = q.M;
+        if (q.M == 0)
+            continue;
+        ++active;
+        if (!q.X || !q.Wp || !q.Y)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: problem %d: null X, Wp or Y", i);
+        if (q.ldx < G->K[i] || q.ldy < G->N[i])
+            return fail(LBV_ERR_INVALID_ARG,
+                        "lbv_verify_grouped: problem %d: ldx=%d < K=%d or ldy=%d < N=%d", i, q.ldx,
+                        G->K[i], q.ldy, G->N[i]);
+        if ((reinterpret_cast<uintptr_t>(q.Wp) & 15u) || (reinterpret_cast<uintptr_t>(q.X) & 1u) ||
+            (reinterpret_cast<uintptr_t>(q.Y) & 3u))
+            return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: problem %d: misaligned pointer", i);
+    }
+    if (active == 0)
+        return LBV_OK;
+    // cluster rows per active problem; the launch order puts the largest
+    // rows first, so the hardware fills the last wave with the small ones
+    static thread_local lbv::GroupedParams gp;
+    int rows[lbv::kMaxGroup];
+    divide_rows(G, G->rows_target, M, rows);
+    if (group_tiles_max(G, rows) > G->tiles_max)        // cannot happen (see group_take)
+        return fail(LBV_ERR_UNSUPPORTED, "lbv_verify_grouped: cluster rows exceed the plan's");
+    int order[lbv::kMaxGroup];
+    int n = 0;
+    for (int i = 0; i < G->count; ++i)
+        if (M[i] > 0)
+            order[n++] = i;
+    std::stable_sort(order, order + n, [&](int a, int b) {
+        return G->bytes[a] / rows[a] > G->bytes[b] / rows[b];
+    });
+    gp.err = G->dev_err;
+    gp.splits = G->shape.splits;
+    gp.count = n;
+    gp.ybegin[0] = 0;
+    for (int j = 0; j < n; ++j) {
+        const int i = order[j];
+        const lbv_problem& q = problems[i];
+        lbv::GroupedProblem& d = gp.prob[j];
+        d.X = q.X;
+        d.W = static_cast<const uint8_t*>(q.Wp);
+        d.Y = q.Y;
+        d.ldx = q.ldx;
+        d.ldy = q.ldy;
+        d.M = q.M;
+        d.K = G->K[i];
+        d.N = G->N[i];
+        d.ntiles = G->ntiles[i];
+        d.nchunks = G->nchunks[i];
+        d.cps = G->cps[i];
+        d.x_vec = ((reinterpret_cast<uintptr_t>(q.X) & 15u) == 0 && (q.ldx % 8) == 0) ? 1 : 0;
+        gp.ybegin[j + 1] = gp.ybegin[j] + rows[i];
+    }
+    lbv::Shape sh = G->shape;
+    sh.ctas_n = gp.ybegin[n];
+    lbv::LaunchOpts o;
+    o.pdl = (G->flags & LBV_PLAN_PDL) != 0;
+    const cudaError_t e = ops_for(G->fmt, G->group)
+                              ->launch_grouped(G->xdtype, sh, gp, o,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_verify_grouped: launch");
     return LBV_OK;
 }

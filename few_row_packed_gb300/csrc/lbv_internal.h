@@ -33,6 +33,30 @@ struct VerifyParams {
     float* amax_val;        // [M] its logit (NULL: not written)
 };
 
+// Grouped verify: one problem of the launch (a compact VerifyParams).
+struct GroupedProblem {
+    const void* X;
+    const uint8_t* W;
+    float* Y;
+    int ldx, ldy;
+    int M, K, N;            // M = 0: skipped
+    int ntiles, nchunks;
+    int cps;                // chunks per K slice (the launch's split)
+    int x_vec;
+};
+
+// Most problems of one grouped launch (the parameters travel in the kernel's
+// parameter space, about 17 KB at this size).
+constexpr int kMaxGroup = 256;
+
+struct GroupedParams {
+    unsigned* err;          // device status word of the group
+    int splits;             // K slices == cluster size, all problems
+    int count;              // problems
+    int ybegin[kMaxGroup + 1];   // cluster rows of problem i: [ybegin[i], ybegin[i + 1])
+    GroupedProblem prob[kMaxGroup];
+};
+
 // Launch shape of the few-row kernel.
 struct Shape {
     int warps;              // 8 or 16
@@ -67,6 +91,26 @@ cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, 
                            int ntiles, int nchunks, uint16_t* W, cudaStream_t st);
 
 }  // namespace lbv
+
+// Plan of a grouped verify: the problems' shapes, the launch shape they share
+// and the problems' packed sizes (for dividing cluster rows).
+struct lbv_group {
+    lbv_format fmt;
+    lbv_dtype xdtype;
+    int group;
+    unsigned flags;
+    int device, sms;
+    int count;
+    lbv::FmtInfo fi;
+    lbv::Shape shape;        // warps, tpw, splits, ctas_n = cluster rows per launch, smem
+    int resident;            // clusters of the shape resident at once
+    int rows_target;         // R the cluster rows are divided from (divide_rows)
+    int tiles_max;           // most tiles of one cluster row (sizes the K-split partials)
+    int K[lbv::kMaxGroup], N[lbv::kMaxGroup];
+    int ntiles[lbv::kMaxGroup], nchunks[lbv::kMaxGroup], cps[lbv::kMaxGroup];
+    double bytes[lbv::kMaxGroup];   // packed bytes of each problem
+    unsigned* dev_err;
+};
 
 struct lbv_plan {
     lbv_format fmt;

@@ -887,15 +887,17 @@ struct VerifyKernel {
         }
     }
 
-    static __device__ void run(const VerifyParams& p, unsigned char* smem)
+    // Cluster row cy of ny (the clusters along N that share the problem's
+    // tiles; blockIdx.x is the K slice).
+    static __device__ void run(const VerifyParams& p, unsigned char* smem, int cy, int ny)
     {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int g = lane >> 2, t = lane & 3;
         const int S = p.splits;
         const int c0 = blockIdx.x * p.cps;
         const int nch = min(p.cps, p.nchunks - c0);          // >= 1 (host guarantees)
-        const int t0 = (int)(((unsigned)p.ntiles * blockIdx.y) / gridDim.y);
-        const int t1 = (int)(((unsigned)p.ntiles * (blockIdx.y + 1)) / gridDim.y);
+        const int t0 = (int)(((unsigned)p.ntiles * cy) / ny);
+        const int t1 = (int)(((unsigned)p.ntiles * (cy + 1)) / ny);
 
         unsigned char* ring = smem;
         unsigned char* bars = ring + G::RING_B;
@@ -1116,7 +1118,56 @@ template <int FMT, int XT, int GROUP, int NW, int TPW>
 __global__ void __launch_bounds__(NW * 32, 1) lbv_verify_kernel(const VerifyParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem);
+    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem, (int)blockIdx.y, (int)gridDim.y);
+}
+
+// Grouped verify: independent problems of one format in one launch.  Cluster
+// row blockIdx.y belongs to the problem i with ybegin[i] <= y < ybegin[i + 1]
+// and is its (y - ybegin[i])-th of (ybegin[i + 1] - ybegin[i]) rows; every
+// problem uses the launch's K split.  Clusters of a problem with M = 0 exit
+// at once.
+template <int FMT, int XT, int GROUP, int NW, int TPW>
+__global__ void __launch_bounds__(NW * 32, 1)
+    lbv_verify_grouped_kernel(const __grid_constant__ GroupedParams gp)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int y = (int)blockIdx.y;
+    int lo = 0, hi = gp.count;                               // ybegin[lo] <= y < ybegin[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (gp.ybegin[mid] <= y)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const GroupedProblem& q = gp.prob[lo];
+    if (q.M == 0)
+        return;
+    VerifyParams p;
+    p.X = q.X;
+    p.W = q.W;
+    p.Y = q.Y;
+    p.err = gp.err;
+    p.ldx = q.ldx;
+    p.ldy = q.ldy;
+    p.M = q.M;
+    p.K = q.K;
+    p.N = q.N;
+    p.ntiles = q.ntiles;
+    p.nchunks = q.nchunks;
+    p.splits = gp.splits;
+    p.cps = q.cps;
+    p.x_vec = q.x_vec;
+    p.zero = 0;
+    p.rot = 0;
+    p.store_y = 1;
+    p.signs = nullptr;
+    p.amax_keys = nullptr;
+    p.amax_done = nullptr;
+    p.amax_idx = nullptr;
+    p.amax_val = nullptr;
+    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem, y - gp.ybegin[lo],
+                                               gp.ybegin[lo + 1] - gp.ybegin[lo]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1129,6 +1180,15 @@ inline void* kernel_ptr(int warps, int tpw)
     if (warps == 8 && tpw == 4) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 8, 4>;
     if (warps == 16 && tpw == 1) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 1>;
     if (warps == 16 && tpw == 2) return (void*)lbv_verify_kernel<FMT, XT, GROUP, 16, 2>;
+    return nullptr;
+}
+
+// Grouped launches use 16 warps with 1 or 2 tiles per unit.
+template <int FMT, int XT, int GROUP>
+inline void* grouped_kernel_ptr(int warps, int tpw)
+{
+    if (warps == 16 && tpw == 1) return (void*)lbv_verify_grouped_kernel<FMT, XT, GROUP, 16, 1>;
+    if (warps == 16 && tpw == 2) return (void*)lbv_verify_grouped_kernel<FMT, XT, GROUP, 16, 2>;
     return nullptr;
 }
 
@@ -1182,9 +1242,24 @@ inline cudaError_t launch_t(const Shape& sh, const VerifyParams& p, const Launch
 }
 
 template <int FMT, int XT, int GROUP>
-inline cudaError_t prepare_t(const Shape& sh)
+inline cudaError_t launch_grouped_t(const Shape& sh, const GroupedParams& gp, const LaunchOpts& o,
+                                    cudaStream_t st)
 {
-    void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    void* k = grouped_kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    if (!k)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_config(cfg, attr, sh, o.pdl, st);
+    void* args[] = {const_cast<GroupedParams*>(&gp)};
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+template <int FMT, int XT, int GROUP>
+inline cudaError_t prepare_t(const Shape& sh, bool grouped = false)
+{
+    void* k = grouped ? grouped_kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw)
+                      : kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
     if (!k)
         return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1193,10 +1268,11 @@ inline cudaError_t prepare_t(const Shape& sh)
 
 // Clusters of the shape that can be resident at once (0 if none fits).
 template <int FMT, int XT, int GROUP>
-inline int max_clusters_t(const Shape& sh)
+inline int max_clusters_t(const Shape& sh, bool grouped = false)
 {
-    void* k = kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
-    if (!k || prepare_t<FMT, XT, GROUP>(sh) != cudaSuccess)
+    void* k = grouped ? grouped_kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw)
+                      : kernel_ptr<FMT, XT, GROUP>(sh.warps, sh.tpw);
+    if (!k || prepare_t<FMT, XT, GROUP>(sh, grouped) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];

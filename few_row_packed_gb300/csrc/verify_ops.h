@@ -12,6 +12,10 @@ struct VerifyOps {
     cudaError_t (*prepare)(lbv_dtype xt, const Shape& sh);
     int (*max_clusters)(lbv_dtype xt, const Shape& sh);
     size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits);
+    // grouped verify (16 warps, 1 or 2 tiles per unit)
+    cudaError_t (*launch_grouped)(lbv_dtype xt, const Shape& sh, const GroupedParams& gp,
+                                  const LaunchOpts& o, cudaStream_t st);
+    int (*max_clusters_grouped)(lbv_dtype xt, const Shape& sh);
 };
 
 extern const VerifyOps sign1_ops;
@@ -46,6 +50,19 @@ extern const VerifyOps q4_0_ops;
     {                                                                                       \
         return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits);                \
     }                                                                                       \
+    static cudaError_t NAME##_launch_grouped(lbv_dtype xt, const Shape& sh,                 \
+                                             const GroupedParams& gp, const LaunchOpts& o,  \
+                                             cudaStream_t st)                               \
+    {                                                                                       \
+        return xt == LBV_F16 ? launch_grouped_t<FMT, LBV_F16, GROUP>(sh, gp, o, st)         \
+                             : launch_grouped_t<FMT, LBV_BF16, GROUP>(sh, gp, o, st);       \
+    }                                                                                       \
+    static int NAME##_max_clusters_grouped(lbv_dtype xt, const Shape& sh)                   \
+    {                                                                                       \
+        return xt == LBV_F16 ? max_clusters_t<FMT, LBV_F16, GROUP>(sh, true)                \
+                             : max_clusters_t<FMT, LBV_BF16, GROUP>(sh, true);              \
+    }                                                                                       \
     const VerifyOps NAME##_ops = {NAME##_launch, NAME##_prepare, NAME##_max_clusters,       \
-                                  NAME##_smem};                                             \
+                                  NAME##_smem, NAME##_launch_grouped,                       \
+                                  NAME##_max_clusters_grouped};                             \
     }

@@ -14,7 +14,8 @@
  *   - Plain C ABI: pointers and sizes only.  "dev" pointers are CUDA device
  *     memory of the current device, "host" pointers are host memory.
  *   - The caller owns every buffer.  The library never allocates in
- *     lbv_verify_gemm, lbv_verify_fused, lbv_fwht128 or lbv_dequant_fp16.  Plans are created and
+ *     lbv_verify_gemm, lbv_verify_fused, lbv_verify_grouped, lbv_fwht128 or
+ *     lbv_dequant_fp16.  Plans are created and
  *     destroyed by the caller and are immutable in between (safe to share
  *     between host threads).
  *   - Device work is asynchronous on the given stream; a status of LBV_OK
@@ -281,6 +282,64 @@ LBV_API lbv_status lbv_verify_fused(const lbv_plan* plan, const void* X, int M, 
                                     const void* Wp, unsigned ops, const uint32_t* signs,
                                     float* Y, int ldy, int32_t* argmax_idx, float* argmax_val,
                                     void* workspace, size_t workspace_bytes, lbv_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped verify: independent problems of one format and dtype in one       */
+/* launch -- a model's matrices (the Q4_0 layer stack) or routed experts,    */
+/* each with its own rows.                                                   */
+
+typedef struct lbv_group lbv_group;     /* opaque, library-owned */
+
+/* One problem of a grouped call (the i-th shape of the group). */
+typedef struct lbv_problem {
+    const void* X;      /* dev [M][ldx], the group's dtype                      */
+    int M;              /* rows, 0..8; 0 skips the problem (nothing is written)  */
+    int ldx;            /* >= K_i                                               */
+    const void* Wp;     /* dev, the default device layout of K_i x N_i
+                           (lbv_pack_*, lbv_packed_bytes), 16-byte aligned      */
+    float* Y;           /* dev [M][ldy] fp32, rows >= M untouched               */
+    int ldy;            /* >= N_i                                               */
+} lbv_problem;
+
+/*
+ * Creates a group plan for `count` (1..256) problems of shapes K[i] x N[i]
+ * (host arrays, each valid for the format as in lbv_plan_create).  All
+ * problems share one launch shape: 16 warps, the K split (cluster size) that
+ * suits every problem and needs the fewest CTAs, and a number of cluster
+ * rows divided among the problems in proportion to their packed bytes (at
+ * least one each, two or more waves of resident clusters for the hardware to
+ * balance).  flags: 0 or LBV_PLAN_PDL.  LBV_ERR_UNSUPPORTED if no K split of
+ * 1..8 fits every problem in shared memory.
+ * Ijah README, "What's new (v0.2)": grouped routed-expert verify, each
+ * expert's weights read once per verify cycle for all the rows routed to it,
+ * bit-identical output.  Ishizuki README, acknowledgements: a megakernel over
+ * a model's matrices needs a grid-wide barrier; these problems are
+ * independent, so one launch needs none.
+ */
+LBV_API lbv_status lbv_group_create(lbv_format fmt, int group, lbv_dtype xdtype, int count,
+                                    const int* K, const int* N, unsigned flags, lbv_group** out);
+LBV_API lbv_status lbv_group_destroy(lbv_group* group);
+
+/* Launch shape: tiles per warp unit (1 or 2), K split, cluster rows of a call
+ * with every problem active.  set_shape: LBV_ERR_UNSUPPORTED if it does not fit. */
+LBV_API lbv_status lbv_group_shape(const lbv_group* group, int* tpw, int* splits, int* rows);
+LBV_API lbv_status lbv_group_set_shape(lbv_group* group, int tpw, int splits, int rows);
+
+/*
+ * Y_i[m][:] = X_i[m][:] . dequant(Wp_i) for every problem i (problems: host
+ * array of `count`, read during the call), in one launch on `stream`.  Row m
+ * of problem i is bit for bit what lbv_verify_gemm gives with a plan of the
+ * same shape and the group's K split (lbv_plan_set_shape(plan, 16, tpw,
+ * splits, 0)).  Problems with M = 0 get no clusters; a call with every M = 0
+ * launches nothing.  Errors: LBV_ERR_INVALID_ARG for M outside 0..8, null or
+ * misaligned pointers of an active problem, ldx < K_i or ldy < N_i.  The
+ * library allocates nothing.
+ */
+LBV_API lbv_status lbv_verify_grouped(const lbv_group* group, const lbv_problem* problems,
+                                      lbv_stream stream);
+
+/* As lbv_plan_device_status, for the group's kernels. */
+LBV_API lbv_status lbv_group_device_status(const lbv_group* group);
 
 /*
  * Test export: X' exactly as lbv_verify_fused with LBV_FUSED_ROTATE computes

@@ -92,6 +92,15 @@ def test_bad_arguments_return_status(L):
                               None, None, 0, None) == lbv.ERR_INVALID_ARG
     assert "lbv_verify_fused" in lbv.last_error()
     assert lbv.fused_workspace_bytes() == 128
+    K = (ctypes.c_int * 2)(128, 128)
+    N = (ctypes.c_int * 2)(16, 16)
+    assert L.lbv_group_create(2, 32, 0, 0, K, N, 0, ctypes.byref(P())) == lbv.ERR_INVALID_ARG
+    assert L.lbv_group_create(2, 32, 0, 2, K, N, 0x2, ctypes.byref(P())) == lbv.ERR_INVALID_ARG
+    K[1] = 100
+    assert L.lbv_group_create(2, 32, 0, 2, K, N, 0, ctypes.byref(P())) == lbv.ERR_INVALID_ARG
+    assert "problem 1" in lbv.last_error()
+    assert L.lbv_verify_grouped(None, None, None) == lbv.ERR_INVALID_ARG
+    assert ctypes.sizeof(lbv.Problem) == 40
     h = P()
     assert L.lbv_plan_create(1, 128, 16, 48, 0, 0, ctypes.byref(h)) == lbv.ERR_UNSUPPORTED
     assert h.value is None

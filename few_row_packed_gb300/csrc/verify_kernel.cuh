@@ -200,6 +200,26 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
     }
 }
 
+// D = A.B + C with C in other registers (starts an accumulator chain from
+// initial values without moving them into D first).
+template <int XT>
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1, float c0,
+                                           float c1)
+{
+    if constexpr (XT == LBV_F16) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};\n"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};\n"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+    }
+}
+
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -537,7 +557,7 @@ struct VerifyKernel {
     using T = Traits<FMT, GROUP>;
     using G = Geometry<FMT, GROUP, NW, TPW>;
     static constexpr int STAGES = G::STAGES;
-    static constexpr int NSET = T::GPC >= 2 ? T::GPC : 2;   // accumulator chains per tile
+    static constexpr int NSET = T::GPC;                     // accumulator chains per tile
 
     // Load cursor of a warp: the record of its next (unit, stage), tracked
     // incrementally by every lane; lane 0 issues.  A stage holds up to CPS
@@ -585,13 +605,19 @@ struct VerifyKernel {
 
     static constexpr int NB = num_bases<FMT>();
 
+    // One k-tile of every tile of the unit into the chain of its group.  The
+    // chains run in the order the k-tile pairs are visited (0, KT/2, 1, ...),
+    // so a group's lowest k-tile comes first and starts its chain from the
+    // group's correction (init) instead of from zero.
     template <int HALF, int KTL>
     static __device__ __forceinline__ void ktile(const uint4 (&w)[TPW], uint32_t b0, uint32_t b1,
                                                  const uint32_t (&bases)[NB],
+                                                 const float2 (&init)[NSET],
                                                  float (&acc)[TPW][NSET][4])
     {
         constexpr int kt = HALF * (T::KT / 2) + KTL;
-        constexpr int set = T::GPC >= 2 ? kt / T::KTG : HALF;
+        constexpr int set = kt / T::KTG;
+        constexpr bool first = kt % T::KTG == 0;
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl) {
             const uint32_t wa = HALF ? w[tl].z : w[tl].x;
@@ -600,7 +626,10 @@ struct VerifyKernel {
             const uint32_t a1 = decode<FMT, XT, 2 * KTL>(wb, bases);
             const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa, bases);
             const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb, bases);
-            mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
+            if constexpr (first)
+                mma16816_c<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1, init[set].x, init[set].y);
+            else
+                mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
         }
     }
 
@@ -610,16 +639,17 @@ struct VerifyKernel {
     static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
                                                  const uint4 (&w)[TPW], uint32_t xa,
                                                  const uint32_t (&bases)[NB],
+                                                 const float2 (&init)[NSET],
                                                  float (&acc)[TPW][NSET][4])
     {
         (
             [&] {
                 const uint4 q0 = ldsm_x4(xa + P * 64);                    // k-tiles 2P, 2P + 1
                 const uint4 q1 = ldsm_x4(xa + (T::KT / 4 + P) * 64);      // the second half's
-                ktile<0, 2 * P>(w, q0.x, q0.y, bases, acc);
-                ktile<1, 2 * P>(w, q1.x, q1.y, bases, acc);
-                ktile<0, 2 * P + 1>(w, q0.z, q0.w, bases, acc);
-                ktile<1, 2 * P + 1>(w, q1.z, q1.w, bases, acc);
+                ktile<0, 2 * P>(w, q0.x, q0.y, bases, init, acc);
+                ktile<1, 2 * P>(w, q1.x, q1.y, bases, init, acc);
+                ktile<0, 2 * P + 1>(w, q0.z, q0.w, bases, init, acc);
+                ktile<1, 2 * P + 1>(w, q1.z, q1.w, bases, init, acc);
             }(),
             ...);
     }
@@ -636,10 +666,7 @@ struct VerifyKernel {
                 constexpr int gi = GI;
 #pragma unroll
                 for (int tl = 0; tl < TPW; ++tl) {
-                    float a[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        a[j] = T::GPC >= 2 ? acc[tl][gi][j] : acc[tl][0][j] + acc[tl][1][j];
+                    const float (&a)[4] = acc[tl][gi];
                     if constexpr (T::AFFINE) {
                         const float2 sc = f16pair(sd[tl][2 * gi]);
                         const float2 bi = f16pair(sd[tl][2 * gi + 1]);
@@ -673,20 +700,12 @@ struct VerifyKernel {
         const float* corr_c = corr + cl * T::GPC * 8;
         const float* rsum_c = rsum + cl * T::GPC * 8;
         float acc[TPW][NSET][4];
+        float2 init[NSET];                  // each group's correction, rows 2t, 2t + 1
 #pragma unroll
-        for (int j = 0; j < NSET; ++j) {
-            float2 I = make_float2(0.f, 0.f);
-            if (T::GPC >= 2 || j == 0)
-                I = *reinterpret_cast<const float2*>(corr_c + (T::GPC >= 2 ? j : 0) * 8 + 2 * t);
-#pragma unroll
-            for (int tl = 0; tl < TPW; ++tl) {
-                acc[tl][j][0] = I.x;
-                acc[tl][j][1] = I.y;
-                acc[tl][j][2] = I.x;
-                acc[tl][j][3] = I.y;
-            }
-        }
-        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xa + cl * T::CHUNK_K * 2, bases, acc);
+        for (int j = 0; j < NSET; ++j)
+            init[j] = *reinterpret_cast<const float2*>(corr_c + j * 8 + 2 * t);
+        pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xa + cl * T::CHUNK_K * 2, bases,
+              init, acc);
         epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
     }
 

@@ -95,6 +95,7 @@ def lib():
             "lbv_group_device_status": (st, [P]),
             "lbv_verify_grouped": (st, [P, P, P]),
             "lbv_fused_rotation": (st, [P, P, I, I, I, P, P]),
+            "lbv_verify_fused_noalloc": (st, [P, P, I, I, P, U, P, P, I, P, P, P]),
             "lbv_verify_fused": (st, [P, P, I, I, P, U, P, P, I, P, P, P, S, P]),
             "lbv_dequant_fp16": (st, [P, P, P, P]),
             "lbv_last_error": (ctypes.c_char_p, []),
@@ -342,6 +343,16 @@ def verify_fused(plan: Plan, X, M: int, Wp, ops: int, Y=None, idx=None, val=None
     _check(lib().lbv_verify_fused(plan.handle, _ptr(X), M, ldx, _ptr(Wp), ops, _ptr(signs),
                                   _ptr(Y), ldy, _ptr(idx), _ptr(val), _ptr(workspace), ws,
                                   _stream(stream)))
+
+
+def verify_fused_noalloc(plan: Plan, X, M: int, Wp, ops: int, Y=None, idx=None, val=None,
+                         signs=None, ldx: int | None = None, ldy: int | None = None, stream=None):
+    """verify_fused with the argmax scratch in the library's own device memory."""
+    ldx = plan.K if ldx is None else ldx
+    ldy = plan.N if ldy is None else ldy
+    _check(lib().lbv_verify_fused_noalloc(plan.handle, _ptr(X), M, ldx, _ptr(Wp), ops,
+                                          _ptr(signs), _ptr(Y), ldy, _ptr(idx), _ptr(val),
+                                          _stream(stream)))
 
 
 def fused_rotation(X, Xr, M: int, K: int, dtype: int = F16, signs=None, stream=None):

@@ -732,6 +732,36 @@ lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, co
     return LBV_OK;
 }
 
+lbv_status lbv_verify_fused_noalloc(const lbv_plan* P, const void* X, int M, int ldx,
+                                    const void* Wp, unsigned ops, const uint32_t* signs, float* Y,
+                                    int ldy, int32_t* argmax_idx, float* argmax_val,
+                                    lbv_stream stream)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_verify_fused_noalloc: plan is NULL");
+    if (M < 1 || M > 8)
+        return fail(LBV_ERR_INVALID_ARG,
+                    "lbv_verify_fused_noalloc: M=%d outside 1..8 (the scratch holds 8 rows)", M);
+    void* scratch = nullptr;
+    if (ops & LBV_FUSED_ARGMAX) {
+        if (lbv::noalloc_scratch_bytes() < kFusedWorkspace)
+            return fail(LBV_ERR_WORKSPACE, "lbv_verify_fused_noalloc: scratch too small");
+        bool first = false;
+        cudaError_t e = lbv::noalloc_scratch(&scratch, &first);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "lbv_verify_fused_noalloc: scratch address");
+        if (first) {            // zero at load already; cleared once more on first use
+            e = cudaMemsetAsync(scratch, 0, lbv::noalloc_scratch_bytes(),
+                                reinterpret_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess)
+                return cuda_fail(e, "lbv_verify_fused_noalloc: clearing the scratch");
+        }
+    }
+    return lbv_verify_fused(P, X, M, ldx, Wp, ops, signs, Y, ldy, argmax_idx, argmax_val,
+                            scratch, scratch ? kFusedWorkspace : 0, stream);
+}
+
 lbv_status lbv_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dtype dtype,
                               const uint32_t* signs, lbv_stream stream)
 {

@@ -1,7 +1,10 @@
-// fused_aux.cu -- test export of the fused head's activation rotation: the
-// prologue device functions of the few-row kernel (sign flip and blockwise
-// FWHT-128 on the tensor cores) run on their own, so their output can be
-// compared element by element.
+// fused_aux.cu -- test export of the fused head's activation rotation (the
+// prologue device functions of the few-row kernel -- sign flip and blockwise
+// FWHT-128 on the tensor cores -- run on their own, so their output can be
+// compared element by element), and the module-owned scratch of
+// lbv_verify_fused_noalloc.
+#include <mutex>
+
 #include "verify_kernel.cuh"
 
 namespace lbv {
@@ -48,6 +51,57 @@ cudaError_t launch_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dty
         lbv_fused_rotation_kernel<LBV_BF16><<<grid, 256, 0, st>>>(
             static_cast<const uint16_t*>(X), static_cast<uint16_t*>(Xr), M, K, signs);
     return cudaGetLastError();
+}
+
+}  // namespace lbv
+
+// ---------------------------------------------------------------------------
+// Scratch of lbv_verify_fused_noalloc: the argmax keys of up to 8 rows and the
+// count of finished CTAs (the layout of lbv_verify_fused's workspace), in the
+// module's own device memory, zero at load and left zero by every call.
+
+namespace {
+
+constexpr size_t kNoAllocScratch = 256;          // bytes; the workspace needs 128
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices];                // symbol address per device, once
+bool g_scratch_cleared[kMaxDevices];
+
+}  // namespace
+
+namespace lbv {
+
+size_t noalloc_scratch_bytes()
+{
+    return kNoAllocScratch;
+}
+
+// The scratch of the current device (its symbol address, looked up once per
+// device).  *first is true on the first request for the device, when the caller
+// clears it on its stream.
+cudaError_t noalloc_scratch(void** out, bool* first)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    *first = !g_scratch_cleared[dev];
+    g_scratch_cleared[dev] = true;
+    return cudaSuccess;
 }
 
 }  // namespace lbv

@@ -283,6 +283,24 @@ LBV_API lbv_status lbv_verify_fused(const lbv_plan* plan, const void* X, int M, 
                                     float* Y, int ldy, int32_t* argmax_idx, float* argmax_val,
                                     void* workspace, size_t workspace_bytes, lbv_stream stream);
 
+/*
+ * lbv_verify_fused without a caller workspace: the argmax scratch (the
+ * 128-byte workspace layout; 256 bytes reserved) is a device array of the
+ * library module itself, one per device, zero at load, cleared once more on
+ * the stream of the first call on each device, and left zero by every call.
+ * The library allocates nothing.  M > 8 is rejected (the scratch holds 8 rows).
+ * Other arguments, rules and errors as lbv_verify_fused.  Races: the scratch is
+ * shared by every call on a device, so calls that could overlap in time (other
+ * streams, other host threads without ordering) must not be made; calls in one
+ * stream are ordered and safe.  The pages have no counterpart of this entry
+ * point: it exists so that a caller need not own device memory for the argmax.
+ */
+LBV_API lbv_status lbv_verify_fused_noalloc(const lbv_plan* plan, const void* X, int M, int ldx,
+                                            const void* Wp, unsigned ops,
+                                            const uint32_t* signs, float* Y, int ldy,
+                                            int32_t* argmax_idx, float* argmax_val,
+                                            lbv_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped verify: independent problems of one format and dtype in one       */
 /* launch -- a model's matrices (the Q4_0 layer stack) or routed experts,    */

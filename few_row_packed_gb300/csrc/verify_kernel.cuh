@@ -969,9 +969,10 @@ struct VerifyKernel {
         cursor_set(p, t0, t1, c0, nch, lcur);
         int lq = 0;
         const int npre = min(STAGES, Q);
-        // two stages before the wait on the previous kernel (they overlap its
-        // tail); the rest after this CTA's activation loads are in flight
-        const int nearly = min(2, npre);
+        // one stage before the wait on the previous kernel (it overlaps that
+        // kernel's tail); the rest after this CTA's activation copies, which
+        // the bulk copy engine serves in issue order
+        const int nearly = min(1, npre);
 #pragma unroll 1
         for (; lq < nearly; ++lq) {
             issue(p, lcur, leader, ring_w, bars_w, lq);

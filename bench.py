@@ -196,15 +196,15 @@ class Stack:
         self.calls = len(self.layers)
         self.launches_per_step = sum(2 if (l[0].rotate and head == "two-call") else 1
                                      for l in self.layers)
-        # a model's matrices in one grouped launch
+        # a model's matrices in grouped launches
         self.group = None
         if len(self.mats) > 1 and stack == "grouped" and kernel == "mma":
             m0 = self.mats[0]
             self.group = lbv.Group(FMT_IDS[m0.fmt], m0.group, lbv.DTYPE_BY_NAME[m0.xdtype],
-                                   [(m.K, m.N) for m in mats], flags)
+                                   [(m.K, m.N) for m in mats], flags | lbv.PLAN_MEASURE)
             if shape:
                 self.group.set_shape(*[int(v) for v in shape.split(",")])
-            self.launches_per_step = 1
+            self.launches_per_step = self.group.launches()
         # greedy head: argmax outputs and the (zeroed) workspace the calls share
         self.idx = torch.zeros(8, dtype=torch.int32, device="cuda")
         self.val = torch.zeros(8, dtype=torch.float32, device="cuda")
@@ -365,7 +365,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                                 args.warmup, barrier))
     else:
         ms_v = ms
-    verify_launches = 1 if grouped else stack.calls
+    verify_launches = stack.group.launches() if grouped else stack.calls
     us_launch = ms_v * 1e3 / (args.steps * verify_launches)
     bytes_launch = bytes_step / verify_launches
     achieved = bytes_launch / (us_launch * 1e-6) / 1e9
@@ -434,15 +434,19 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
-            "shape": ({"warps": 16, "tiles_per_warp": stack.group.shape()[0],
-                       "splits": stack.group.shape()[1], "cluster_rows": stack.group.shape()[2]}
+            "shape": ([{"warps": 16, "tiles_per_warp": t, "splits": sp, "cluster_rows": r,
+                        "matrices": sum(stack.group.problem_launch(i) == c
+                                        for i in range(stack.group.count))}
+                       for c in range(stack.group.launches())
+                       for t, sp, r in [stack.group.shape(c)]]
                       if grouped else
                       {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
                        "ctas_n": shape[3]}),
             "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
             "head": args.head if rotated else None,
-            "stack": (("grouped: every matrix in one launch" if grouped else
-                       "one verify call per matrix") if len(stack.mats) > 1 else None),
+            "stack": ((f"grouped: every matrix in {stack.group.launches()} launch(es), one per "
+                       "K split" if grouped else "one verify call per matrix")
+                      if len(stack.mats) > 1 else None),
             "us_per_step": round(ms_per_step * 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },

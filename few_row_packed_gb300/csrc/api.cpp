@@ -999,13 +999,13 @@ extern "C" lbv_status lbv_plan_measured(const lbv_plan* P, int M, float* fewrow_
 }
 
 // --------------------------------------------------------------------------
-// Grouped verify: independent problems of one format in one launch
+// Grouped verify: independent problems of one format, one launch per class
 
 namespace {
 
-// Chunks per K slice of a problem under the group's split: whole 128-element
-// blocks where K allows it (as for plans); 0 if the problem would not have
-// exactly `splits` slices.
+// Chunks per K slice of a problem under a split: whole 128-element blocks
+// where K allows it (as for plans); 0 if the problem would not have exactly
+// `splits` slices.
 int group_problem_cps(const lbv_group* G, int i, int splits)
 {
     const int step = (G->K[i] % 128 == 0 && G->fi.chunk_k < 128) ? 128 / G->fi.chunk_k : 1;
@@ -1014,19 +1014,20 @@ int group_problem_cps(const lbv_group* G, int i, int splits)
     return (G->nchunks[i] + cps - 1) / cps == splits ? cps : 0;
 }
 
-// Cluster rows of each problem for about R rows in all: in proportion to its
-// packed bytes, at least 1 and at most its tiles; problems with active[i] == 0
-// get none.  Returns the total.
-int divide_rows(const lbv_group* G, int R, const int* M, int* rows)
+// Cluster rows of each problem of class c for about R rows in all: in
+// proportion to its packed bytes, at least 1 and at most its tiles; problems
+// of other classes, and those with M[i] == 0 when M is given, get none.
+// Returns the total.
+int divide_rows(const lbv_group* G, int c, int R, const int* M, int* rows)
 {
     double B = 0.0;
     for (int i = 0; i < G->count; ++i)
-        if (!M || M[i] > 0)
+        if (G->cls[i] == c && (!M || M[i] > 0))
             B += G->bytes[i];
     int total = 0;
     for (int i = 0; i < G->count; ++i) {
         rows[i] = 0;
-        if (M && M[i] == 0)
+        if (G->cls[i] != c || (M && M[i] == 0))
             continue;
         const long r = std::lround((double)R * G->bytes[i] / B);
         rows[i] = (int)std::max<long>(1, std::min<long>(r, G->ntiles[i]));
@@ -1044,86 +1045,267 @@ int group_tiles_max(const lbv_group* G, const int* rows)
     return t;
 }
 
-// Launch shape for (tpw, splits) with about R cluster rows; false if the K
-// split does not suit every problem, or shared memory or occupancy rule it out.
-bool group_fit(lbv_group* G, int tpw, int splits, int R, lbv::Shape* out, int* resident,
-               int* tiles_max)
+// Launch shape of class c for (tpw, splits) with about R cluster rows; false
+// if the split does not suit every problem of the class, or shared memory or
+// occupancy rule it out.
+bool group_fit(lbv_group* G, int c, int tpw, int splits, int R, lbv::GroupLaunch* out)
 {
     const lbv::VerifyOps* ops = ops_for(G->fmt, G->group);
     int cps_max = 0;
     for (int i = 0; i < G->count; ++i) {
-        const int c = group_problem_cps(G, i, splits);
-        if (c == 0)
+        if (G->cls[i] != c)
+            continue;
+        const int cp = group_problem_cps(G, i, splits);
+        if (cp == 0)
             return false;
-        cps_max = std::max(cps_max, c);
+        cps_max = std::max(cps_max, cp);
     }
     std::vector<int> rows(G->count);
-    lbv::Shape sh = {16, tpw, splits, 0, 0};
-    sh.ctas_n = divide_rows(G, R, nullptr, rows.data());
-    const int tmax = group_tiles_max(G, rows.data());
-    sh.smem = std::max(ops->smem(16, tpw, cps_max, tmax, splits), kSmemOnePerSm);
-    if (sh.smem > kSmemCap)
+    lbv::GroupLaunch L;
+    L.shape = {16, tpw, splits, 0, 0};
+    L.shape.ctas_n = divide_rows(G, c, R, nullptr, rows.data());
+    L.tiles_max = group_tiles_max(G, rows.data());
+    L.shape.smem = std::max(ops->smem(16, tpw, cps_max, L.tiles_max, splits), kSmemOnePerSm);
+    if (L.shape.smem > kSmemCap)
         return false;
-    const int res = ops->max_clusters_grouped(G->xdtype, sh);
-    if (res < 1)
+    L.resident = ops->max_clusters_grouped(G->xdtype, L.shape);
+    if (L.resident < 1)
         return false;
-    *out = sh;
-    *resident = res;
-    *tiles_max = tmax;
+    L.rows_target = R;
+    *out = L;
     return true;
 }
 
-// Takes a fitted shape: a call divides its rows from the same R, so no
-// cluster row of a call gets more tiles than tiles_max (fewer active problems
-// only give each one more rows).
-void group_take(lbv_group* G, const lbv::Shape& sh, int R, int res, int tmax)
-{
-    G->shape = sh;
-    G->rows_target = R;
-    G->resident = res;
-    G->tiles_max = tmax;
-    for (int i = 0; i < G->count; ++i)
-        G->cps[i] = group_problem_cps(G, i, sh.splits);
-}
-
-// The smallest R (from R0, growing) whose shape fits for (tpw, splits).
-bool group_fit_rows(lbv_group* G, int tpw, int splits, int R0, lbv::Shape* out, int* resident,
-                    int* tiles_max, int* R_out)
+// The smallest R (from R0, growing) whose shape fits class c for (tpw, splits).
+bool group_fit_rows(lbv_group* G, int c, int tpw, int splits, int R0, lbv::GroupLaunch* out)
 {
     int tiles = 0;
     for (int i = 0; i < G->count; ++i)
-        tiles += G->ntiles[i];
+        if (G->cls[i] == c)
+            tiles += G->ntiles[i];
     for (int R = std::max(1, R0);; R = R + std::max(1, R / 4)) {
-        *R_out = std::min(R, tiles);
-        if (group_fit(G, tpw, splits, *R_out, out, resident, tiles_max))
+        if (group_fit(G, c, tpw, splits, std::min(R, tiles), out))
             return true;
         if (R >= tiles)
             return false;
     }
 }
 
-// Default shape: two tiles per unit; the K split (1..8) that needs the fewest
-// CTAs in all (each CTA pays the prologue once), with at least two waves of
-// resident clusters for the hardware to balance.
-bool group_default_shape(lbv_group* G)
+// Default shape of class c: two tiles per unit; the K split from s0 up that
+// needs the fewest CTAs in all (each CTA pays the prologue once), with at
+// least two waves of resident clusters (measured on the Q4_0 stack: better
+// than one wave per split class or more waves of one split).
+bool group_fit_class(lbv_group* G, int c, int s0, lbv::GroupLaunch* out)
 {
     bool found = false;
     long best_ctas = 0;
-    for (int s = 1; s <= 8; ++s) {
-        lbv::Shape sh;
-        int res = 0, tmax = 0, R = 0;
-        if (!group_fit_rows(G, 2, s, 2 * std::max(1, G->sms / s), &sh, &res, &tmax, &R))
+    for (int sp = s0; sp <= 8; ++sp) {
+        lbv::GroupLaunch L;
+        if (!group_fit_rows(G, c, 2, sp, 2 * std::max(1, G->sms / sp), &L))
             continue;
-        if (sh.ctas_n < 2 * res && !group_fit_rows(G, 2, s, 2 * res, &sh, &res, &tmax, &R))
+        if (L.shape.ctas_n < 2 * L.resident &&
+            !group_fit_rows(G, c, 2, sp, 2 * L.resident, &L))
             continue;
-        const long ctas = (long)sh.ctas_n * s;
+        const long ctas = (long)L.shape.ctas_n * sp;
         if (!found || ctas < best_ctas) {
             found = true;
             best_ctas = ctas;
-            group_take(G, sh, R, res, tmax);
+            *out = L;
         }
     }
     return found;
+}
+
+// Launch classes: one for all problems when a K split suits every one of
+// them (problems of different lengths then share the GPU within one launch,
+// which hides the long-K ones' slower streaming); otherwise each problem goes
+// to the smallest split (1..8) at which its X slice fits in shared memory
+// next to the ring, one class per split.
+bool group_default_launches(lbv_group* G)
+{
+    const lbv::VerifyOps* ops = ops_for(G->fmt, G->group);
+    std::fill(G->cls, G->cls + G->count, 0);
+    G->nlaunch = 1;
+    if (group_fit_class(G, 0, 1, &G->launch[0])) {
+        for (int i = 0; i < G->count; ++i)
+            G->cps[i] = group_problem_cps(G, i, G->launch[0].shape.splits);
+        return true;
+    }
+    int smin[lbv::kMaxGroup];
+    for (int i = 0; i < G->count; ++i) {
+        smin[i] = 0;
+        for (int s = 1; s <= 8 && !smin[i]; ++s) {
+            const int cp = group_problem_cps(G, i, s);
+            if (cp && std::max(ops->smem(16, 2, cp, 1, s), kSmemOnePerSm) <= kSmemCap)
+                smin[i] = s;
+        }
+        if (!smin[i])
+            return false;
+    }
+    G->nlaunch = 0;
+    std::fill(G->cls, G->cls + G->count, -1);         // no class yet
+    for (int s = 1; s <= 8; ++s) {
+        bool any = false;
+        for (int i = 0; i < G->count; ++i)
+            any |= smin[i] == s;
+        if (!any)
+            continue;
+        const int c = G->nlaunch++;
+        for (int i = 0; i < G->count; ++i)
+            if (smin[i] == s)
+                G->cls[i] = c;
+        if (!group_fit_class(G, c, s, &G->launch[c]))
+            return false;
+    }
+    for (int i = 0; i < G->count; ++i)
+        G->cps[i] = group_problem_cps(G, i, G->launch[G->cls[i]].shape.splits);
+    return true;
+}
+
+}  // namespace
+
+namespace {
+
+// One launch of class c over its problems with M[i] > 0 (none active: nothing).
+lbv_status launch_class(const lbv_group* G, int c, const lbv_problem* problems, const int* M,
+                        cudaStream_t stream)
+{
+    static thread_local lbv::GroupedParams gp;
+    const lbv::GroupLaunch& L = G->launch[c];
+    // cluster rows per active problem of the class, divided from the plan's R
+    // so that no row gets more tiles than the partials were sized for; the
+    // largest rows go first, the hardware fills the wave's end with the small
+    // ones
+    int rows[lbv::kMaxGroup];
+    divide_rows(G, c, L.rows_target, M, rows);
+    if (group_tiles_max(G, rows) > L.tiles_max)        // cannot happen (fewer active
+        return fail(LBV_ERR_UNSUPPORTED,               // problems only add rows)
+                    "lbv_verify_grouped: cluster rows exceed the plan's");
+    int order[lbv::kMaxGroup];
+    int n = 0;
+    for (int i = 0; i < G->count; ++i)
+        if (rows[i] > 0)
+            order[n++] = i;
+    if (n == 0)
+        return LBV_OK;
+    std::stable_sort(order, order + n, [&](int a, int b) {
+        return G->bytes[a] / rows[a] > G->bytes[b] / rows[b];
+    });
+    gp.err = G->dev_err;
+    gp.splits = L.shape.splits;
+    gp.count = n;
+    gp.ybegin[0] = 0;
+    for (int j = 0; j < n; ++j) {
+        const int i = order[j];
+        const lbv_problem& q = problems[i];
+        lbv::GroupedProblem& d = gp.prob[j];
+        d.X = q.X;
+        d.W = static_cast<const uint8_t*>(q.Wp);
+        d.Y = q.Y;
+        d.ldx = q.ldx;
+        d.ldy = q.ldy;
+        d.M = q.M;
+        d.K = G->K[i];
+        d.N = G->N[i];
+        d.ntiles = G->ntiles[i];
+        d.nchunks = G->nchunks[i];
+        d.cps = G->cps[i];
+        d.x_vec = ((reinterpret_cast<uintptr_t>(q.X) & 15u) == 0 && (q.ldx % 8) == 0) ? 1 : 0;
+        gp.ybegin[j + 1] = gp.ybegin[j] + rows[i];
+    }
+    lbv::Shape sh = L.shape;
+    sh.ctas_n = gp.ybegin[n];
+    lbv::LaunchOpts o;
+    o.pdl = (G->flags & LBV_PLAN_PDL) != 0;
+    const cudaError_t e = ops_for(G->fmt, G->group)->launch_grouped(G->xdtype, sh, gp, o, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lbv_verify_grouped: launch");
+    return LBV_OK;
+}
+
+// LBV_PLAN_MEASURE: for every class, time the default shape and one to four
+// waves of each K split from the class's own up to 8 (cold L2, scratch
+// weights and activations of the class's shapes, M = 8); keep the fastest.
+lbv_status group_measure(lbv_group* G)
+{
+    std::vector<size_t> woff(G->count), xoff(G->count), yoff(G->count);
+    size_t wb = 0, xb = 0, yb = 0;
+    for (int i = 0; i < G->count; ++i) {
+        woff[i] = wb;
+        wb += ((size_t)G->bytes[i] + 255) / 256 * 256;
+        xoff[i] = xb;
+        xb += ((size_t)8 * G->K[i] * 2 + 255) / 256 * 256;
+        yoff[i] = yb;
+        yb += ((size_t)8 * G->N[i] * 4 + 255) / 256 * 256;
+    }
+    Scratch s;
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, G->device);
+    s.flush_bytes = (size_t)std::max(l2, 1 << 20) * 2;
+    cudaError_t e = cudaMalloc(&s.w, wb);
+    if (e == cudaSuccess) e = cudaMalloc(&s.x, xb);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&s.y, yb);
+    if (e == cudaSuccess) e = cudaMalloc(&s.flush, s.flush_bytes);
+    if (e == cudaSuccess) e = cudaMemset(s.w, 0x5A, wb);
+    if (e == cudaSuccess) e = cudaMemset(s.x, 0x11, xb);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "group measure: scratch");
+    std::vector<lbv_problem> probs(G->count);
+    int M[lbv::kMaxGroup];
+    for (int i = 0; i < G->count; ++i) {
+        probs[i].X = static_cast<unsigned char*>(s.x) + xoff[i];
+        probs[i].M = 8;
+        probs[i].ldx = G->K[i];
+        probs[i].Wp = static_cast<unsigned char*>(s.w) + woff[i];
+        probs[i].Y = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s.y) + yoff[i]);
+        probs[i].ldy = G->N[i];
+        M[i] = 8;
+    }
+    cudaStream_t st = nullptr;
+    for (int c = 0; c < G->nlaunch; ++c) {
+        const int s0 = G->launch[c].shape.splits;
+        int tiles = 0;
+        for (int i = 0; i < G->count; ++i)
+            if (G->cls[i] == c)
+                tiles += G->ntiles[i];
+        const lbv::GroupLaunch dflt = G->launch[c];
+        lbv::GroupLaunch best = dflt;
+        float best_us = 1e30f;
+        for (int sp = s0; sp <= 8; ++sp) {
+            lbv::GroupLaunch probe;
+            int res = std::max(1, G->sms / sp);
+            if (group_fit(G, c, 2, sp, std::min(res, tiles), &probe))
+                res = probe.resident;
+            for (int waves = 0; waves <= 4; ++waves) {   // 0: the default shape
+                lbv::GroupLaunch L;
+                if (waves == 0) {
+                    if (sp != dflt.shape.splits)
+                        continue;
+                    L = dflt;
+                } else if (!group_fit(G, c, 2, sp, std::min(res * waves, tiles), &L)) {
+                    continue;
+                }
+                G->launch[c] = L;
+                for (int i = 0; i < G->count; ++i)
+                    if (G->cls[i] == c)
+                        G->cps[i] = group_problem_cps(G, i, sp);
+                float us = 0.f;
+                const lbv_status rc =
+                    time_cold([&] { return launch_class(G, c, probs.data(), M, st); }, s, st, 5, &us);
+                if (rc != LBV_OK)
+                    return rc;
+                if (us < best_us) {
+                    best_us = us;
+                    best = L;
+                }
+            }
+        }
+        G->launch[c] = best;
+        for (int i = 0; i < G->count; ++i)
+            if (G->cls[i] == c)
+                G->cps[i] = group_problem_cps(G, i, best.shape.splits);
+    }
+    return LBV_OK;
 }
 
 }  // namespace
@@ -1147,8 +1329,9 @@ lbv_status lbv_group_create(lbv_format fmt, int group, lbv_dtype xdtype, int cou
     if (count < 1 || count > lbv::kMaxGroup || !K || !N)
         return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: count=%d outside 1..%d or no shapes",
                     count, lbv::kMaxGroup);
-    if (flags & ~LBV_PLAN_PDL)
-        return fail(LBV_ERR_INVALID_ARG, "lbv_group_create: flags 0x%x (only LBV_PLAN_PDL)", flags);
+    if (flags & ~(LBV_PLAN_PDL | LBV_PLAN_MEASURE))
+        return fail(LBV_ERR_INVALID_ARG,
+                    "lbv_group_create: flags 0x%x (only LBV_PLAN_PDL, LBV_PLAN_MEASURE)", flags);
     for (int i = 0; i < count; ++i)
         if (K[i] <= 0 || N[i] <= 0 || K[i] % k_quantum(fmt, group) != 0)
             return fail(LBV_ERR_INVALID_ARG,
@@ -1183,10 +1366,17 @@ lbv_status lbv_group_create(lbv_format fmt, int group, lbv_dtype xdtype, int cou
         delete G;
         return cuda_fail(e, "lbv_group_create: device set-up");
     }
-    if (!group_default_shape(G)) {
+    if (!group_default_launches(G)) {
         lbv_group_destroy(G);
         return fail(LBV_ERR_UNSUPPORTED,
-                    "lbv_group_create: no K split of 1..8 suits every problem in shared memory");
+                    "lbv_group_create: a problem fits no K split of 1..8 in shared memory");
+    }
+    if (flags & LBV_PLAN_MEASURE) {
+        const lbv_status st = group_measure(G);
+        if (st != LBV_OK) {
+            lbv_group_destroy(G);
+            return st;
+        }
     }
     *out = G;
     return LBV_OK;
@@ -1201,17 +1391,30 @@ lbv_status lbv_group_destroy(lbv_group* G)
     return LBV_OK;
 }
 
-lbv_status lbv_group_shape(const lbv_group* G, int* tpw, int* splits, int* rows)
+int lbv_group_launches(const lbv_group* G)
+{
+    return G ? G->nlaunch : 0;
+}
+
+int lbv_group_problem_launch(const lbv_group* G, int problem)
+{
+    return (G && problem >= 0 && problem < G->count) ? G->cls[problem] : -1;
+}
+
+lbv_status lbv_group_shape(const lbv_group* G, int launch, int* tpw, int* splits, int* rows)
 {
     g_err.clear();
     if (!G)
         return fail(LBV_ERR_INVALID_ARG, "lbv_group_shape: group is NULL");
+    if (launch < 0 || launch >= G->nlaunch)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_shape: launch %d of %d", launch, G->nlaunch);
+    const lbv::Shape& sh = G->launch[launch].shape;
     if (tpw)
-        *tpw = G->shape.tpw;
+        *tpw = sh.tpw;
     if (splits)
-        *splits = G->shape.splits;
+        *splits = sh.splits;
     if (rows)
-        *rows = G->shape.ctas_n;
+        *rows = sh.ctas_n;
     return LBV_OK;
 }
 
@@ -1223,13 +1426,20 @@ lbv_status lbv_group_set_shape(lbv_group* G, int tpw, int splits, int rows)
     if ((tpw != 1 && tpw != 2) || splits < 1 || splits > 8 || rows < 1)
         return fail(LBV_ERR_INVALID_ARG, "lbv_group_set_shape: tpw=%d splits=%d rows=%d", tpw,
                     splits, rows);
-    lbv::Shape sh;
-    int res = 0, tmax = 0;
-    if (!group_fit(G, tpw, splits, rows, &sh, &res, &tmax))
+    int cls_saved[lbv::kMaxGroup];
+    std::copy(G->cls, G->cls + G->count, cls_saved);
+    std::fill(G->cls, G->cls + G->count, 0);
+    lbv::GroupLaunch L;
+    if (!group_fit(G, 0, tpw, splits, rows, &L)) {
+        std::copy(cls_saved, cls_saved + G->count, G->cls);
         return fail(LBV_ERR_UNSUPPORTED,
                     "lbv_group_set_shape: the split does not suit every problem, or the shape "
                     "does not fit (shared memory or occupancy)");
-    group_take(G, sh, rows, res, tmax);
+    }
+    G->nlaunch = 1;
+    G->launch[0] = L;
+    for (int i = 0; i < G->count; ++i)
+        G->cps[i] = group_problem_cps(G, i, splits);
     return LBV_OK;
 }
 
@@ -1259,7 +1469,6 @@ lbv_status lbv_verify_grouped(const lbv_group* G, const lbv_problem* problems, l
         return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: current device %d is not the group's %d",
                     dev, G->device);
     int M[lbv::kMaxGroup];
-    int active = 0;
     for (int i = 0; i < G->count; ++i) {
         const lbv_problem& q = problems[i];
         if (q.M < 0 || q.M > 8)
@@ -1268,7 +1477,6 @@ lbv_status lbv_verify_grouped(const lbv_group* G, const lbv_problem* problems, l
         M[i] = q.M;
         if (q.M == 0)
             continue;
-        ++active;
         if (!q.X || !q.Wp || !q.Y)
             return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: problem %d: null X, Wp or Y", i);
         if (q.ldx < G->K[i] || q.ldy < G->N[i])
@@ -1279,53 +1487,10 @@ lbv_status lbv_verify_grouped(const lbv_group* G, const lbv_problem* problems, l
             (reinterpret_cast<uintptr_t>(q.Y) & 3u))
             return fail(LBV_ERR_INVALID_ARG, "lbv_verify_grouped: problem %d: misaligned pointer", i);
     }
-    if (active == 0)
-        return LBV_OK;
-    // cluster rows per active problem; the launch order puts the largest
-    // rows first, so the hardware fills the last wave with the small ones
-    static thread_local lbv::GroupedParams gp;
-    int rows[lbv::kMaxGroup];
-    divide_rows(G, G->rows_target, M, rows);
-    if (group_tiles_max(G, rows) > G->tiles_max)        // cannot happen (see group_take)
-        return fail(LBV_ERR_UNSUPPORTED, "lbv_verify_grouped: cluster rows exceed the plan's");
-    int order[lbv::kMaxGroup];
-    int n = 0;
-    for (int i = 0; i < G->count; ++i)
-        if (M[i] > 0)
-            order[n++] = i;
-    std::stable_sort(order, order + n, [&](int a, int b) {
-        return G->bytes[a] / rows[a] > G->bytes[b] / rows[b];
-    });
-    gp.err = G->dev_err;
-    gp.splits = G->shape.splits;
-    gp.count = n;
-    gp.ybegin[0] = 0;
-    for (int j = 0; j < n; ++j) {
-        const int i = order[j];
-        const lbv_problem& q = problems[i];
-        lbv::GroupedProblem& d = gp.prob[j];
-        d.X = q.X;
-        d.W = static_cast<const uint8_t*>(q.Wp);
-        d.Y = q.Y;
-        d.ldx = q.ldx;
-        d.ldy = q.ldy;
-        d.M = q.M;
-        d.K = G->K[i];
-        d.N = G->N[i];
-        d.ntiles = G->ntiles[i];
-        d.nchunks = G->nchunks[i];
-        d.cps = G->cps[i];
-        d.x_vec = ((reinterpret_cast<uintptr_t>(q.X) & 15u) == 0 && (q.ldx % 8) == 0) ? 1 : 0;
-        gp.ybegin[j + 1] = gp.ybegin[j] + rows[i];
+    for (int c = 0; c < G->nlaunch; ++c) {
+        const lbv_status st = launch_class(G, c, problems, M, reinterpret_cast<cudaStream_t>(stream));
+        if (st != LBV_OK)
+            return st;
     }
-    lbv::Shape sh = G->shape;
-    sh.ctas_n = gp.ybegin[n];
-    lbv::LaunchOpts o;
-    o.pdl = (G->flags & LBV_PLAN_PDL) != 0;
-    const cudaError_t e = ops_for(G->fmt, G->group)
-                              ->launch_grouped(G->xdtype, sh, gp, o,
-                                               reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return cuda_fail(e, "lbv_verify_grouped: launch");
     return LBV_OK;
 }

@@ -98,8 +98,19 @@ cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, 
 
 }  // namespace lbv
 
-// Plan of a grouped verify: the problems' shapes, the launch shape they share
-// and the problems' packed sizes (for dividing cluster rows).
+// Plan of a grouped verify: the problems' shapes and their launches.  Each
+// problem belongs to one launch class; a class's problems share a launch
+// shape (warps, tiles per unit, K split, cluster rows) and run in one launch.
+namespace lbv {
+constexpr int kMaxGroupLaunches = 8;
+struct GroupLaunch {
+    Shape shape;             // warps, tpw, splits, ctas_n = cluster rows with all active, smem
+    int resident;            // clusters of the shape resident at once
+    int rows_target;         // R the class's cluster rows are divided from (divide_rows)
+    int tiles_max;           // most tiles of one cluster row (sizes the K-split partials)
+};
+}  // namespace lbv
+
 struct lbv_group {
     lbv_format fmt;
     lbv_dtype xdtype;
@@ -108,13 +119,12 @@ struct lbv_group {
     int device, sms;
     int count;
     lbv::FmtInfo fi;
-    lbv::Shape shape;        // warps, tpw, splits, ctas_n = cluster rows per launch, smem
-    int resident;            // clusters of the shape resident at once
-    int rows_target;         // R the cluster rows are divided from (divide_rows)
-    int tiles_max;           // most tiles of one cluster row (sizes the K-split partials)
+    int nlaunch;                               // launch classes
+    lbv::GroupLaunch launch[lbv::kMaxGroupLaunches];
+    int cls[lbv::kMaxGroup];                   // launch class of each problem
     int K[lbv::kMaxGroup], N[lbv::kMaxGroup];
     int ntiles[lbv::kMaxGroup], nchunks[lbv::kMaxGroup], cps[lbv::kMaxGroup];
-    double bytes[lbv::kMaxGroup];   // packed bytes of each problem
+    double bytes[lbv::kMaxGroup];              // packed bytes of each problem
     unsigned* dev_err;
 };
 

@@ -321,35 +321,49 @@ typedef struct lbv_problem {
 
 /*
  * Creates a group plan for `count` (1..256) problems of shapes K[i] x N[i]
- * (host arrays, each valid for the format as in lbv_plan_create).  All
- * problems share one launch shape: 16 warps, the K split (cluster size) that
- * suits every problem and needs the fewest CTAs, and a number of cluster
- * rows divided among the problems in proportion to their packed bytes (at
- * least one each, two or more waves of resident clusters for the hardware to
- * balance).  flags: 0 or LBV_PLAN_PDL.  LBV_ERR_UNSUPPORTED if no K split of
- * 1..8 fits every problem in shared memory.
+ * (host arrays, each valid for the format as in lbv_plan_create).  The
+ * problems of a launch class share one launch shape: 16 warps, two tiles per
+ * unit, a K split (cluster size) that suits each of them, and cluster rows
+ * (at least two waves of resident clusters) divided among them in proportion
+ * to their packed bytes.  There is one class when some split of 1..8 suits
+ * every problem (the split needing the fewest CTAs); otherwise each problem
+ * joins the class of the smallest split at which its X slice fits in shared
+ * memory.  flags: LBV_PLAN_PDL and/or LBV_PLAN_MEASURE, which times, per
+ * class, the default shape and one to four waves of every split from the
+ * class's own up to 8 on scratch buffers (allocated and freed here, cold L2,
+ * M = 8) and keeps the fastest.  LBV_ERR_UNSUPPORTED if a problem fits no
+ * split of 1..8.
  * Ijah README, "What's new (v0.2)": grouped routed-expert verify, each
  * expert's weights read once per verify cycle for all the rows routed to it,
  * bit-identical output.  Ishizuki README, acknowledgements: a megakernel over
  * a model's matrices needs a grid-wide barrier; these problems are
- * independent, so one launch needs none.
+ * independent, so their launches need none.
  */
 LBV_API lbv_status lbv_group_create(lbv_format fmt, int group, lbv_dtype xdtype, int count,
                                     const int* K, const int* N, unsigned flags, lbv_group** out);
 LBV_API lbv_status lbv_group_destroy(lbv_group* group);
 
-/* Launch shape: tiles per warp unit (1 or 2), K split, cluster rows of a call
- * with every problem active.  set_shape: LBV_ERR_UNSUPPORTED if it does not fit. */
-LBV_API lbv_status lbv_group_shape(const lbv_group* group, int* tpw, int* splits, int* rows);
+/* Launch classes of the plan (0 for NULL), and the class of a problem (-1 if
+ * out of range). */
+LBV_API int lbv_group_launches(const lbv_group* group);
+LBV_API int lbv_group_problem_launch(const lbv_group* group, int problem);
+
+/* Launch shape of class `launch`: tiles per warp unit (1 or 2), K split,
+ * cluster rows with every problem of the class active.  set_shape puts every
+ * problem in one class with the given shape; LBV_ERR_UNSUPPORTED if the split
+ * does not suit every problem or the shape does not fit. */
+LBV_API lbv_status lbv_group_shape(const lbv_group* group, int launch, int* tpw, int* splits,
+                                   int* rows);
 LBV_API lbv_status lbv_group_set_shape(lbv_group* group, int tpw, int splits, int rows);
 
 /*
  * Y_i[m][:] = X_i[m][:] . dequant(Wp_i) for every problem i (problems: host
- * array of `count`, read during the call), in one launch on `stream`.  Row m
- * of problem i is bit for bit what lbv_verify_gemm gives with a plan of the
- * same shape and the group's K split (lbv_plan_set_shape(plan, 16, tpw,
- * splits, 0)).  Problems with M = 0 get no clusters; a call with every M = 0
- * launches nothing.  Errors: LBV_ERR_INVALID_ARG for M outside 0..8, null or
+ * array of `count`, read during the call), one launch per class with an
+ * active problem, in order on `stream`.  Row m of problem i is bit for bit
+ * what lbv_verify_gemm gives with a plan of the same shape and the K split of
+ * the problem's class (lbv_plan_set_shape(plan, 16, tpw, splits, 0)).
+ * Problems with M = 0 get no clusters; a call with every M = 0 launches
+ * nothing.  Errors: LBV_ERR_INVALID_ARG for M outside 0..8, null or
  * misaligned pointers of an active problem, ldx < K_i or ldy < N_i.  The
  * library allocates nothing.
  */

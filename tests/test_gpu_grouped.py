@@ -62,9 +62,9 @@ class Problems:
         return [Y.cpu().numpy() for Y in Ys]
 
     def single(self, i, M):
-        """lbv_verify_gemm of problem i with the group's tiles per unit and K split."""
+        """lbv_verify_gemm of problem i with its launch class's tiles per unit and K split."""
         K, N = self.shapes[i]
-        tpw, splits, _ = self.G.shape()
+        tpw, splits, _ = self.G.shape(self.G.problem_launch(i))
         plan = lbv.Plan(self.fmt, K, N, self.group, DT[self.xdtype])
         plan.set_shape(16, tpw, splits, 0)
         Y = torch.full((8, N), float(SENT), dtype=torch.float32, device="cuda")
@@ -93,6 +93,38 @@ LAYER = [(640, 96), (640, 32), (640, 32), (768, 80), (1280, 48), (1280, 40), (20
 def test_q4_0_layer_like_group():
     P = Problems(synth.Q4_0, 32, "f16", LAYER, seed=1)
     for Ms in ([8] * 7, [1] * 7, [3, 8, 0, 5, 1, 8, 2]):
+        P.check(P.run(Ms), Ms)
+
+
+def test_two_launch_classes():
+    """Problems whose X slice needs a K split next to one too short to be
+    split (K = 128 is two Q4_0 chunks, one 128-element block): no split suits
+    all, so two launch classes in one call, each problem equal to its single
+    call."""
+    shapes = [(17408, 64), (128, 96), (2048, 48), (17408, 32)]
+    P = Problems(synth.Q4_0, 32, "f16", shapes, seed=8)
+    assert P.G.launches() == 2
+    assert P.G.problem_launch(0) == P.G.problem_launch(3) != P.G.problem_launch(1)
+    assert P.G.shape(P.G.problem_launch(1))[1] == 1 and P.G.shape(P.G.problem_launch(0))[1] > 1
+    with pytest.raises(lbv.LbvError):
+        P.G.shape(2)
+    for Ms in ([8, 8, 8, 8], [0, 3, 0, 1], [2, 0, 8, 0]):
+        P.check(P.run(Ms), Ms)
+
+
+def test_measured_shapes():
+    """LBV_PLAN_MEASURE picks each class's split and rows by timing; results
+    still equal single calls with the chosen split."""
+    shapes = [(17408, 64), (128, 96), (2048, 48), (6144, 80)]
+    P = Problems(synth.Q4_0, 32, "f16", shapes, seed=9, flags=lbv.PLAN_MEASURE | lbv.PLAN_PDL)
+    assert P.G.launches() == 2
+    Q = Problems(synth.Q4_0, 32, "f16", LAYER, seed=10, flags=lbv.PLAN_MEASURE)
+    assert Q.G.launches() == 1
+    Q.check(Q.run([8, 1, 0, 3, 8, 2, 5]), [8, 1, 0, 3, 8, 2, 5])
+    for c in range(P.G.launches()):
+        tpw, sp, rows = P.G.shape(c)
+        assert tpw == 2 and 1 <= sp <= 8 and rows >= 1
+    for Ms in ([8, 8, 8, 8], [1, 0, 5, 2]):
         P.check(P.run(Ms), Ms)
 
 
@@ -131,6 +163,7 @@ def test_shapes_agree_bitwise():
     result; only the K split does, and every split stays within tolerance."""
     P = Problems(synth.Q4_0, 32, "bf16", LAYER, seed=6)
     Ms = [8, 2, 5, 8, 1, 8, 3]
+    assert P.G.launches() == 1
     tpw0, s0, r0 = P.G.shape()
     base = P.run(Ms)
     P.check(base, Ms)

@@ -1014,26 +1014,65 @@ int group_problem_cps(const lbv_group* G, int i, int splits)
     return (G->nchunks[i] + cps - 1) / cps == splits ? cps : 0;
 }
 
-// Cluster rows of each problem of class c for about R rows in all: in
-// proportion to its packed bytes, at least 1 and at most its tiles; problems
-// of other classes, and those with M[i] == 0 when M is given, get none.
-// Returns the total.
+// Cluster rows of each problem of class c, R in all where the bounds allow:
+// in proportion to its packed bytes by largest remainders, at least 1 and at
+// most its tiles; problems of other classes, and those with M[i] == 0 when M
+// is given, get none.  Returns the total.
 int divide_rows(const lbv_group* G, int c, int R, const int* M, int* rows)
 {
     double B = 0.0;
+    int n = 0;
     for (int i = 0; i < G->count; ++i)
-        if (G->cls[i] == c && (!M || M[i] > 0))
+        if (G->cls[i] == c && (!M || M[i] > 0)) {
             B += G->bytes[i];
+            ++n;
+        }
+    double quota[lbv::kMaxGroup];
     int total = 0;
     for (int i = 0; i < G->count; ++i) {
         rows[i] = 0;
         if (G->cls[i] != c || (M && M[i] == 0))
             continue;
-        const long r = std::lround((double)R * G->bytes[i] / B);
-        rows[i] = (int)std::max<long>(1, std::min<long>(r, G->ntiles[i]));
+        quota[i] = (double)R * G->bytes[i] / B;
+        rows[i] = std::max(1, std::min((int)quota[i], G->ntiles[i]));
         total += rows[i];
     }
+    // one row at a time to the largest remainder (or away from the most
+    // over-served) until the total is R or no problem can take or give one
+    for (int step = 0; step < 4 * lbv::kMaxGroup && total != R && n > 0; ++step) {
+        int pick = -1;
+        double best = 0.0;
+        for (int i = 0; i < G->count; ++i) {
+            if (rows[i] == 0)
+                continue;
+            const double rem = quota[i] - rows[i];
+            if (total < R && rows[i] < G->ntiles[i] && (pick < 0 || rem > best)) {
+                pick = i;
+                best = rem;
+            }
+            if (total > R && rows[i] > 1 && (pick < 0 || rem < best)) {
+                pick = i;
+                best = rem;
+            }
+        }
+        if (pick < 0)
+            break;
+        const int d = total < R ? 1 : -1;
+        rows[pick] += d;
+        total += d;
+    }
     return total;
+}
+
+// Records the rows of class c with every problem active (a call never gives
+// an active problem fewer, so no row gets more tiles than the partials hold).
+void group_commit_rows(lbv_group* G, int c)
+{
+    int rows[lbv::kMaxGroup];
+    divide_rows(G, c, G->launch[c].rows_target, nullptr, rows);
+    for (int i = 0; i < G->count; ++i)
+        if (G->cls[i] == c)
+            G->rows_plan[i] = rows[i];
 }
 
 int group_tiles_max(const lbv_group* G, const int* rows)
@@ -1076,35 +1115,40 @@ bool group_fit(lbv_group* G, int c, int tpw, int splits, int R, lbv::GroupLaunch
     return true;
 }
 
-// The smallest R (from R0, growing) whose shape fits class c for (tpw, splits).
-bool group_fit_rows(lbv_group* G, int c, int tpw, int splits, int R0, lbv::GroupLaunch* out)
+// Whole waves of resident clusters, the fewest from `waves0` up whose shape
+// fits class c for (tpw, splits) (a partial last wave would leave SMs idle
+// for a whole row's time).
+bool group_fit_rows(lbv_group* G, int c, int tpw, int splits, int waves0, lbv::GroupLaunch* out)
 {
     int tiles = 0;
     for (int i = 0; i < G->count; ++i)
         if (G->cls[i] == c)
             tiles += G->ntiles[i];
-    for (int R = std::max(1, R0);; R = R + std::max(1, R / 4)) {
-        if (group_fit(G, c, tpw, splits, std::min(R, tiles), out))
+    lbv::GroupLaunch probe;
+    int res = std::max(1, G->sms / splits);
+    if (group_fit(G, c, tpw, splits, std::min(res, tiles), &probe))
+        res = probe.resident;
+    for (int waves = waves0; waves <= 32; ++waves) {
+        const int R = std::min(res * waves, tiles);
+        if (group_fit(G, c, tpw, splits, R, out))
             return true;
-        if (R >= tiles)
+        if (R == tiles)
             return false;
     }
+    return false;
 }
 
 // Default shape of class c: two tiles per unit; the K split from s0 up that
-// needs the fewest CTAs in all (each CTA pays the prologue once), with at
-// least two waves of resident clusters (measured on the Q4_0 stack: better
-// than one wave per split class or more waves of one split).
+// needs the fewest CTAs in all (each CTA pays the prologue once), in whole
+// waves of resident clusters, at least two (measured on the Q4_0 stack:
+// better than one wave per split class).
 bool group_fit_class(lbv_group* G, int c, int s0, lbv::GroupLaunch* out)
 {
     bool found = false;
     long best_ctas = 0;
     for (int sp = s0; sp <= 8; ++sp) {
         lbv::GroupLaunch L;
-        if (!group_fit_rows(G, c, 2, sp, 2 * std::max(1, G->sms / sp), &L))
-            continue;
-        if (L.shape.ctas_n < 2 * L.resident &&
-            !group_fit_rows(G, c, 2, sp, 2 * L.resident, &L))
+        if (!group_fit_rows(G, c, 2, sp, 2, &L))
             continue;
         const long ctas = (long)L.shape.ctas_n * sp;
         if (!found || ctas < best_ctas) {
@@ -1129,6 +1173,7 @@ bool group_default_launches(lbv_group* G)
     if (group_fit_class(G, 0, 1, &G->launch[0])) {
         for (int i = 0; i < G->count; ++i)
             G->cps[i] = group_problem_cps(G, i, G->launch[0].shape.splits);
+        group_commit_rows(G, 0);
         return true;
     }
     int smin[lbv::kMaxGroup];
@@ -1159,6 +1204,8 @@ bool group_default_launches(lbv_group* G)
     }
     for (int i = 0; i < G->count; ++i)
         G->cps[i] = group_problem_cps(G, i, G->launch[G->cls[i]].shape.splits);
+    for (int c = 0; c < G->nlaunch; ++c)
+        group_commit_rows(G, c);
     return true;
 }
 
@@ -1173,11 +1220,14 @@ lbv_status launch_class(const lbv_group* G, int c, const lbv_problem* problems, 
     static thread_local lbv::GroupedParams gp;
     const lbv::GroupLaunch& L = G->launch[c];
     // cluster rows per active problem of the class, divided from the plan's R
-    // so that no row gets more tiles than the partials were sized for; the
-    // largest rows go first, the hardware fills the wave's end with the small
-    // ones
+    // and never fewer than the plan's, so that no row gets more tiles than
+    // the partials were sized for; the largest rows go first, the hardware
+    // fills the wave's end with the small ones
     int rows[lbv::kMaxGroup];
     divide_rows(G, c, L.rows_target, M, rows);
+    for (int i = 0; i < G->count; ++i)
+        if (rows[i] > 0)
+            rows[i] = std::max(rows[i], G->rows_plan[i]);
     if (group_tiles_max(G, rows) > L.tiles_max)        // cannot happen (fewer active
         return fail(LBV_ERR_UNSUPPORTED,               // problems only add rows)
                     "lbv_verify_grouped: cluster rows exceed the plan's");
@@ -1289,6 +1339,7 @@ lbv_status group_measure(lbv_group* G)
                 for (int i = 0; i < G->count; ++i)
                     if (G->cls[i] == c)
                         G->cps[i] = group_problem_cps(G, i, sp);
+                group_commit_rows(G, c);
                 float us = 0.f;
                 const lbv_status rc =
                     time_cold([&] { return launch_class(G, c, probs.data(), M, st); }, s, st, 5, &us);
@@ -1304,6 +1355,7 @@ lbv_status group_measure(lbv_group* G)
         for (int i = 0; i < G->count; ++i)
             if (G->cls[i] == c)
                 G->cps[i] = group_problem_cps(G, i, best.shape.splits);
+        group_commit_rows(G, c);
     }
     return LBV_OK;
 }
@@ -1440,6 +1492,7 @@ lbv_status lbv_group_set_shape(lbv_group* G, int tpw, int splits, int rows)
     G->launch[0] = L;
     for (int i = 0; i < G->count; ++i)
         G->cps[i] = group_problem_cps(G, i, splits);
+    group_commit_rows(G, 0);
     return LBV_OK;
 }
 

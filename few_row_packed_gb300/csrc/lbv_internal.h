@@ -122,6 +122,7 @@ struct lbv_group {
     int nlaunch;                               // launch classes
     lbv::GroupLaunch launch[lbv::kMaxGroupLaunches];
     int cls[lbv::kMaxGroup];                   // launch class of each problem
+    int rows_plan[lbv::kMaxGroup];             // its cluster rows with every problem active
     int K[lbv::kMaxGroup], N[lbv::kMaxGroup];
     int ntiles[lbv::kMaxGroup], nchunks[lbv::kMaxGroup], cps[lbv::kMaxGroup];
     double bytes[lbv::kMaxGroup];              // packed bytes of each problem

@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M=1..8 table")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-measure", action="store_true",
+                    help="plans without LBV_PLAN_MEASURE (default launch shapes)")
     ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override of the launch shape")
     ap.add_argument("--kernel", default="mma", choices=["mma", "tc"],
                     help="few-row kernel: mma.sync (default plans) or tcgen05 (PLAN_TCGEN05)")
@@ -150,7 +152,7 @@ class Stack:
 
     def __init__(self, workload, pdl: bool, shape: str, l2_bytes: int, M: int,
                  use_graphs: bool = True, kernel: str = "mma", head: str = "fused",
-                 stack: str = "grouped"):
+                 stack: str = "grouped", measure: bool = True):
         import torch
         self.use_graphs = use_graphs
         self.graphs = {}
@@ -160,6 +162,9 @@ class Stack:
         wl = synth.WORKLOADS[workload]
         self.mats = list(wl.matrices)
         flags = (lbv.PLAN_PDL if pdl else 0) | (lbv.PLAN_TCGEN05 if kernel == "tc" else 0)
+        # plans are set up once per weight shape, timing their candidate launch
+        # shapes and the 1-row crossover (LBV_PLAN_MEASURE)
+        mflag = lbv.PLAN_MEASURE if measure else 0
         self.layers = []
         if len(self.mats) == 1:
             mat = self.mats[0]
@@ -178,7 +183,8 @@ class Stack:
             key = (mat.fmt, mat.K, mat.N, mat.group, mat.xdtype)
             if key not in plans:
                 plans[key] = lbv.Plan(FMT_IDS[mat.fmt], mat.K, mat.N, mat.group,
-                                      lbv.DTYPE_BY_NAME[mat.xdtype], flags)
+                                      lbv.DTYPE_BY_NAME[mat.xdtype],
+                                      flags | (mflag if not shape else 0))
                 if shape and (len(self.mats) == 1 or stack != "grouped"):
                     plans[key].set_shape(*[int(v) for v in shape.split(",")])
             pid = id(parts[0])
@@ -201,7 +207,7 @@ class Stack:
         if len(self.mats) > 1 and stack == "grouped" and kernel == "mma":
             m0 = self.mats[0]
             self.group = lbv.Group(FMT_IDS[m0.fmt], m0.group, lbv.DTYPE_BY_NAME[m0.xdtype],
-                                   [(m.K, m.N) for m in mats], flags | lbv.PLAN_MEASURE)
+                                   [(m.K, m.N) for m in mats], flags | mflag)
             if shape:
                 self.group.set_shape(*[int(v) for v in shape.split(",")])
             self.launches_per_step = self.group.launches()
@@ -334,7 +340,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
-                  use_graphs=not args.no_graph, head=args.head, stack=args.stack)
+                  use_graphs=not args.no_graph, head=args.head, stack=args.stack,
+                  measure=not args.no_measure)
     grouped = stack.group is not None
     kernel_key = "grouped" if grouped else args.kernel
     rotated = any(l[0].rotate for l in stack.layers)
@@ -431,6 +438,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
             "us_per_call": round(ms_per_step * 1e3 / stack.calls, 3),
             "l2": f"inputs larger than L2: {stack.calls} distinct resident matrices, "
                   f"{bytes_step / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
+            "plans": "launch shapes measured at plan creation (LBV_PLAN_MEASURE)"
+                     if not (args.no_measure or args.shape) else "default launch shapes",
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",

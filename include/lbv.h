@@ -72,10 +72,13 @@ typedef enum {
 typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
 
 /* Plan flags. */
-#define LBV_PLAN_MEASURE     0x1u  /* time the candidate launch shapes and the
-                                      1-row path at plan creation and keep the
-                                      fastest per row count (allocates and
-                                      synchronises inside lbv_plan_create) */
+#define LBV_PLAN_MEASURE     0x1u  /* time the candidate launch shapes (as
+                                      back-to-back launches over copies of
+                                      scratch weights, >= 2x L2, after an L2
+                                      flush) and the 1-row path at plan
+                                      creation and keep the fastest per row
+                                      count (allocates and synchronises
+                                      inside lbv_plan_create) */
 #define LBV_PLAN_FORCE_FEWROW 0x2u /* always use the few-row kernel           */
 #define LBV_PLAN_FORCE_GEMV   0x4u /* always use the 1-row path (run per row) */
 #define LBV_PLAN_PDL          0x8u /* launch with programmatic dependent launch:

@@ -207,7 +207,7 @@ class Stack:
         if len(self.mats) > 1 and stack == "grouped" and kernel == "mma":
             m0 = self.mats[0]
             self.group = lbv.Group(FMT_IDS[m0.fmt], m0.group, lbv.DTYPE_BY_NAME[m0.xdtype],
-                                   [(m.K, m.N) for m in mats], flags | mflag)
+                                   [(m.K, m.N) for m in mats], flags | (mflag if not shape else 0))
             if shape:
                 self.group.set_shape(*[int(v) for v in shape.split(",")])
             self.launches_per_step = self.group.launches()
@@ -274,9 +274,14 @@ def timed(torch, fn, steps, warmup, barrier):
 
 
 def kernel_hash():
+    """Hash of the device code (kernels and the headers they include); the
+    host-side planning in the .cpp files does not change what a captured
+    launch executes."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "few_row_packed_gb300", "csrc")
     for f in sorted(os.listdir(d)):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -332,7 +332,7 @@ typedef struct lbv_problem {
  * every problem (the split needing the fewest CTAs); otherwise each problem
  * joins the class of the smallest split at which its X slice fits in shared
  * memory.  flags: LBV_PLAN_PDL and/or LBV_PLAN_MEASURE, which times, per
- * class, the default shape and one to four waves of every split from the
+ * class, the default shape and one to six waves of every split from the
  * class's own up to 8 on scratch buffers (allocated and freed here, cold L2,
  * M = 8) and keeps the fastest.  LBV_ERR_UNSUPPORTED if a problem fits no
  * split of 1..8.

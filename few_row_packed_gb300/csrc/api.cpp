@@ -883,21 +883,43 @@ lbv_status time_cold(F&& launch, Scratch& s, cudaStream_t st, int reps, float* u
 }
 
 // Median time (us) per launch of `reps` chains, each after an L2 flush: every
-// chain runs launch(c) for c = 0 .. n-1 twice, back to back on the stream
-// (the steady state of a caller that verifies through many matrices).
+// chain runs launch(c, stream) for c = 0 .. n-1 twice, back to back, captured
+// once in a CUDA graph (the steady state of a caller that verifies through
+// many matrices; launched one by one from the host, ~10 us kernels would be
+// timed at the host's launch rate).  Without graph capture: direct launches.
 template <class F>
-lbv_status time_chain(F&& launch, int n, Scratch& s, cudaStream_t st, int reps, float* us)
+lbv_status time_chain(F&& launch, int n, Scratch& s, int reps, float* us)
 {
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess)
+        return fail(LBV_ERR_CUDA, "plan measure: stream");
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    lbv_status rc = LBV_OK;
+    if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        for (int k = 0; k < 2 * n && rc == LBV_OK; ++k)
+            rc = launch(k % n, st);
+        const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+        if (rc == LBV_OK && ec == cudaSuccess &&
+            cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+            exec = nullptr;
+    }
+    cudaGetLastError();                           // a failed capture leaves no error behind
     cudaEvent_t a, b;
     cudaEventCreate(&a);
     cudaEventCreate(&b);
     std::vector<float> v;
-    lbv_status rc = LBV_OK;
+    rc = LBV_OK;
     for (int i = 0; i < reps + 1 && rc == LBV_OK; ++i) {
         cudaMemsetAsync(s.flush, i & 0xFF, s.flush_bytes, st);
         cudaEventRecord(a, st);
-        for (int k = 0; k < 2 * n && rc == LBV_OK; ++k)
-            rc = launch(k % n);
+        if (exec) {
+            if (cudaGraphLaunch(exec, st) != cudaSuccess)
+                rc = fail(LBV_ERR_CUDA, "plan measure: graph launch");
+        } else {
+            for (int k = 0; k < 2 * n && rc == LBV_OK; ++k)
+                rc = launch(k % n, st);
+        }
         cudaEventRecord(b, st);
         if (cudaEventSynchronize(b) != cudaSuccess) {
             rc = fail(LBV_ERR_CUDA, "plan measure: %s", cudaGetErrorString(cudaGetLastError()));
@@ -910,6 +932,11 @@ lbv_status time_chain(F&& launch, int n, Scratch& s, cudaStream_t st, int reps, 
     }
     cudaEventDestroy(a);
     cudaEventDestroy(b);
+    if (exec)
+        cudaGraphExecDestroy(exec);
+    if (graph)
+        cudaGraphDestroy(graph);
+    cudaStreamDestroy(st);
     if (rc != LBV_OK)
         return rc;
     std::sort(v.begin(), v.end());
@@ -994,12 +1021,12 @@ lbv_status lbv_plan_measure_internal(lbv_plan* P)
                 P->shape = sh;
                 float us = 0.f;
                 lbv_status rc = time_chain(
-                    [&](int c) {
+                    [&](int c, cudaStream_t cs) {
                         return lbv_verify_launch_internal(
                             P, s.x, 8, P->K, static_cast<unsigned char*>(copies) + (size_t)c * wbytes,
-                            s.y, P->N, false, st);
+                            s.y, P->N, false, cs);
                     },
-                    ncopy, s, st, 5, &us);
+                    ncopy, s, 5, &us);
                 if (rc != LBV_OK) {
                     cudaFree(copies);
                     return rc;

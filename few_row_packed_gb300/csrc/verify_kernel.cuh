@@ -579,17 +579,23 @@ struct VerifyKernel {
         c.nc = min(G::CPS, nch - ch);
     }
 
+    // Next stage: within a unit the record pointer just moves on by a
+    // stage's chunks; only a new unit recomputes it.
     static __device__ __forceinline__ void cursor_next(const VerifyParams& p, int t0, int t1,
                                                        int c0, int nch, int nstage, Cursor& c)
     {
         if (++c.stage == nstage) {
             c.stage = 0;
             c.unit += NW;
+            cursor_set(p, t0, t1, c0, nch, c);
+        } else {
+            c.rec += G::CPS * G::REC;
+            c.nc = min(G::CPS, nch - c.stage * G::CPS);
         }
-        cursor_set(p, t0, t1, c0, nch, c);
     }
 
-    static __device__ __forceinline__ void issue(const VerifyParams& p, const Cursor& c,
+    // tstride: bytes between the records of consecutive tiles (nchunks * REC)
+    static __device__ __forceinline__ void issue(const Cursor& c, size_t tstride,
                                                  uint32_t leader, uint32_t ring_w,
                                                  uint32_t bars_w, int slot)
     {
@@ -600,7 +606,7 @@ struct VerifyKernel {
 #pragma unroll
         for (int tl = 0; tl < TPW; ++tl)
             bulk_g2s_if(leader && tl < c.nvalid, dst + tl * G::CPS * G::REC,
-                        c.rec + (size_t)tl * p.nchunks * G::REC, bytes, bar);
+                        c.rec + tl * tstride, bytes, bar);
     }
 
     static constexpr int NB = num_bases<FMT>();
@@ -967,6 +973,7 @@ struct VerifyKernel {
         lcur.unit = warp;
         lcur.stage = 0;
         cursor_set(p, t0, t1, c0, nch, lcur);
+        const size_t tstride = (size_t)p.nchunks * G::REC;
         int lq = 0;
         const int npre = min(STAGES, Q);
         // one stage before the wait on the previous kernel (it overlaps that
@@ -975,7 +982,7 @@ struct VerifyKernel {
         const int nearly = min(1, npre);
 #pragma unroll 1
         for (; lq < nearly; ++lq) {
-            issue(p, lcur, leader, ring_w, bars_w, lq);
+            issue(lcur, tstride, leader, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
 
@@ -983,7 +990,7 @@ struct VerifyKernel {
         const bool x_async = stage_x(p, xs, RS, xbar, c0, nch);
 #pragma unroll 1
         for (; lq < npre; ++lq) {
-            issue(p, lcur, leader, ring_w, bars_w, lq);
+            issue(lcur, tstride, leader, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
         __syncthreads();               // X barrier initialised, tails zeroed (or X copied)
@@ -1046,7 +1053,7 @@ struct VerifyKernel {
             __syncwarp();
             if (lq < Q) {
                 fence_proxy_async_if(leader);
-                issue(p, lcur, leader, ring_w, bars_w, slot);
+                issue(lcur, tstride, leader, ring_w, bars_w, slot);
                 ++lq;
                 cursor_next(p, t0, t1, c0, nch, nstage, lcur);
             }

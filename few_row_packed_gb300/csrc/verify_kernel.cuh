@@ -514,6 +514,8 @@ struct Geometry {
     using T = Traits<FMT, GROUP>;
     static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (record, g)
     static constexpr int REC = 512 + 8 * SIDE_B;              // record bytes (tile, chunk)
+    static_assert(REC % 16 == 0 && (SIDE_B == 8 || SIDE_B % 16 == 0),
+                  "records and side words stay aligned for 8/16-byte shared loads");
     static constexpr int CPS = 2;                             // chunks per ring stage
     static constexpr int SLOT_B = TPW * CPS * REC;            // one ring stage
     static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
@@ -1045,10 +1047,24 @@ struct VerifyKernel {
                 for (int tl = 0; tl < TPW; ++tl) {
                     const unsigned char* r = src + (tl * G::CPS + ci) * G::REC;
                     w[ci][tl] = reinterpret_cast<const uint4*>(r)[lane];
-                    const uint32_t* sp = reinterpret_cast<const uint32_t*>(r + 512 + g * G::SIDE_B);
+                    // side words of column pair g: 8, 16 or 32 bytes, as wide loads
+                    // (records are 16-byte aligned, so is r + 512 + g * SIDE_B)
+                    const unsigned char* sp = r + 512 + g * G::SIDE_B;
+                    if constexpr (T::SIDE_W == 2) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(sp);
+                        sd[ci][tl][0] = v.x;
+                        sd[ci][tl][1] = v.y;
+                    } else {
+                        static_assert(T::SIDE_W % 4 == 0, "side words in 16-byte pieces");
 #pragma unroll
-                    for (int i = 0; i < T::SIDE_W; ++i)
-                        sd[ci][tl][i] = sp[i];
+                        for (int i = 0; i < T::SIDE_W / 4; ++i) {
+                            const uint4 v = reinterpret_cast<const uint4*>(sp)[i];
+                            sd[ci][tl][4 * i] = v.x;
+                            sd[ci][tl][4 * i + 1] = v.y;
+                            sd[ci][tl][4 * i + 2] = v.z;
+                            sd[ci][tl][4 * i + 3] = v.w;
+                        }
+                    }
                 }
             __syncwarp();
             if (lq < Q) {

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) lbv_fused_rotation_kernel(const uint16_t*
         flip_signs(signs, xs, RS, M, kb, have, threadIdx.x, 256);
         __syncthreads();
     }
-    rotate_x<XT>(smem_u32(xs), xs, RS, have / 128, threadIdx.x >> 5, 8, threadIdx.x & 31);
+    rotate_x<XT>(smem_u32(xs), RS, have / 128, threadIdx.x >> 5, 8, threadIdx.x & 31);
     __syncthreads();
     for (int i = threadIdx.x; i < M * have; i += 256) {
         const int m = i / have, k = i - m * have;

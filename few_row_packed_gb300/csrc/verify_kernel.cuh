@@ -369,14 +369,29 @@ __device__ __forceinline__ float2 f16pair(uint32_t v)
     return __half22float2(h);
 }
 
-// One fp32 value rounded to nearest even in the X dtype (bit pattern).
+// Two fp32 values rounded to nearest even in the X dtype, packed (lo in the
+// low half).
 template <int XT>
-__device__ __forceinline__ uint16_t round_x(float v)
+__device__ __forceinline__ uint32_t round_x2(float lo, float hi)
 {
-    if constexpr (XT == LBV_F16)
-        return __half_as_ushort(__float2half_rn(v));
-    else
-        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    if constexpr (XT == LBV_F16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// Four 8x8 b16 matrices to shared memory, transposed: thread (g, t) gives row
+// g, columns 2t and 2t + 1 of matrix i in register i; lanes 8i..8i+7 give the
+// addresses of the 8 stored rows of matrix i (its columns).
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                              uint32_t r3)
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};\n"
+                 ::"r"(addr), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
 }
 
 // Two entries (i, j), (i, j + 1) of the 16-point Sylvester Hadamard matrix,
@@ -463,8 +478,8 @@ __device__ __forceinline__ void flip_signs(const uint32_t* signs, unsigned char*
 // to the X dtype.  A warp reads its whole block before writing it back.  All 8
 // rows are rotated; a row's results depend on that row alone.
 template <int XT>
-__device__ __forceinline__ void rotate_x(uint32_t xs_a, unsigned char* xs, int RS, int nblk,
-                                         int warp, int nwarps, int lane)
+__device__ __forceinline__ void rotate_x(uint32_t xs_a, int RS, int nblk, int warp, int nwarps,
+                                         int lane)
 {
     const int g = lane >> 2, t = lane & 3;
     const uint32_t h0 = h16_pair<XT>(g, 2 * t), h1 = h16_pair<XT>(g + 8, 2 * t);
@@ -494,15 +509,21 @@ __device__ __forceinline__ void rotate_x(uint32_t xs_a, unsigned char* xs, int R
                         u[J][e] = a + c;
                         u[J + h][e] = a - c;
                     }
-        // u[I][e] is element 16 I + g + 8 (e >> 1) of row 2 t + (e & 1)
+        // u[I][e] is element 16 I + g + 8 (e >> 1) of row 2 t + (e & 1): per I
+        // two 8x8 matrices (elements 16 I + 0..7 and + 8..15 by rows), whose
+        // transposes are the rows' elements, written with stmatrix .trans.
+        // Lane 8j + r gives row r's address in matrix j of each store.
+        const int mj = lane >> 3, mr = lane & 7;
 #pragma unroll
-        for (int I = 0; I < 8; ++I)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = 2 * t + (e & 1), i = 16 * I + g + 8 * (e >> 1);
-                *reinterpret_cast<uint16_t*>(xs + (size_t)m * RS + (b * 128 + i) * 2) =
-                    round_x<XT>(u[I][e] * kInvSqrt128);
-            }
+        for (int k = 0; k < 4; ++k) {                    // tiles I = 2k, 2k + 1
+            const int I = 2 * k + (mj >> 1), half = mj & 1;
+            const uint32_t addr = xs_a + (uint32_t)(mr * RS + (b * 128 + 16 * I + 8 * half) * 2);
+            stsm_x4_trans(addr,
+                          round_x2<XT>(u[2 * k][0] * kInvSqrt128, u[2 * k][1] * kInvSqrt128),
+                          round_x2<XT>(u[2 * k][2] * kInvSqrt128, u[2 * k][3] * kInvSqrt128),
+                          round_x2<XT>(u[2 * k + 1][0] * kInvSqrt128, u[2 * k + 1][1] * kInvSqrt128),
+                          round_x2<XT>(u[2 * k + 1][2] * kInvSqrt128, u[2 * k + 1][3] * kInvSqrt128));
+        }
     }
 }
 
@@ -1008,7 +1029,7 @@ struct VerifyKernel {
                     flip_signs(p.signs, xs, RS, p.M, kb, have, threadIdx.x, NW * 32);
                     __syncthreads();
                 }
-                rotate_x<XT>(xs_a, xs, RS, have / 128, warp, NW, lane);
+                rotate_x<XT>(xs_a, RS, have / 128, warp, NW, lane);
             }
             __syncthreads();
         }

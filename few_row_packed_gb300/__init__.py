@@ -90,7 +90,9 @@ def lib():
             "lbv_fused_workspace_bytes": (S, []),
             "lbv_group_create": (st, [I, I, I, I, P, P, U, ctypes.POINTER(P)]),
             "lbv_group_destroy": (st, [P]),
-            "lbv_group_shape": (st, [P] + [ctypes.POINTER(I)] * 3),
+            "lbv_group_shape": (st, [P, I] + [ctypes.POINTER(I)] * 3),
+            "lbv_group_launches": (I, [P]),
+            "lbv_group_problem_launch": (I, [P, I]),
             "lbv_group_set_shape": (st, [P, I, I, I]),
             "lbv_group_device_status": (st, [P]),
             "lbv_verify_grouped": (st, [P, P, P]),
@@ -282,9 +284,16 @@ class Group:
         except Exception:
             pass
 
-    def shape(self):
+    def launches(self) -> int:
+        return int(lib().lbv_group_launches(self.handle))
+
+    def problem_launch(self, i: int) -> int:
+        return int(lib().lbv_group_problem_launch(self.handle, i))
+
+    def shape(self, launch: int = 0):
+        """(tiles per unit, K split, cluster rows) of launch class `launch`."""
         v = [ctypes.c_int() for _ in range(3)]
-        _check(lib().lbv_group_shape(self.handle, *[ctypes.byref(x) for x in v]))
+        _check(lib().lbv_group_shape(self.handle, launch, *[ctypes.byref(x) for x in v]))
         return tuple(x.value for x in v)
 
     def set_shape(self, tpw: int, splits: int, rows: int):

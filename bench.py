@@ -62,6 +62,8 @@ def parse_args():
                     help="multi-matrix workloads: every matrix in one grouped launch "
                          "(default) or one verify call per matrix")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense fp16 cuBLAS context timing")
     ap.add_argument("--no-graph", action="store_true", help="launch each call from Python")
     ap.add_argument("--quick", action="store_true", help="no sustained clock window (profiling)")
     ap.add_argument("--json-out", default="")
@@ -273,6 +275,61 @@ def timed(torch, fn, steps, warmup, barrier):
     return e0.elapsed_time(e1)
 
 
+def dense_context(stack, M, l2_bytes, steps, warmup, peak, barrier, reduce_max):
+    """Context, not the product: the step's matrices as a dense fp16 GEMM in
+    cuBLAS (torch.matmul, fp16 x fp16 -> fp16) on the weights expanded once
+    by lbv_dequant_fp16, with enough dense copies that a step's weights
+    exceed 4x L2, captured in a CUDA graph like the packed step."""
+    import torch
+
+    import few_row_packed_gb300 as lbv
+    dense_b = [l[0].K * l[0].N * 2 for l in stack.layers]
+    if len(stack.mats) == 1:
+        n = min(len(stack.layers), max(2, math.ceil(4 * l2_bytes / dense_b[0])))
+    else:
+        n = len(stack.layers)
+    calls = []
+    for mat, plan, Wp, X, _, _ in stack.layers[:n]:
+        W = torch.empty((mat.K, mat.N), dtype=torch.float16, device="cuda")
+        lbv.dequant_fp16(plan, Wp, W.view(torch.int16))
+        Xh = X[:M].view(torch.float16 if mat.xdtype == "f16" else torch.bfloat16)
+        Xh = Xh.to(torch.float16).contiguous()
+        Yh = torch.empty((M, mat.N), dtype=torch.float16, device="cuda")
+        calls.append((Xh, W, Yh))
+
+    def step():
+        for Xh, W, Yh in calls:
+            torch.matmul(Xh, W, out=Yh)
+
+    how = "CUDA graph of the step"
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        run = g.replay
+    except Exception as e:                       # eager launches, said so below
+        torch.cuda.synchronize()
+        run, how = step, f"eager launches (graph capture failed: {type(e).__name__})"
+    ms = reduce_max(timed(torch, run, steps, warmup, barrier))
+    us = ms * 1e3 / (steps * n)
+    bytes_call = sum(b + M * mat.K * 2 + M * mat.N * 2
+                     for b, (mat, *_r) in zip(dense_b[:n], stack.layers[:n])) / n
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    del calls
+    torch.cuda.empty_cache()
+    return {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "bytes_per_call": round(bytes_call),
+            "matrices_per_step": n,
+            "how": f"cuBLAS fp16 GEMM (torch.matmul) on the dequantized weights, {how}; "
+                   "rotation not included; context only"}
+
+
 def kernel_hash():
     """Hash of the device code (kernels and the headers they include); the
     host-side planning in the .cpp files does not change what a captured
@@ -302,9 +359,47 @@ def recorded_traffic(workload, M, kernel):
     return None
 
 
-def cpu_baseline(workload, M, budget_s=10.0, head="fused"):
-    """The fp64 oracle as it stands, single-threaded on the host: verify calls
-    on full matrices of the workload until about budget_s has passed."""
+def host_cpu():
+    """The host's processor model and core counts (where the oracle runs)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"model": model or os.uname().machine, "nproc": os.cpu_count(),
+            "usable": len(os.sched_getaffinity(0))}
+
+
+def oracle_columns(oracle, fmt, parts, Xf, mat, cols, nthreads):
+    """The oracle's verify over `cols`, split into contiguous column ranges
+    run on `nthreads` host threads (the C call releases the GIL; columns are
+    independent, so this is the oracle unchanged, over N in parallel)."""
+    if nthreads <= 1:
+        oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(lambda c: oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=c),
+                    np.array_split(cols, nthreads)))
+
+
+def oracle_sample(workload, M, budget_s, head, nthreads):
+    """GB/s of the fp64 oracle on nthreads host threads: verify calls on the
+    workload's matrices (whole, or a slice of columns) until about budget_s
+    has passed."""
     import oracle
     oracle.build()
     wl = synth.WORKLOADS[workload]
@@ -316,24 +411,36 @@ def cpu_baseline(workload, M, budget_s=10.0, head="fused"):
         Xf = oracle.x_to_f64(xb[:M], mat.xdtype)
         if mat.rotate:
             Xf = oracle.x_to_f64(oracle.round_x(oracle.fwht128(Xf), mat.xdtype), mat.xdtype)
-        # columns: whole matrix if it fits in the remaining budget, else a sample
-        ncols = mat.N if mat.N <= 20000 else 16384
+        # columns: the whole matrix if it is small enough, else a slice
+        ncols = mat.N if mat.N <= 20000 * nthreads else min(mat.N, 16384 * nthreads)
         cols = np.arange(ncols)
         t0 = time.perf_counter()
-        oracle.verify(FMT_IDS[mat.fmt], parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+        oracle_columns(oracle, FMT_IDS[mat.fmt], parts, Xf, mat, cols, nthreads)
         dt = time.perf_counter() - t0
-        frac = ncols / mat.N
-        done_bytes += call_bytes(mat, M, head) * frac
+        done_bytes += call_bytes(mat, M, head) * ncols / mat.N
         t_total += dt
         cols_done += ncols
         calls += 1
         i += 1
     gbs = done_bytes / t_total / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "us_per_call": t_total / (done_bytes / call_bytes(wl.matrices[0], M, head)) * 1e6,
+    us_per_call = t_total / (done_bytes / call_bytes(wl.matrices[0], M, head)) * 1e6
+    how = "single-threaded" if nthreads == 1 else f"on {nthreads} threads over column ranges"
+    return {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "us_per_call": us_per_call,
             "sample": f"{calls} oracle verify call(s), {cols_done} output columns x {M} rows "
-                      f"of {workload}, {t_total:.1f} s single-threaded; GB/s of the sample's "
+                      f"of {workload}, {t_total:.1f} s {how}; GB/s of the sample's "
                       "algorithmic bytes"}
+
+
+def cpu_baseline(workload, M, budget_s=10.0, head="fused"):
+    """The fp64 oracle as it stands on the host: single-threaded (the reported
+    baseline), and the same calls spread over every usable core."""
+    line = oracle_sample(workload, M, budget_s, head, 1)
+    host = host_cpu()
+    line["host"] = host
+    if host["usable"] > 1:
+        line["all_cores"] = oracle_sample(workload, M, budget_s / 2, head, host["usable"])
+    return line
 
 
 def run_lbv(args, rank, world, barrier, reduce_max):
@@ -422,6 +529,12 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     t_e2e = reduce_max((time.perf_counter() - t0) * 1e3)
     e2e_val = replica_value(bytes_step, world, t_e2e / args.steps)
 
+    dense = None
+    if not args.no_dense:
+        dense = dense_context(stack, args.M, l2, max(3, args.steps // 4), args.warmup, peak,
+                              barrier, reduce_max)
+        dense["packed_speedup"] = round(dense["us_per_call"] / (ms_per_step * 1e3 / stack.calls), 2)
+
     shape = next(iter(stack.plans.values())).shape()
     line = {
         "metric": METRIC,
@@ -478,6 +591,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * stack.launches_per_step,
         "clocks": clocks,
+        "dense_fp16_context": dense,
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.M, head=args.head)
@@ -485,8 +599,9 @@ def run_lbv(args, rank, world, barrier, reduce_max):
 
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle as it stands on the host cores; each
-    step is a bounded sample (a slice of output columns) of the workload."""
+    """The reference arm: the fp64 oracle as it stands on the host cores
+    (threads over column ranges, every usable core); each step is a bounded
+    sample (a slice of output columns) of the workload."""
     import oracle
     oracle.build()
     wl = synth.WORKLOADS[args.workload]
@@ -496,27 +611,29 @@ def run_reference(args):
     Xf = oracle.x_to_f64(xb[:M], mat.xdtype)
     if mat.rotate:
         Xf = oracle.x_to_f64(oracle.round_x(oracle.fwht128(Xf), mat.xdtype), mat.xdtype)
-    ncols = min(mat.N, 256)
+    host = host_cpu()
+    nthr = host["usable"]
+    ncols = min(mat.N, 256 * nthr)
     cols = np.arange(ncols)
     fmt = FMT_IDS[mat.fmt]
     for _ in range(max(0, args.warmup)):
-        oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+        oracle_columns(oracle, fmt, parts, Xf, mat, cols, nthr)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.verify(fmt, parts, Xf, mat.K, mat.N, mat.group, cols=cols)
+        oracle_columns(oracle, fmt, parts, Xf, mat, cols, nthr)
     dt = time.perf_counter() - t0
     sample_bytes = call_bytes(mat, M, args.head) * ncols / mat.N
     gbs = sample_bytes * args.steps / dt / 1e9
     sample = (f"{ncols} of {mat.N} output columns x {M} rows of {args.workload} per step, "
-              "fp64 oracle, single-threaded")
+              f"fp64 oracle on {nthr} threads over column ranges")
     return {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "sample_columns": ncols},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle",
+                         "sample": sample, "host": host},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

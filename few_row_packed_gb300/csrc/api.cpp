@@ -118,7 +118,8 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
         G = std::min<int64_t>(G, ctas_req);
     for (int it = 0; it < 4; ++it) {
         const int tiles_max = (int)((ntiles + G - 1) / G);
-        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits), kSmemOnePerSm);
+        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits, false),
+                           kSmemOnePerSm);
         if (sh.smem > kSmemCap)
             return false;
         sh.ctas_n = (int)G;
@@ -131,7 +132,8 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
             return true;
         G = maxc;
     }
-    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits),
+    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits,
+                                 false),
                        kSmemOnePerSm);
     sh.ctas_n = (int)G;
     return ops->prepare(P->xdtype, sh) == cudaSuccess;
@@ -1184,7 +1186,7 @@ bool group_fit(lbv_group* G, int c, int tpw, int splits, int R, lbv::GroupLaunch
     L.shape = {16, tpw, splits, 0, 0};
     L.shape.ctas_n = divide_rows(G, c, R, nullptr, rows.data());
     L.tiles_max = group_tiles_max(G, rows.data());
-    L.shape.smem = std::max(ops->smem(16, tpw, cps_max, L.tiles_max, splits), kSmemOnePerSm);
+    L.shape.smem = std::max(ops->smem(16, tpw, cps_max, L.tiles_max, splits, true), kSmemOnePerSm);
     if (L.shape.smem > kSmemCap)
         return false;
     L.resident = ops->max_clusters_grouped(G->xdtype, L.shape);
@@ -1271,7 +1273,7 @@ bool group_default_launches(lbv_group* G)
         smin[i] = 0;
         for (int s = 1; s <= 8 && !smin[i]; ++s) {
             const int cp = group_problem_cps(G, i, s);
-            if (cp && std::max(ops->smem(16, 2, cp, 1, s), kSmemOnePerSm) <= kSmemCap)
+            if (cp && std::max(ops->smem(16, 2, cp, 1, s, true), kSmemOnePerSm) <= kSmemCap)
                 smin[i] = s;
         }
         if (!smin[i])

@@ -530,14 +530,28 @@ __device__ __forceinline__ void rotate_x(uint32_t xs_a, int RS, int nblk, int wa
 // ---------------------------------------------------------------------------
 // Compile-time geometry of one (format, group, warps, tiles-per-warp) kernel.
 
-template <int FMT, int GROUP, int NW, int TPW>
+// Chunks of each tile per ring stage.  A stage's fixed work (the barrier
+// wait, the copy issue, the cursor) is spread over TPW * STAGE_CHUNKS * KT
+// MMAs; the single-matrix kernel takes three chunks per stage with two-tile
+// units (rings of ~110 KB; two where a record has more than four side words,
+// whose registers would spill) and four with one-tile units (~80 KB).  The
+// grouped kernel keeps two, so that its long-K problems still fit their rings
+// beside their X slices.
+template <int FMT, int GROUP, int TPW>
+__host__ __device__ constexpr int single_stage_chunks()
+{
+    return TPW == 1 ? 4 : (TPW == 2 && Traits<FMT, GROUP>::SIDE_W <= 4) ? 3 : 2;
+}
+constexpr int kGroupedStageChunks = 2;
+
+template <int FMT, int GROUP, int NW, int TPW, int STAGE_CHUNKS>
 struct Geometry {
     using T = Traits<FMT, GROUP>;
     static constexpr int SIDE_B = T::SIDE_W * 4;              // side bytes per (record, g)
     static constexpr int REC = 512 + 8 * SIDE_B;              // record bytes (tile, chunk)
     static_assert(REC % 16 == 0 && (SIDE_B == 8 || SIDE_B % 16 == 0),
                   "records and side words stay aligned for 8/16-byte shared loads");
-    static constexpr int CPS = 2;                             // chunks per ring stage
+    static constexpr int CPS = STAGE_CHUNKS;                  // chunks per ring stage
     static constexpr int SLOT_B = TPW * CPS * REC;            // one ring stage
     static constexpr int STAGES_RAW = 98304 / (NW * SLOT_B);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -560,10 +574,10 @@ __host__ __device__ constexpr int x_row_stride(int cps)
 // Shared memory carve-up (bytes):
 //   ring | mbarriers (+ X barrier, flag, argmax keys) | xs (X rows) | corr |
 //   rsum (affine) | part (K split)
-template <int FMT, int GROUP, int NW, int TPW>
+template <int FMT, int GROUP, int NW, int TPW, int STAGE_CHUNKS>
 __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int splits)
 {
-    using G = Geometry<FMT, GROUP, NW, TPW>;
+    using G = Geometry<FMT, GROUP, NW, TPW, STAGE_CHUNKS>;
     using T = Traits<FMT, GROUP>;
     size_t b = G::RING_B + G::BAR_B;
     b += 8 * x_row_stride<FMT, GROUP>(cps);
@@ -575,10 +589,10 @@ __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int spl
 
 // ---------------------------------------------------------------------------
 
-template <int FMT, int XT, int GROUP, int NW, int TPW>
+template <int FMT, int XT, int GROUP, int NW, int TPW, int STAGE_CHUNKS>
 struct VerifyKernel {
     using T = Traits<FMT, GROUP>;
-    using G = Geometry<FMT, GROUP, NW, TPW>;
+    using G = Geometry<FMT, GROUP, NW, TPW, STAGE_CHUNKS>;
     static constexpr int STAGES = G::STAGES;
     static constexpr int NSET = T::GPC;                     // accumulator chains per tile
 
@@ -1098,9 +1112,10 @@ struct VerifyKernel {
                 slot = 0;
                 parity ^= 1u;
             }
-            process_chunk(w[0], sd[0], cc, xa_lane, corr, rsum, bases, y, lane);
-            if (nc > 1)
-                process_chunk(w[1], sd[1], cc + 1, xa_lane, corr, rsum, bases, y, lane);
+#pragma unroll
+            for (int ci = 0; ci < G::CPS; ++ci)
+                if (ci == 0 || ci < nc)
+                    process_chunk(w[ci], sd[ci], cc + ci, xa_lane, corr, rsum, bases, y, lane);
             cc += nc;
             if (cc == nch) {
                 store_unit(p, t1, t0 + cu * TPW, y, g, t, part, t0, lane, ak);
@@ -1182,7 +1197,8 @@ template <int FMT, int XT, int GROUP, int NW, int TPW>
 __global__ void __launch_bounds__(NW * 32, 1) lbv_verify_kernel(const VerifyParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem, (int)blockIdx.y, (int)gridDim.y);
+    constexpr int SC = single_stage_chunks<FMT, GROUP, TPW>();
+    VerifyKernel<FMT, XT, GROUP, NW, TPW, SC>::run(p, smem, (int)blockIdx.y, (int)gridDim.y);
 }
 
 // Grouped verify: independent problems of one format in one launch.  Cluster
@@ -1230,8 +1246,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     p.amax_done = nullptr;
     p.amax_idx = nullptr;
     p.amax_val = nullptr;
-    VerifyKernel<FMT, XT, GROUP, NW, TPW>::run(p, smem, y - gp.ybegin[lo],
-                                               gp.ybegin[lo + 1] - gp.ybegin[lo]);
+    VerifyKernel<FMT, XT, GROUP, NW, TPW, kGroupedStageChunks>::run(
+        p, smem, y - gp.ybegin[lo], gp.ybegin[lo + 1] - gp.ybegin[lo]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1256,13 +1272,22 @@ inline void* grouped_kernel_ptr(int warps, int tpw)
     return nullptr;
 }
 
-template <int FMT, int GROUP>
-inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits)
+template <int FMT, int GROUP, int NW, int TPW>
+inline size_t smem_bytes_k(int cps, int tiles_max, int splits, bool grouped)
 {
-    if (warps == 8 && tpw == 2) return smem_bytes_for<FMT, GROUP, 8, 2>(cps, tiles_max, splits);
-    if (warps == 8 && tpw == 4) return smem_bytes_for<FMT, GROUP, 8, 4>(cps, tiles_max, splits);
-    if (warps == 16 && tpw == 1) return smem_bytes_for<FMT, GROUP, 16, 1>(cps, tiles_max, splits);
-    if (warps == 16 && tpw == 2) return smem_bytes_for<FMT, GROUP, 16, 2>(cps, tiles_max, splits);
+    constexpr int SC = single_stage_chunks<FMT, GROUP, TPW>();
+    return grouped ? smem_bytes_for<FMT, GROUP, NW, TPW, kGroupedStageChunks>(cps, tiles_max, splits)
+                   : smem_bytes_for<FMT, GROUP, NW, TPW, SC>(cps, tiles_max, splits);
+}
+
+// Shared memory of a launch of the single-matrix kernel, or of the grouped one.
+template <int FMT, int GROUP>
+inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits, bool grouped)
+{
+    if (warps == 8 && tpw == 2) return smem_bytes_k<FMT, GROUP, 8, 2>(cps, tiles_max, splits, grouped);
+    if (warps == 8 && tpw == 4) return smem_bytes_k<FMT, GROUP, 8, 4>(cps, tiles_max, splits, grouped);
+    if (warps == 16 && tpw == 1) return smem_bytes_k<FMT, GROUP, 16, 1>(cps, tiles_max, splits, grouped);
+    if (warps == 16 && tpw == 2) return smem_bytes_k<FMT, GROUP, 16, 2>(cps, tiles_max, splits, grouped);
     return (size_t)1 << 40;
 }
 

@@ -11,7 +11,8 @@ struct VerifyOps {
                           const LaunchOpts& o, cudaStream_t st);
     cudaError_t (*prepare)(lbv_dtype xt, const Shape& sh);
     int (*max_clusters)(lbv_dtype xt, const Shape& sh);
-    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits);
+    // shared memory of the single-matrix kernel, or of the grouped one
+    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits, bool grouped);
     // grouped verify (16 warps, 1 or 2 tiles per unit)
     cudaError_t (*launch_grouped)(lbv_dtype xt, const Shape& sh, const GroupedParams& gp,
                                   const LaunchOpts& o, cudaStream_t st);
@@ -46,9 +47,10 @@ extern const VerifyOps q4_0_ops;
         return xt == LBV_F16 ? max_clusters_t<FMT, LBV_F16, GROUP>(sh)                      \
                              : max_clusters_t<FMT, LBV_BF16, GROUP>(sh);                    \
     }                                                                                       \
-    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits)       \
+    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits,       \
+                              bool grouped)                                                 \
     {                                                                                       \
-        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits);                \
+        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits, grouped);       \
     }                                                                                       \
     static cudaError_t NAME##_launch_grouped(lbv_dtype xt, const Shape& sh,                 \
                                              const GroupedParams& gp, const LaunchOpts& o,  \

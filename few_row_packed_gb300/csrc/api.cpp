@@ -118,8 +118,7 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
         G = std::min<int64_t>(G, ctas_req);
     for (int it = 0; it < 4; ++it) {
         const int tiles_max = (int)((ntiles + G - 1) / G);
-        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits, false),
-                           kSmemOnePerSm);
+        sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits), kSmemOnePerSm);
         if (sh.smem > kSmemCap)
             return false;
         sh.ctas_n = (int)G;
@@ -132,8 +131,7 @@ bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
             return true;
         G = maxc;
     }
-    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits,
-                                 false),
+    sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, (int)((ntiles + G - 1) / G), sh.splits),
                        kSmemOnePerSm);
     sh.ctas_n = (int)G;
     return ops->prepare(P->xdtype, sh) == cudaSuccess;
@@ -1172,21 +1170,23 @@ int group_tiles_max(const lbv_group* G, const int* rows)
 bool group_fit(lbv_group* G, int c, int tpw, int splits, int R, lbv::GroupLaunch* out)
 {
     const lbv::VerifyOps* ops = ops_for(G->fmt, G->group);
-    int cps_max = 0;
-    for (int i = 0; i < G->count; ++i) {
-        if (G->cls[i] != c)
-            continue;
-        const int cp = group_problem_cps(G, i, splits);
-        if (cp == 0)
+    for (int i = 0; i < G->count; ++i)
+        if (G->cls[i] == c && group_problem_cps(G, i, splits) == 0)
             return false;
-        cps_max = std::max(cps_max, cp);
-    }
     std::vector<int> rows(G->count);
     lbv::GroupLaunch L;
     L.shape = {16, tpw, splits, 0, 0};
     L.shape.ctas_n = divide_rows(G, c, R, nullptr, rows.data());
     L.tiles_max = group_tiles_max(G, rows.data());
-    L.shape.smem = std::max(ops->smem(16, tpw, cps_max, L.tiles_max, splits, true), kSmemOnePerSm);
+    // a CTA lays out its own problem's X slice and partials: the launch
+    // needs the largest of the problems' needs, not the largest slice next
+    // to the largest partials
+    size_t need = 0;
+    for (int i = 0; i < G->count; ++i)
+        if (rows[i] > 0)
+            need = std::max(need, ops->smem(16, tpw, group_problem_cps(G, i, splits),
+                                            (G->ntiles[i] + rows[i] - 1) / rows[i], splits));
+    L.shape.smem = std::max(need, kSmemOnePerSm);
     if (L.shape.smem > kSmemCap)
         return false;
     L.resident = ops->max_clusters_grouped(G->xdtype, L.shape);
@@ -1273,7 +1273,7 @@ bool group_default_launches(lbv_group* G)
         smin[i] = 0;
         for (int s = 1; s <= 8 && !smin[i]; ++s) {
             const int cp = group_problem_cps(G, i, s);
-            if (cp && std::max(ops->smem(16, 2, cp, 1, s, true), kSmemOnePerSm) <= kSmemCap)
+            if (cp && std::max(ops->smem(16, 2, cp, 1, s), kSmemOnePerSm) <= kSmemCap)
                 smin[i] = s;
         }
         if (!smin[i])

@@ -532,17 +532,14 @@ __device__ __forceinline__ void rotate_x(uint32_t xs_a, int RS, int nblk, int wa
 
 // Chunks of each tile per ring stage.  A stage's fixed work (the barrier
 // wait, the copy issue, the cursor) is spread over TPW * STAGE_CHUNKS * KT
-// MMAs; the single-matrix kernel takes three chunks per stage with two-tile
-// units (rings of ~110 KB; two where a record has more than four side words,
-// whose registers would spill) and four with one-tile units (~80 KB).  The
-// grouped kernel keeps two, so that its long-K problems still fit their rings
-// beside their X slices.
+// MMAs: three chunks per stage with two-tile units (rings of ~110 KB; two
+// where a record has more than four side words, whose registers would
+// spill), four with one-tile units (~80 KB), two with four-tile units.
 template <int FMT, int GROUP, int TPW>
-__host__ __device__ constexpr int single_stage_chunks()
+__host__ __device__ constexpr int stage_chunks()
 {
     return TPW == 1 ? 4 : (TPW == 2 && Traits<FMT, GROUP>::SIDE_W <= 4) ? 3 : 2;
 }
-constexpr int kGroupedStageChunks = 2;
 
 template <int FMT, int GROUP, int NW, int TPW, int STAGE_CHUNKS>
 struct Geometry {
@@ -1197,7 +1194,7 @@ template <int FMT, int XT, int GROUP, int NW, int TPW>
 __global__ void __launch_bounds__(NW * 32, 1) lbv_verify_kernel(const VerifyParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int SC = single_stage_chunks<FMT, GROUP, TPW>();
+    constexpr int SC = stage_chunks<FMT, GROUP, TPW>();
     VerifyKernel<FMT, XT, GROUP, NW, TPW, SC>::run(p, smem, (int)blockIdx.y, (int)gridDim.y);
 }
 
@@ -1246,8 +1243,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     p.amax_done = nullptr;
     p.amax_idx = nullptr;
     p.amax_val = nullptr;
-    VerifyKernel<FMT, XT, GROUP, NW, TPW, kGroupedStageChunks>::run(
-        p, smem, y - gp.ybegin[lo], gp.ybegin[lo + 1] - gp.ybegin[lo]);
+    constexpr int SC = stage_chunks<FMT, GROUP, TPW>();
+    VerifyKernel<FMT, XT, GROUP, NW, TPW, SC>::run(p, smem, y - gp.ybegin[lo],
+                                                   gp.ybegin[lo + 1] - gp.ybegin[lo]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1273,21 +1271,19 @@ inline void* grouped_kernel_ptr(int warps, int tpw)
 }
 
 template <int FMT, int GROUP, int NW, int TPW>
-inline size_t smem_bytes_k(int cps, int tiles_max, int splits, bool grouped)
+inline size_t smem_bytes_k(int cps, int tiles_max, int splits)
 {
-    constexpr int SC = single_stage_chunks<FMT, GROUP, TPW>();
-    return grouped ? smem_bytes_for<FMT, GROUP, NW, TPW, kGroupedStageChunks>(cps, tiles_max, splits)
-                   : smem_bytes_for<FMT, GROUP, NW, TPW, SC>(cps, tiles_max, splits);
+    return smem_bytes_for<FMT, GROUP, NW, TPW, stage_chunks<FMT, GROUP, TPW>()>(cps, tiles_max,
+                                                                              splits);
 }
 
-// Shared memory of a launch of the single-matrix kernel, or of the grouped one.
 template <int FMT, int GROUP>
-inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits, bool grouped)
+inline size_t smem_bytes_t(int warps, int tpw, int cps, int tiles_max, int splits)
 {
-    if (warps == 8 && tpw == 2) return smem_bytes_k<FMT, GROUP, 8, 2>(cps, tiles_max, splits, grouped);
-    if (warps == 8 && tpw == 4) return smem_bytes_k<FMT, GROUP, 8, 4>(cps, tiles_max, splits, grouped);
-    if (warps == 16 && tpw == 1) return smem_bytes_k<FMT, GROUP, 16, 1>(cps, tiles_max, splits, grouped);
-    if (warps == 16 && tpw == 2) return smem_bytes_k<FMT, GROUP, 16, 2>(cps, tiles_max, splits, grouped);
+    if (warps == 8 && tpw == 2) return smem_bytes_k<FMT, GROUP, 8, 2>(cps, tiles_max, splits);
+    if (warps == 8 && tpw == 4) return smem_bytes_k<FMT, GROUP, 8, 4>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 1) return smem_bytes_k<FMT, GROUP, 16, 1>(cps, tiles_max, splits);
+    if (warps == 16 && tpw == 2) return smem_bytes_k<FMT, GROUP, 16, 2>(cps, tiles_max, splits);
     return (size_t)1 << 40;
 }
 

@@ -11,8 +11,7 @@ struct VerifyOps {
                           const LaunchOpts& o, cudaStream_t st);
     cudaError_t (*prepare)(lbv_dtype xt, const Shape& sh);
     int (*max_clusters)(lbv_dtype xt, const Shape& sh);
-    // shared memory of the single-matrix kernel, or of the grouped one
-    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits, bool grouped);
+    size_t (*smem)(int warps, int tpw, int cps, int tiles_max, int splits);
     // grouped verify (16 warps, 1 or 2 tiles per unit)
     cudaError_t (*launch_grouped)(lbv_dtype xt, const Shape& sh, const GroupedParams& gp,
                                   const LaunchOpts& o, cudaStream_t st);
@@ -47,10 +46,9 @@ extern const VerifyOps q4_0_ops;
         return xt == LBV_F16 ? max_clusters_t<FMT, LBV_F16, GROUP>(sh)                      \
                              : max_clusters_t<FMT, LBV_BF16, GROUP>(sh);                    \
     }                                                                                       \
-    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits,       \
-                              bool grouped)                                                 \
+    static size_t NAME##_smem(int warps, int tpw, int cps, int tiles_max, int splits)       \
     {                                                                                       \
-        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits, grouped);       \
+        return smem_bytes_t<FMT, GROUP>(warps, tpw, cps, tiles_max, splits);                \
     }                                                                                       \
     static cudaError_t NAME##_launch_grouped(lbv_dtype xt, const Shape& sh,                 \
                                              const GroupedParams& gp, const LaunchOpts& o,  \

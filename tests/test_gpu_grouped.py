@@ -62,19 +62,11 @@ class Problems:
         return [Y.cpu().numpy() for Y in Ys]
 
     def single(self, i, M):
-        """lbv_verify_gemm of problem i with its launch class's K split (and
-        tiles per unit).  The single-matrix kernel streams more chunks per ring
-        stage, so a class's two-tile shape may not fit it next to a long X
-        slice; one-tile units then stand in: which warp owns a tile does not
-        change the tile's arithmetic."""
+        """lbv_verify_gemm of problem i with its launch class's tiles per unit and K split."""
         K, N = self.shapes[i]
         tpw, splits, _ = self.G.shape(self.G.problem_launch(i))
         plan = lbv.Plan(self.fmt, K, N, self.group, DT[self.xdtype])
-        try:
-            plan.set_shape(16, tpw, splits, 0)
-        except lbv.LbvError as e:
-            assert e.status == lbv.ERR_UNSUPPORTED and tpw == 2, e
-            plan.set_shape(16, 1, splits, 0)
+        plan.set_shape(16, tpw, splits, 0)
         Y = torch.full((8, N), float(SENT), dtype=torch.float32, device="cuda")
         lbv.verify_gemm(plan, self.X[i], M, self.Wp[i], Y)
         torch.cuda.synchronize()

@@ -330,17 +330,40 @@ def dense_context(stack, M, l2_bytes, steps, warmup, peak, barrier, reduce_max):
                    "rotation not included; context only"}
 
 
+def code_text(src: str) -> str:
+    """C/C++ source without its comments, trailing blanks and empty lines."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] in "\"'":                    # string or character literal
+            q, j = src[i], i + 1
+            while j < n and src[j] != q:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_hash():
-    """Hash of the device code (kernels and the headers they include); the
-    host-side planning in the .cpp files does not change what a captured
-    launch executes."""
+    """Hash of the device code (kernels and the headers they include, without
+    comments); the host-side planning in the .cpp files does not change what a
+    captured launch executes."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "few_row_packed_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         if not f.endswith((".cu", ".cuh", ".h")):
             continue
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

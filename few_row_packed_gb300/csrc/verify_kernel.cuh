@@ -13,8 +13,8 @@
 //     writes, start streaming before it.
 //   * Each warp streams its tiles' packed codes and scales through a private
 //     ring of shared-memory stages filled by 1-D bulk async copies (TMA engine)
-//     and tracked by mbarriers, so a few tens of KB per SM stay in flight with
-//     no registers held.  Every wait is bounded; a wait that gives up sets the
+//     and tracked by mbarriers, so 75-110 KB per SM stay in flight with no
+//     registers held; a stage carries two to four chunks of each tile.  Every wait is bounded; a wait that gives up sets the
 //     plan's status word and the warp stops.
 //   * Decode is one LOP3 per A-fragment register: (word_variant & mask) ^ base
 //     places a code in the mantissa/exponent field of an fp16 or bf16 whose
@@ -26,7 +26,8 @@
 //     are the M side and the M <= 8 activation rows the N side (rows >= M are
 //     zero), so each decoded weight meets every drafted row at once (Ishizuki
 //     README, "Kernels written for the verify").  The k-tiles of a chunk are
-//     issued alternately from two independent accumulator chains.
+//     visited alternately from its two halves (two interleaved accumulator
+//     chains for groups of 64 or fewer), and each tile of a unit has its own.
 //   * The offsets c enter each group's accumulator as its initial value
 //     -sum_k c_k x_k, computed once per CTA from the staged activations (the
 //     "row-sum prep" of the dflash-mlx-bonsai2 README); the group scale (and

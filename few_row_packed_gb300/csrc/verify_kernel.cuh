@@ -14,8 +14,9 @@
 //   * Each warp streams its tiles' packed codes and scales through a private
 //     ring of shared-memory stages filled by 1-D bulk async copies (TMA engine)
 //     and tracked by mbarriers, so 75-110 KB per SM stay in flight with no
-//     registers held; a stage carries two to four chunks of each tile.  Every wait is bounded; a wait that gives up sets the
-//     plan's status word and the warp stops.
+//     registers held; a stage carries two to four chunks of each tile.  Every
+//     wait is bounded; a wait that gives up sets the plan's status word and
+//     the warp stops.
 //   * Decode is one LOP3 per A-fragment register: (word_variant & mask) ^ base
 //     places a code in the mantissa/exponent field of an fp16 or bf16 whose
 //     value is  code_value + c  for a small integer c fixed by the bit position
@@ -529,8 +530,6 @@ __device__ __forceinline__ void rotate_x(uint32_t xs_a, int RS, int nblk, int wa
 }
 
 // ---------------------------------------------------------------------------
-// Compile-time geometry of one (format, group, warps, tiles-per-warp) kernel.
-
 // Chunks of each tile per ring stage.  A stage's fixed work (the barrier
 // wait, the copy issue, the cursor) is spread over TPW * STAGE_CHUNKS * KT
 // MMAs: three chunks per stage with two-tile units (rings of ~110 KB; two
@@ -542,6 +541,8 @@ __host__ __device__ constexpr int stage_chunks()
     return TPW == 1 ? 4 : (TPW == 2 && Traits<FMT, GROUP>::SIDE_W <= 4) ? 3 : 2;
 }
 
+// Compile-time geometry of one (format, group, warps, tiles per warp, chunks
+// per stage) kernel.
 template <int FMT, int GROUP, int NW, int TPW, int STAGE_CHUNKS>
 struct Geometry {
     using T = Traits<FMT, GROUP>;

@@ -747,15 +747,16 @@ lbv_status lbv_verify_fused_noalloc(const lbv_plan* P, const void* X, int M, int
     if (ops & LBV_FUSED_ARGMAX) {
         if (lbv::noalloc_scratch_bytes() < kFusedWorkspace)
             return fail(LBV_ERR_WORKSPACE, "lbv_verify_fused_noalloc: scratch too small");
-        bool first = false;
-        cudaError_t e = lbv::noalloc_scratch(&scratch, &first);
+        bool needs_clear = false;
+        cudaError_t e = lbv::noalloc_scratch(&scratch, &needs_clear);
         if (e != cudaSuccess)
             return cuda_fail(e, "lbv_verify_fused_noalloc: scratch address");
-        if (first) {            // zero at load already; cleared once more on first use
+        if (needs_clear) {      // zero at load already; cleared once more on first use
             e = cudaMemsetAsync(scratch, 0, lbv::noalloc_scratch_bytes(),
                                 reinterpret_cast<cudaStream_t>(stream));
             if (e != cudaSuccess)
                 return cuda_fail(e, "lbv_verify_fused_noalloc: clearing the scratch");
+            lbv::noalloc_scratch_cleared();
         }
     }
     return lbv_verify_fused(P, X, M, ldx, Wp, ops, signs, Y, ldy, argmax_idx, argmax_val,

@@ -217,10 +217,12 @@ cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, 
 // codes the few-row kernel's lane does; the 4 lanes of a column pair reduce
 // by shuffles.
 
+// Elements k and k + 1 of an X row.  Two 16-bit loads: X need only be 2-byte
+// aligned and ldx may be odd, so a 4-byte load could be misaligned.
 template <int DT>
 __device__ __forceinline__ float2 x_pair(const uint16_t* x, int k)
 {
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(x + k);   // k even
+    const uint32_t v = (uint32_t)x[k] | ((uint32_t)x[k + 1] << 16);
     if constexpr (DT == LBV_F16) {
         return __half22float2(*reinterpret_cast<const __half2*>(&v));
     } else {

@@ -79,10 +79,12 @@ size_t noalloc_scratch_bytes()
     return kNoAllocScratch;
 }
 
-// The scratch of the current device (its symbol address, looked up once per
-// device).  *first is true on the first request for the device, when the caller
-// clears it on its stream.
-cudaError_t noalloc_scratch(void** out, bool* first)
+// The scratch of the current device: its symbol address, looked up once per
+// device (a cudaDeviceReset invalidates it for the rest of the process).
+// *needs_clear stays true until noalloc_scratch_cleared() records that a
+// clear of the device's scratch was enqueued, so a failed clear is retried on
+// the next call.
+cudaError_t noalloc_scratch(void** out, bool* needs_clear)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -99,9 +101,18 @@ cudaError_t noalloc_scratch(void** out, bool* first)
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
-    *first = !g_scratch_cleared[dev];
-    g_scratch_cleared[dev] = true;
+    *needs_clear = !g_scratch_cleared[dev];
     return cudaSuccess;
+}
+
+// Records that the clear of the current device's scratch was enqueued.
+void noalloc_scratch_cleared()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    g_scratch_cleared[dev] = true;
 }
 
 }  // namespace lbv

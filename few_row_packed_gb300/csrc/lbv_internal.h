@@ -91,7 +91,8 @@ cudaError_t launch_fused_rotation(const void* X, void* Xr, int M, int K, lbv_dty
 // (fused_aux.cu): its size, and its address on the current device; *first is
 // true on the first request for a device.
 size_t noalloc_scratch_bytes();
-cudaError_t noalloc_scratch(void** out, bool* first);
+cudaError_t noalloc_scratch(void** out, bool* needs_clear);
+void noalloc_scratch_cleared();
 
 cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, int N,
                            int ntiles, int nchunks, uint16_t* W, cudaStream_t st);

@@ -287,16 +287,22 @@ LBV_API lbv_status lbv_verify_fused(const lbv_plan* plan, const void* X, int M, 
                                     void* workspace, size_t workspace_bytes, lbv_stream stream);
 
 /*
- * lbv_verify_fused without a caller workspace: the argmax scratch (the
- * 128-byte workspace layout; 256 bytes reserved) is a device array of the
- * library module itself, one per device, zero at load, cleared once more on
- * the stream of the first call on each device, and left zero by every call.
- * The library allocates nothing.  M > 8 is rejected (the scratch holds 8 rows).
- * Other arguments, rules and errors as lbv_verify_fused.  Races: the scratch is
- * shared by every call on a device, so calls that could overlap in time (other
- * streams, other host threads without ordering) must not be made; calls in one
- * stream are ordered and safe.  The pages have no counterpart of this entry
- * point: it exists so that a caller need not own device memory for the argmax.
+ * lbv_verify_fused without a caller workspace, for callers that cannot
+ * allocate device memory: an engine whose memory is one arena sized at start-up
+ * (nothing may call cudaMalloc after that), or host code that must not make a
+ * blocking allocation on its decode path.  The argmax scratch (the 128-byte
+ * workspace layout; 256 bytes reserved) is a device array of the library
+ * module itself, one per device, held by every device that loads the library
+ * until the process exits.  Set-up: the first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) and clears it on that call's
+ * stream, so make the first call on each device before any stream capture; a
+ * cudaDeviceReset invalidates the looked-up address for the rest of the
+ * process.  Every call leaves the scratch zero.  The library allocates
+ * nothing.  M > 8 is rejected (the scratch holds 8 rows).  Other arguments,
+ * rules and errors as lbv_verify_fused.  Races: the scratch is shared by every
+ * call on a device, so calls that could overlap in time (other streams, other
+ * host threads without ordering) must not be made; calls in one stream are
+ * ordered and safe.  The pages have no counterpart of this entry point.
  */
 LBV_API lbv_status lbv_verify_fused_noalloc(const lbv_plan* plan, const void* X, int M, int ldx,
                                             const void* Wp, unsigned ops,

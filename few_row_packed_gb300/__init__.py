@@ -25,6 +25,7 @@ PLAN_FORCE_FEWROW = 0x2
 PLAN_FORCE_GEMV = 0x4
 PLAN_PDL = 0x8
 PLAN_TCGEN05 = 0x10
+PLAN_TEST_WAIT_LIMIT = 0x20
 KERNEL_FEWROW = 1
 KERNEL_GEMV = 2
 KERNEL_FEWROW_TC = 3

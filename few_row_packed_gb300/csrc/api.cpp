@@ -381,6 +381,13 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: both FORCE flags set");
     if ((flags & LBV_PLAN_TCGEN05) && (flags & LBV_PLAN_FORCE_GEMV))
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: TCGEN05 with FORCE_GEMV");
+    if ((flags & LBV_PLAN_TEST_WAIT_LIMIT) &&
+        (flags & (LBV_PLAN_TCGEN05 | LBV_PLAN_FORCE_GEMV | LBV_PLAN_MEASURE)))
+        return fail(LBV_ERR_INVALID_ARG,
+                    "lbv_plan_create: TEST_WAIT_LIMIT with TCGEN05, FORCE_GEMV or MEASURE");
+    if (flags & ~(LBV_PLAN_MEASURE | LBV_PLAN_FORCE_FEWROW | LBV_PLAN_FORCE_GEMV | LBV_PLAN_PDL |
+                  LBV_PLAN_TCGEN05 | LBV_PLAN_TEST_WAIT_LIMIT))
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: unknown flags 0x%x", flags);
 
     lbv_plan* P = new (std::nothrow) lbv_plan();
     if (!P)
@@ -606,6 +613,9 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.x_vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 8) == 0) ? 1 : 0;
     p.err = P->dev_err;
     p.zero = 0;
+    const bool wait_test = (P->flags & LBV_PLAN_TEST_WAIT_LIMIT) != 0;
+    p.wait_limit = wait_test ? 256 : 0;
+    p.skip_q = wait_test ? 1 : -1;
     p.rot = 0;
     p.store_y = 1;
     p.signs = nullptr;

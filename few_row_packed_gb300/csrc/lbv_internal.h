@@ -22,6 +22,8 @@ struct VerifyParams {
     int cps;                // chunks per slice (the last slice may be shorter)
     int x_vec;              // 1: X rows 16-byte aligned (vector staging)
     unsigned zero;          // always 0 (keeps decode constants in registers)
+    int wait_limit;         // tries of a main-loop ring wait (0: the default, ~1 s)
+    int skip_q;             // ring stage the first warp of CTA 0 does not issue (-1: none)
     // fused head (lbv_verify_fused); lbv_verify_gemm leaves rot = 0,
     // amax_keys = NULL and store_y = 1
     int rot;                // 1: rotate the staged X blockwise (FWHT-128) first

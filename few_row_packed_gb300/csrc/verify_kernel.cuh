@@ -86,8 +86,8 @@ struct DecSpec {
 __host__ __device__ constexpr DecSpec sign1_spec(int xt, int s)
 {
     if (xt == LBV_F16) {
-        // left shifts only: slots 0-4 -> 5-9, 11-12 -> 14-15, 13 -> 14
-        const int sh = (s <= 4) ? 5 : (s == 11 || s == 12) ? 3 : (s == 13) ? 1 : 0;
+        // two shifts per word: slots 0-4 -> 5-9 (left 5), 11-13 -> 8-10 (right 3)
+        const int sh = (s <= 4) ? 5 : (s >= 11 && s <= 13) ? -3 : 0;
         const int j = s + sh;
         return j == 15   ? DecSpec{sh, j, 0xBC00u, 0, 0}
                : j == 14 ? DecSpec{sh, j, 0x0000u, 1, 1}
@@ -333,11 +333,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait for phase `parity` of an mbarrier.  Returns false if it did
-// not complete within roughly a second.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// not complete within `limit` tries: by default (2^20 tries, sleeping 1 us
+// between tries after the first 4096) roughly a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t limit = 1u << 20)
 {
-    constexpr uint32_t kSpin = 1u << 12, kLimit = 1u << 20;
-    for (uint32_t i = 0; i < kLimit; ++i) {
+    constexpr uint32_t kSpin = 1u << 12;
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -630,7 +632,9 @@ struct VerifyKernel {
         }
     }
 
-    // tstride: bytes between the records of consecutive tiles (nchunks * REC)
+    // tstride: bytes between the records of consecutive tiles (nchunks * REC).
+    // leader = 0 issues nothing (the lanes that do not issue, and the stage a
+    // wait-limit test leaves out).
     static __device__ __forceinline__ void issue(const Cursor& c, size_t tstride,
                                                  uint32_t leader, uint32_t ring_w,
                                                  uint32_t bars_w, int slot)
@@ -1005,6 +1009,11 @@ struct VerifyKernel {
         const int nstage = (nch + G::CPS - 1) / G::CPS;
         const int Q = nu * nstage;
         const uint32_t leader = lane == 0;
+        // wait-limit test (LBV_PLAN_TEST_WAIT_LIMIT): the first warp of the
+        // first CTA does not issue its ring stage skip_q, so its wait on that
+        // stage runs out; ring waits give up after wait_limit tries
+        const int skip_q = (warp == 0 && blockIdx.x == 0 && blockIdx.y == 0) ? p.skip_q : -1;
+        const uint32_t wait_limit = p.wait_limit ? (uint32_t)p.wait_limit : 1u << 20;
         Cursor lcur;
         lcur.unit = warp;
         lcur.stage = 0;
@@ -1018,7 +1027,7 @@ struct VerifyKernel {
         const int nearly = min(1, npre);
 #pragma unroll 1
         for (; lq < nearly; ++lq) {
-            issue(lcur, tstride, leader, ring_w, bars_w, lq);
+            issue(lcur, tstride, leader && lq != skip_q, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
 
@@ -1026,7 +1035,7 @@ struct VerifyKernel {
         const bool x_async = stage_x(p, xs, RS, xbar, c0, nch);
 #pragma unroll 1
         for (; lq < npre; ++lq) {
-            issue(lcur, tstride, leader, ring_w, bars_w, lq);
+            issue(lcur, tstride, leader && lq != skip_q, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
         __syncthreads();               // X barrier initialised, tails zeroed (or X copied)
@@ -1066,7 +1075,7 @@ struct VerifyKernel {
         for (; q < Q; ++q) {
             const uint32_t bar = bars_w + slot * 8;
             // the whole warp leaves together (the unit store below shuffles)
-            const bool landed = mbar_try(bar, parity) || mbar_wait(bar, parity);
+            const bool landed = mbar_try(bar, parity) || mbar_wait(bar, parity, wait_limit);
             if (!__all_sync(0xffffffffu, landed)) {
                 ok = false;
                 break;
@@ -1103,7 +1112,7 @@ struct VerifyKernel {
             __syncwarp();
             if (lq < Q) {
                 fence_proxy_async_if(leader);
-                issue(lcur, tstride, leader, ring_w, bars_w, slot);
+                issue(lcur, tstride, leader && lq != skip_q, ring_w, bars_w, slot);
                 ++lq;
                 cursor_next(p, t0, t1, c0, nch, nstage, lcur);
             }
@@ -1130,7 +1139,8 @@ struct VerifyKernel {
                 atomicOr(p.err, 1u);
             // let the copies already issued into this warp's ring (and X) land
             for (int r = q; r < lq; ++r)
-                mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
+                if (r != skip_q)
+                    mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
             if (x_async && !x_ok)
                 mbar_wait(xbar, 0);
         }
@@ -1236,6 +1246,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     p.nchunks = q.nchunks;
     p.splits = gp.splits;
     p.cps = q.cps;
+    p.wait_limit = 0;
+    p.skip_q = -1;
     p.x_vec = q.x_vec;
     p.zero = 0;
     p.rot = 0;

@@ -93,6 +93,18 @@ typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
                                       layout: pack with lbv_plan_pack and size
                                       buffers with lbv_plan_packed_bytes.  Not
                                       combinable with LBV_PLAN_FORCE_GEMV. */
+#define LBV_PLAN_TEST_WAIT_LIMIT 0x20u /* test only: the few-row kernel's waits
+                                      on its weight stages give up after 256
+                                      tries, and the first warp of the first
+                                      CTA leaves its second stage's copy out,
+                                      so that wait runs out on purpose: the
+                                      warp stops, waits (with the normal
+                                      limit) for the copies it did issue and
+                                      the kernel ends; the plan's device status
+                                      then reports LBV_ERR_TIMEOUT and the
+                                      output is incomplete.  Not combinable with
+                                      LBV_PLAN_TCGEN05, LBV_PLAN_FORCE_GEMV or
+                                      LBV_PLAN_MEASURE. */
 
 /* Kernel ids reported by lbv_plan_query. */
 #define LBV_KERNEL_FEWROW    1     /* mma.sync few-row kernel (default)       */

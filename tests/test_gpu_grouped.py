@@ -215,28 +215,3 @@ def test_all_skipped_and_errors():
     with pytest.raises(lbv.LbvError) as e:
         lbv.Group(lbv.FMT_Q4_0, 32, lbv.F16, [(64, 32)] * 257)
     assert e.value.status == lbv.ERR_INVALID_ARG
-
-
-def test_full_q4_0_stack_grouped():
-    """The 4 x 7 Q4_0 stack in one launch (the benchmark's launch: PDL), on
-    sampled columns of every matrix."""
-    gen = list(synth.gen_workload("q4_0_stack_4x7"))
-    shapes = [(m.K, m.N) for m, _, _ in gen]
-    G = lbv.Group(lbv.FMT_Q4_0, 32, lbv.F16, shapes, lbv.PLAN_PDL)
-    Wp = [dev(lbv.pack(lbv.FMT_Q4_0, parts, m.K, m.N, 32)) for m, parts, _ in gen]
-    X = [dev(xb.view(np.int16)) for _, _, xb in gen]
-    rng = np.random.default_rng(0)
-    for M in (1, 8):
-        Ys = [torch.full((8, m.N), float(SENT), dtype=torch.float32, device="cuda")
-              for m, _, _ in gen]
-        lbv.verify_grouped(G, [(x, M, w, y) for x, w, y in zip(X, Wp, Ys)])
-        torch.cuda.synchronize()
-        G.device_status()
-        for (m, parts, xb), Y in zip(gen, Ys):
-            got = Y.cpu().numpy()
-            cols = np.unique(np.concatenate([np.arange(8), np.arange(m.N - 8, m.N),
-                                             rng.choice(m.N, 48, replace=False)]))
-            Yref, A = oracle.verify(lbv.FMT_Q4_0, parts, oracle.x_to_f64(xb[:M], "f16"), m.K,
-                                    m.N, 32, cols=cols)
-            assert np.all(np.abs(got[:M][:, cols] - Yref) <= RTOL * A + ATOL), m.name
-            assert np.all(got[M:] == SENT)

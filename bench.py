@@ -8,7 +8,12 @@ back to back on one stream through the C ABI.  Metric: packed-weight GB/s
 (algorithmic bytes: packed weights + X + Y per call) and us per call, at
 M = 1..8 rows, as a fraction of the measured HBM copy bandwidth.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl lbv|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|NAME] [--impl lbv|reference]
+
+With no --workload every configuration is timed (the rotated output head,
+the 1-bit MLP-up, both 2-bit g64 shapes, the Q4_0 stack per call and as one
+grouped launch); the JSON line's headline is the rotated head and "configs"
+holds one entry per configuration.
 
 N > 1 (under torchrun): independent replicas, one per GPU; no data-path
 collective (the verify path shards by output columns, and each replica here
@@ -35,7 +40,6 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "us/call and packed-weight GB/s at M=1..8 rows, as % of GB300 HBM peak"
-DEFAULT_WORKLOAD = "sign1_mlp_up_5120x17408"
 FMT_IDS = {synth.SIGN1_G128: 0, synth.AFFINE2: 1, synth.Q4_0: 2}
 
 
@@ -45,7 +49,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="lbv", choices=["lbv", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(synth.WORKLOADS),
+                    help="one workload, or all of them (the default; the first, the rotated "
+                         "head, is the headline)")
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M=1..8 table")
     ap.add_argument("--no-pdl", action="store_true")
@@ -79,13 +85,23 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def packed_weight_bytes(mat):
+    """Algorithmic packed bytes of one matrix from its format: 1 bit per
+    weight + an fp16 scale per 128 (sign g128), 2 bits + fp16 scale and bias
+    per group (2-bit affine), 18 bytes per 32 weights (Q4_0)."""
+    K, N = mat.K, mat.N
+    if mat.fmt == synth.SIGN1_G128:
+        return N * K // 8 + N * (K // 128) * 2
+    if mat.fmt == synth.AFFINE2:
+        return N * K // 4 + N * (K // mat.group) * 4
+    return N * (K // 32) * 18
+
+
 def call_bytes(mat, M, head="fused"):
     """Algorithmic bytes of one call: packed weights, X, and Y (or, for the
     greedy head, the argmax column and logit of each row)."""
-    import few_row_packed_gb300 as lbv
-    fmt = FMT_IDS[mat.fmt]
     out = M * 8 if (mat.rotate and head == "greedy") else M * mat.N * 4
-    return lbv.packed_bytes(fmt, mat.K, mat.N, mat.group) + M * mat.K * 2 + out
+    return packed_weight_bytes(mat) + M * mat.K * 2 + out
 
 
 # ---------------------------------------------------------------------------
@@ -149,6 +165,20 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the lbv arm
 
+_GEN = {"workload": None}
+
+
+def gen_cached(workload, mat, seed):
+    """synth.gen_matrix, kept while the configurations of one workload run."""
+    if _GEN["workload"] != workload:
+        _GEN.clear()
+        _GEN["workload"] = workload
+    key = (mat, str(seed))
+    if key not in _GEN:
+        _GEN[key] = synth.gen_matrix(mat, seed)
+    return _GEN[key]
+
+
 class Stack:
     """Distinct packed matrices of a workload resident on the device."""
 
@@ -170,15 +200,15 @@ class Stack:
         self.layers = []
         if len(self.mats) == 1:
             mat = self.mats[0]
-            per = lbv.packed_bytes(FMT_IDS[mat.fmt], mat.K, mat.N, mat.group)
+            per = packed_weight_bytes(mat)
             L = max(64 if per < 100e6 else 3, math.ceil(4 * l2_bytes / per))
             ndistinct = min(L, 4)
-            gens = [synth.gen_matrix(mat, [wl.seed, i]) for i in range(ndistinct)]
+            gens = [gen_cached(workload, mat, [wl.seed, i]) for i in range(ndistinct)]
             mats = [mat] * L
             gen_of = [gens[i % ndistinct] for i in range(L)]
         else:
             mats = self.mats
-            gen_of = [synth.gen_matrix(m, synth.matrix_seed(wl, i)) for i, m in enumerate(mats)]
+            gen_of = [gen_cached(workload, m, synth.matrix_seed(wl, i)) for i, m in enumerate(mats)]
         plans = {}
         packed_cache = {}
         for i, (mat, (parts, xb)) in enumerate(zip(mats, gen_of)):
@@ -217,6 +247,39 @@ class Stack:
         self.idx = torch.zeros(8, dtype=torch.int32, device="cuda")
         self.val = torch.zeros(8, dtype=torch.float32, device="cuda")
         self.ws = torch.zeros(lbv.fused_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+    def shape_desc(self):
+        """The launch shapes the step uses."""
+        if self.group is not None:
+            return [{"warps": 16, "tiles_per_warp": t, "splits": sp, "cluster_rows": r,
+                     "matrices": sum(self.group.problem_launch(i) == c
+                                     for i in range(self.group.count))}
+                    for c in range(self.group.launches())
+                    for t, sp, r in [self.group.shape(c)]]
+        out = []
+        for key, plan in self.plans.items():
+            w, t, sp, ctas = plan.shape()
+            out.append({"K": key[1], "N": key[2], "warps": w, "tiles_per_warp": t, "splits": sp,
+                        "ctas_n": ctas})
+        return out if len(out) > 1 else out[0]
+
+    def dispatch_desc(self):
+        """Per shape, the row-count dispatch the plan chose (LBV_PLAN_MEASURE
+        times the few-row kernel and the 1-row path run M times)."""
+        if self.group is not None:
+            return None
+        import few_row_packed_gb300 as lbv
+        out = []
+        for key, plan in self.plans.items():
+            per = {}
+            crossover = None
+            for M in range(1, 9):
+                few, gemv, crossover = plan.measured(M)
+                kernel = plan.query(M)[0]
+                per[str(M)] = {"kernel": ("1-row" if kernel == lbv.KERNEL_GEMV else "few-row"),
+                               "fewrow_us": round(few, 3), "one_row_times_M_us": round(gemv, 3)}
+            out.append({"K": key[1], "N": key[2], "crossover": crossover, "per_M": per})
+        return out if len(out) > 1 else out[0]
 
     def graph(self, M, verify_only=False):
         """A CUDA graph of one step (launches captured through the C ABI)."""
@@ -466,42 +529,53 @@ def cpu_baseline(workload, M, budget_s=10.0, head="fused"):
     return line
 
 
-def run_lbv(args, rank, world, barrier, reduce_max):
+# The configurations timed by default, in order; the headline line is the
+# first: the rotated output head, the largest single verify call (219 MB of
+# packed weights) and one of the shapes with a 70 % bandwidth target.  The
+# Q4_0 layer stack is larger in all (767 MB) but is 28 calls; it is reported
+# per call and as one grouped launch of its 28 independent problems.
+ALL_CONFIGS = [
+    ("head_rot_affine2_g128_5120x151936", "grouped"),
+    ("sign1_mlp_up_5120x17408", "grouped"),
+    ("affine2_g64_6144x6144", "grouped"),
+    ("affine2_g64_kv_5120x1024", "grouped"),
+    ("q4_0_stack_4x7", "calls"),
+    ("q4_0_stack_4x7", "grouped"),
+]
+
+
+def config_label(workload, stack_mode, multi):
+    if not multi:
+        return workload
+    return (f"{workload} (one verify call per matrix)" if stack_mode == "calls" else
+            f"{workload} (one grouped launch of its independent problems)")
+
+
+def measure_config(args, workload, stack_mode, l2, peak, barrier, reduce_max, world,
+                   headline):
+    """Times one configuration: the step (args.steps steps after args.warmup),
+    the M = 1..8 sweep, and for the headline the end-to-end and dense-GEMM
+    context.  Returns (summary dict, Stack, extra headline fields)."""
     import torch
 
-    import few_row_packed_gb300 as lbv
-    lbv.build()
-    dev = torch.cuda.current_device()
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
-    stack = Stack(args.workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
-                  use_graphs=not args.no_graph, head=args.head, stack=args.stack,
+    stack = Stack(workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
+                  use_graphs=not args.no_graph, head=args.head, stack=stack_mode,
                   measure=not args.no_measure)
     grouped = stack.group is not None
-    kernel_key = "grouped" if grouped else args.kernel
     rotated = any(l[0].rotate for l in stack.layers)
-    greedy = rotated and args.head == "greedy"
-    peak, peak_kind = peaks()
-    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
-
-    # sustained warm-up with clock sampling, then the timed region
-    sampler = ClockSampler(int(phys) if phys.isdigit() else dev)
-    sampler.start()
     stack.run(args.M)
-    t_end = time.time() + (0.0 if args.quick else 1.5)
+    t_end = time.time() + (0.0 if args.quick else 1.0)
     while time.time() < t_end:
         for _ in range(max(1, args.warmup)):
             stack.run(args.M)
         torch.cuda.synchronize()
-    ms = timed(torch, lambda: stack.run(args.M), args.steps, args.warmup, barrier)
-    clocks = sampler.stop()
-    ms = reduce_max(ms)
+    ms = reduce_max(timed(torch, lambda: stack.run(args.M), args.steps, args.warmup, barrier))
     ms_per_step = ms / args.steps
     bytes_step = stack.bytes_per_step[args.M]
     value = replica_value(bytes_step, world, ms_per_step)
 
-    # dominant kernel: the verify launch, timed alone (verify-only loop) when
-    # the step also launches the separate rotation
+    # the dominant kernel: the verify launch, timed alone (verify-only loop)
+    # when the step also launches the separate rotation
     if rotated and args.head == "two-call":
         ms_v = reduce_max(timed(torch, lambda: stack.run(args.M, verify_only=True), args.steps,
                                 args.warmup, barrier))
@@ -511,20 +585,57 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     us_launch = ms_v * 1e3 / (args.steps * verify_launches)
     bytes_launch = bytes_step / verify_launches
     achieved = bytes_launch / (us_launch * 1e-6) / 1e9
-    traffic = recorded_traffic(args.workload, args.M, kernel_key)
 
     per_M = {}
     if not args.no_sweep:
         for M in range(1, 9):
-            msm = reduce_max(timed(torch, lambda: stack.run(M), max(10, args.steps // 4),
-                                   args.warmup, barrier))
-            us = msm * 1e3 / (max(10, args.steps // 4) * stack.calls)
+            n = max(10, args.steps // 2)
+            msm = reduce_max(timed(torch, lambda: stack.run(M), n, args.warmup, barrier))
+            us = msm * 1e3 / (n * stack.calls)
             gbs = stack.bytes_per_step[M] / stack.calls / (us * 1e-6) / 1e9
             per_M[str(M)] = {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
                              "frac_of_measured_hbm": round(gbs / peak, 4)}
 
-    # end to end through the public API with host buffers: per step, X from
-    # pinned host memory to the device, the verify stack, the last Y back
+    multi = len(stack.mats) > 1
+    summary = {
+        "workload": workload,
+        "label": config_label(workload, stack_mode, multi),
+        "M": args.M,
+        "calls_per_step": stack.calls,
+        "us_per_call": round(ms_per_step * 1e3 / stack.calls, 3),
+        "GBps": round(value / world, 1),
+        "frac_of_measured_hbm": round(value / world / peak, 4),
+        "per_M": per_M,
+        "m8_over_m1": (round(per_M["8"]["us_per_call"] / per_M["1"]["us_per_call"], 3)
+                       if per_M else None),
+        "launches_per_step": stack.launches_per_step,
+        "shape": stack.shape_desc(),
+        "dispatch": stack.dispatch_desc(),
+        "head": args.head if rotated else None,
+    }
+    if grouped:
+        summary["note"] = ("one launch over the stack's matrices as independent problems, each "
+                           "with its own X; us_per_call is the launch time divided by the "
+                           "matrices")
+    extra = {"ms_per_step": ms_per_step, "bytes_step": bytes_step, "value": value,
+             "achieved": achieved, "bytes_launch": bytes_launch, "us_launch": us_launch,
+             "grouped": grouped, "rotated": rotated, "kernel_key": "grouped" if grouped else args.kernel}
+    if headline:
+        extra["e2e"] = e2e_measure(args, stack, bytes_step, world, barrier, reduce_max)
+        if not args.no_dense:
+            dense = dense_context(stack, args.M, l2, max(3, args.steps // 4), args.warmup, peak,
+                                  barrier, reduce_max)
+            dense["packed_speedup"] = round(dense["us_per_call"] / (ms_per_step * 1e3 / stack.calls), 2)
+            extra["dense"] = dense
+    return summary, stack, extra
+
+
+def e2e_measure(args, stack, bytes_step, world, barrier, reduce_max):
+    """End to end through the public API with host buffers: per step, X from
+    pinned host memory to the device, the verify stack, the result back."""
+    import torch
+    rotated = any(l[0].rotate for l in stack.layers)
+    greedy = rotated and args.head == "greedy"
     mat0 = stack.layers[0][0]
     x_host = torch.from_numpy(stack.layers[0][3].cpu().numpy()).pin_memory()
     X_dev = stack.layers[0][3]
@@ -550,74 +661,94 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     for _ in range(args.steps):
         e2e_step()
     t_e2e = reduce_max((time.perf_counter() - t0) * 1e3)
-    e2e_val = replica_value(bytes_step, world, t_e2e / args.steps)
+    return {"value": round(replica_value(bytes_step, world, t_e2e / args.steps), 2),
+            "unit": "GB/s", "h2d_bytes_per_step": args.M * mat0.K * 2,
+            "d2h_bytes_per_step": d2h}
 
-    dense = None
-    if not args.no_dense:
-        dense = dense_context(stack, args.M, l2, max(3, args.steps // 4), args.warmup, peak,
-                              barrier, reduce_max)
-        dense["packed_speedup"] = round(dense["us_per_call"] / (ms_per_step * 1e3 / stack.calls), 2)
 
-    shape = next(iter(stack.plans.values())).shape()
+def run_lbv(args, rank, world, barrier, reduce_max):
+    import torch
+
+    import few_row_packed_gb300 as lbv
+    lbv.build()
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    peak, peak_kind = peaks()
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
+    configs = ([(args.workload, args.stack)] if args.workload != "all" else ALL_CONFIGS)
+
+    sampler = ClockSampler(int(phys) if phys.isdigit() else dev)
+    sampler.start()
+    results = []
+    head_summary = head_stack = head_extra = None
+    for i, (workload, stack_mode) in enumerate(configs):
+        summary, stack, extra = measure_config(args, workload, stack_mode, l2, peak, barrier,
+                                               reduce_max, world, headline=(i == 0))
+        results.append(summary)
+        if i == 0:
+            head_summary, head_stack, head_extra = summary, stack, extra
+        else:
+            del stack
+            torch.cuda.empty_cache()
+    clocks = sampler.stop()
+
+    workload = configs[0][0]
+    mat0 = head_stack.layers[0][0]
+    traffic = recorded_traffic(workload, args.M, head_extra["kernel_key"])
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(head_extra["value"], 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 6),
+        "ms_per_step": round(head_extra["ms_per_step"], 6),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16" if mat0.xdtype == "f16" else "bf16",
         "data": "synthetic",
         "config": {
-            "workload": args.workload,
+            "workload": workload,
+            "label": head_summary["label"],
             "M": args.M,
-            "calls_per_step": stack.calls,
-            "us_per_call": round(ms_per_step * 1e3 / stack.calls, 3),
-            "l2": f"inputs larger than L2: {stack.calls} distinct resident matrices, "
-                  f"{bytes_step / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
+            "calls_per_step": head_stack.calls,
+            "us_per_call": head_summary["us_per_call"],
+            "l2": f"inputs larger than L2: {head_stack.calls} distinct resident matrices, "
+                  f"{head_extra['bytes_step'] / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
             "plans": "launch shapes measured at plan creation (LBV_PLAN_MEASURE)"
                      if not (args.no_measure or args.shape) else "default launch shapes",
             "launch": ("CUDA graph of the step, " if not args.no_graph else "") +
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
-            "shape": ([{"warps": 16, "tiles_per_warp": t, "splits": sp, "cluster_rows": r,
-                        "matrices": sum(stack.group.problem_launch(i) == c
-                                        for i in range(stack.group.count))}
-                       for c in range(stack.group.launches())
-                       for t, sp, r in [stack.group.shape(c)]]
-                      if grouped else
-                      {"warps": shape[0], "tiles_per_warp": shape[1], "splits": shape[2],
-                       "ctas_n": shape[3]}),
+            "shape": head_summary["shape"],
             "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
-            "head": args.head if rotated else None,
-            "stack": ((f"grouped: every matrix in {stack.group.launches()} launch(es), one per "
-                       "K split" if grouped else "one verify call per matrix")
-                      if len(stack.mats) > 1 else None),
-            "us_per_step": round(ms_per_step * 1e3, 3),
+            "head": head_summary["head"],
+            "us_per_step": round(head_extra["ms_per_step"] * 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "per_M": per_M,
-        "m8_over_m1": (round(per_M["8"]["us_per_call"] / per_M["1"]["us_per_call"], 3)
-                       if per_M else None),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_kind": peak_kind,
-                     "kernel": ("lbv_verify_grouped_kernel" if grouped else
+        "per_M": head_summary["per_M"],
+        "m8_over_m1": head_summary["m8_over_m1"],
+        "roofline": {"bound": "hbm", "achieved": round(head_extra["achieved"], 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(head_extra["achieved"] / peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": ("lbv_verify_grouped_kernel" if head_extra["grouped"] else
                                 "lbv_tc_kernel" if args.kernel == "tc" else "lbv_verify_kernel"),
-                     "bytes_per_launch": bytes_launch, "us_per_launch": round(us_launch, 3)},
-        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": args.M * mat0.K * 2,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * stack.launches_per_step,
+                     "bytes_per_launch": head_extra["bytes_launch"],
+                     "us_per_launch": round(head_extra["us_launch"], 3)},
+        "e2e": head_extra["e2e"],
+        "gpu_launches": args.steps * head_stack.launches_per_step,
         "clocks": clocks,
-        "dense_fp16_context": dense,
+        "dense_fp16_context": head_extra.get("dense"),
+        "configs": results,
     }
     if rank == 0 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.M, head=args.head)
+        line["cpu_baseline"] = cpu_baseline(workload, args.M, budget_s=10.0, head=args.head)
+        if len(configs) > 1:
+            nthr = line["cpu_baseline"]["host"]["usable"]
+            for r in results[1:]:
+                r["cpu_baseline"] = oracle_sample(r["workload"], args.M, 2.0, args.head, nthr)
     return line
 
 
@@ -627,7 +758,8 @@ def run_reference(args):
     sample (a slice of output columns) of the workload."""
     import oracle
     oracle.build()
-    wl = synth.WORKLOADS[args.workload]
+    workload = ALL_CONFIGS[0][0] if args.workload == "all" else args.workload
+    wl = synth.WORKLOADS[workload]
     mat = wl.matrices[0]
     parts, xb = synth.gen_matrix(mat, synth.matrix_seed(wl, 0))
     M = args.M
@@ -647,14 +779,14 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     sample_bytes = call_bytes(mat, M, args.head) * ncols / mat.N
     gbs = sample_bytes * args.steps / dt / 1e9
-    sample = (f"{ncols} of {mat.N} output columns x {M} rows of {args.workload} per step, "
+    sample = (f"{ncols} of {mat.N} output columns x {M} rows of {workload} per step, "
               f"fp64 oracle on {nthr} threads over column ranges")
     return {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "sample_columns": ncols},
+        "config": {"workload": workload, "M": M, "sample_columns": ncols},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle",
                          "sample": sample, "host": host},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -57,3 +57,33 @@ def test_oracle_over_threads_equals_one_thread(monkeypatch):
     for cols, Yc in got.values():
         Y[:, cols] = Yc
     assert np.array_equal(Y, Y1)
+
+
+def test_packed_bytes_formula_matches_library():
+    """The bench's algorithmic byte counts (from the formats' bits per weight)
+    equal the library's packed sizes on every configuration."""
+    import few_row_packed_gb300 as lbv
+    for wl in synth.WORKLOADS.values():
+        for m in wl.matrices:
+            assert bench.packed_weight_bytes(m) == lbv.packed_bytes(
+                bench.FMT_IDS[m.fmt], m.K, m.N, m.group), m.name
+
+
+def test_reference_arm_does_not_load_the_library():
+    """`bench.py --impl reference` times the oracle alone: the CUDA library's
+    package is never imported."""
+    import json
+    import subprocess
+    import sys
+    code = ("import sys, json, bench\n"
+            "class A: pass\n"
+            "a = A(); a.workload = 'sign1_tiny_512x256'; a.M = 8; a.steps = 1; a.warmup = 0\n"
+            "a.head = 'fused'; a.gpus = 1\n"
+            "line = bench.run_reference(a)\n"
+            "assert 'few_row_packed_gb300' not in sys.modules\n"
+            "print(json.dumps(line))\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=bench.ROOT, capture_output=True,
+                         text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0

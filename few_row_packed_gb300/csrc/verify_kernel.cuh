@@ -111,32 +111,44 @@ __host__ __device__ constexpr DecSpec sign1_spec(int xt, int s)
     }
 }
 
-// 2-bit affine code q at bits 2s: value = q + c.
-//   fp16 targets 4 (64.0, c 64), 6 (16.0, 16), 8 (4.0, 4)
-//   bf16 targets 1 (64.0, 64), 3 (16.0, 16), 5 (4.0, 4)
+// 2-bit affine code q at bits 2s: value = q + c.  A field at mantissa bit j
+// under a base of 2^(m - j) (m = 10 for fp16, 7 for bf16) reads as q + base.
+//   fp16: targets 0, 2, 4, 6, 8 (bases 1024, 256, 64, 16, 4): slots 0-4 in
+//         place, slots 5-7 shifted right by 6 onto 4, 6, 8
+//   bf16: targets 0, 2, 4 (bases 128, 32, 8): slots 0-2 in place, slots 3-5
+//         shifted right by 6 and slots 6-7 by 12 onto them
+// (one shifted copy of a word for fp16, two for bf16)
 __host__ __device__ constexpr DecSpec affine2_spec(int xt, int s)
 {
     if (xt == LBV_F16) {
-        const int sh = (s <= 1) ? 4 : (s <= 4) ? 0 : -6;
+        const int sh = (s <= 4) ? 0 : -6;
         const int j = 2 * s + sh;
-        return j == 4 ? DecSpec{sh, j, 0x5400u, 64, 0}
-               : j == 6 ? DecSpec{sh, j, 0x4C00u, 16, 1}
-                        : DecSpec{sh, j, 0x4400u, 4, 2};
+        return j == 0   ? DecSpec{sh, j, 0x6400u, 1024, 0}
+               : j == 2 ? DecSpec{sh, j, 0x5C00u, 256, 1}
+               : j == 4 ? DecSpec{sh, j, 0x5400u, 64, 2}
+               : j == 6 ? DecSpec{sh, j, 0x4C00u, 16, 3}
+                        : DecSpec{sh, j, 0x4400u, 4, 4};     // j == 8
     } else {
-        const int sh = (s <= 2) ? 1 : (s <= 5) ? -5 : -11;
+        const int sh = (s <= 2) ? 0 : (s <= 5) ? -6 : -12;
         const int j = 2 * s + sh;
-        return j == 1 ? DecSpec{sh, j, 0x4280u, 64, 0}
-               : j == 3 ? DecSpec{sh, j, 0x4180u, 16, 1}
-                        : DecSpec{sh, j, 0x4080u, 4, 2};
+        return j == 0   ? DecSpec{sh, j, 0x4300u, 128, 0}
+               : j == 2 ? DecSpec{sh, j, 0x4200u, 32, 1}
+                        : DecSpec{sh, j, 0x4100u, 8, 2};     // j == 4
     }
 }
 
-// Q4_0 nibble q at bits 4s: value = q + c, one target per dtype.
-//   fp16: target 4, base 64.0, c 64;  bf16: target 3, base 16.0, c 16
+// Q4_0 nibble q at bits 4s: value = q + c.
+//   fp16: targets 0 (base 1024) and 4 (base 64): slots 0-1 in place, slots
+//         2-3 shifted right by 8 onto them (one shifted copy of a word)
+//   bf16: target 0 (base 128): slot s shifted right by 4s
 __host__ __device__ constexpr DecSpec q4_0_spec(int xt, int s)
 {
-    return xt == LBV_F16 ? DecSpec{4 - 4 * s, 4, 0x5400u, 64, 0}
-                         : DecSpec{3 - 4 * s, 3, 0x4180u, 16, 0};
+    if (xt == LBV_F16) {
+        const int sh = s <= 1 ? 0 : -8;
+        return 4 * s + sh == 0 ? DecSpec{sh, 0, 0x6400u, 1024, 0}
+                               : DecSpec{sh, 4, 0x5400u, 64, 1};
+    }
+    return DecSpec{-4 * s, 0, 0x4300u, 128, 0};
 }
 
 template <int FMT>
@@ -147,11 +159,31 @@ __host__ __device__ constexpr DecSpec dec_spec(int xt, int s)
                                      : q4_0_spec(xt, s);
 }
 
-// Distinct XOR bases of a format (kept in registers: one LOP3 per decode).
-template <int FMT>
+// Value of a 16-bit fp16 / bf16 pattern (finite), for the compile-time check
+// below.
+__host__ __device__ constexpr double half_bits_value(int xt, uint32_t h)
+{
+    const int mbits = xt == LBV_F16 ? 10 : 7, ebits = xt == LBV_F16 ? 5 : 8;
+    const int bias = (1 << (ebits - 1)) - 1;
+    const uint32_t mant = h & ((1u << mbits) - 1u);
+    const int e = (int)((h >> mbits) & ((1u << ebits) - 1u));
+    double v = e ? (double)((1u << mbits) + mant) : (double)mant;
+    int p = (e ? e : 1) - bias - mbits;
+    for (; p > 0; --p)
+        v *= 2.0;
+    for (; p < 0; ++p)
+        v *= 0.5;
+    return (h >> 15) ? -v : v;
+}
+
+// Distinct XOR bases of a format and activation dtype (kept in registers:
+// one LOP3 per decode).
+template <int FMT, int XT>
 __host__ __device__ constexpr int num_bases()
 {
-    return FMT == LBV_FMT_SIGN1_G128 ? 8 : FMT == LBV_FMT_AFFINE2 ? 3 : 1;
+    return FMT == LBV_FMT_SIGN1_G128 ? 8
+           : FMT == LBV_FMT_AFFINE2  ? (XT == LBV_F16 ? 5 : 3)
+                                     : (XT == LBV_F16 ? 2 : 1);
 }
 
 template <int FMT>
@@ -165,7 +197,7 @@ __host__ __device__ constexpr uint32_t base_of(int xt, int bid)
 }
 
 template <int FMT, int XT, int S>
-__device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[num_bases<FMT>()])
+__device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[num_bases<FMT, XT>()])
 {
     constexpr DecSpec d = dec_spec<FMT>(XT, S);
     constexpr int W = Traits<FMT, FMT == LBV_FMT_SIGN1_G128 ? 128 : FMT == LBV_FMT_Q4_0 ? 32 : 64>::W;
@@ -181,6 +213,44 @@ __device__ __forceinline__ uint32_t decode(uint32_t w, const uint32_t (&bases)[n
     return r;
 }
 
+
+// Every slot of every decode table, emulated for every code value in both
+// halves of a word: shift, mask, XOR with the slot's base must read as
+// value + c (value = +-1 for a sign bit, q for 2- and 4-bit codes).
+template <int FMT, int XT>
+__host__ __device__ constexpr bool decode_tables_ok()
+{
+    constexpr int W = FMT == LBV_FMT_SIGN1_G128 ? 1 : FMT == LBV_FMT_AFFINE2 ? 2 : 4;
+    constexpr int slots = 16 / W;
+    for (int s = 0; s < slots; ++s) {
+        const DecSpec d = dec_spec<FMT>(XT, s);
+        const uint32_t field = (1u << W) - 1u;
+        const uint32_t mask = (field << d.target) | (field << (d.target + 16));
+        uint32_t base = 0;
+        for (int i = 0; i < 16; ++i)
+            if (dec_spec<FMT>(XT, i).bid == d.bid)
+                base = dec_spec<FMT>(XT, i).base;
+        if (base != d.base || d.bid >= num_bases<FMT, XT>())
+            return false;
+        for (uint32_t q = 0; q <= field; ++q) {
+            const uint32_t w = (q << (W * s)) | (q << (16 + W * s));
+            const uint32_t v = d.shift > 0 ? w << d.shift : d.shift < 0 ? w >> -d.shift : w;
+            const uint32_t r = (v & mask) ^ (base | (base << 16));
+            const double want = (FMT == LBV_FMT_SIGN1_G128 ? (q ? 1.0 : -1.0) : (double)q) + d.c;
+            if (half_bits_value(XT, r & 0xFFFFu) != want || half_bits_value(XT, r >> 16) != want)
+                return false;
+        }
+    }
+    return true;
+}
+
+static_assert(decode_tables_ok<LBV_FMT_SIGN1_G128, LBV_F16>() &&
+                  decode_tables_ok<LBV_FMT_SIGN1_G128, LBV_BF16>() &&
+                  decode_tables_ok<LBV_FMT_AFFINE2, LBV_F16>() &&
+                  decode_tables_ok<LBV_FMT_AFFINE2, LBV_BF16>() &&
+                  decode_tables_ok<LBV_FMT_Q4_0, LBV_F16>() &&
+                  decode_tables_ok<LBV_FMT_Q4_0, LBV_BF16>(),
+              "a decode table slot does not read as value + c");
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -649,7 +719,7 @@ struct VerifyKernel {
                         c.rec + tl * tstride, bytes, bar);
     }
 
-    static constexpr int NB = num_bases<FMT>();
+    static constexpr int NB = num_bases<FMT, XT>();
 
     // One k-tile of every tile of the unit into the chain of its group.  The
     // chains run in the order the k-tile pairs are visited (0, KT/2, 1, ...),
@@ -850,7 +920,7 @@ struct VerifyKernel {
     }
 
     // Per-group corrections of the slice, one warp per chunk:
-    //   corr = -sum_k c_k x_k (Q4_0: -(c + 8) * rowsum), rsum = rowsum.
+    //   corr = -sum_k c_k x_k (Q4_0: -sum_k (c_k + 8) x_k), rsum = rowsum.
     template <int... KP>
     static __device__ __forceinline__ void corr_pairs(std::integer_sequence<int, KP...>,
                                                       uint32_t xa, float (&cs)[T::GPC],
@@ -905,8 +975,8 @@ struct VerifyKernel {
                 rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
                 if (t == 0) {
                     const int gr = cl * T::GPC + i;
-                    if constexpr (FMT == LBV_FMT_Q4_0)
-                        corr[gr * 8 + g] = -(float)(dec_spec<FMT>(XT, 0).c + 8) * rs[i];
+                    if constexpr (FMT == LBV_FMT_Q4_0)        // w = d (q - 8)
+                        corr[gr * 8 + g] = -(cs[i] + 8.f * rs[i]);
                     else
                         corr[gr * 8 + g] = -cs[i];
                     if constexpr (T::AFFINE)

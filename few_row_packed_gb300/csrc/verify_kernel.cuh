@@ -273,22 +273,24 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // D = A.B + C with C in other registers (starts an accumulator chain from
-// initial values without moving them into D first).
+// initial values without moving them into D first; c is the C fragment as
+// one register quad).
 template <int XT>
 __device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                           uint32_t a3, uint32_t b0, uint32_t b1, float c0,
-                                           float c1)
+                                           uint32_t a3, uint32_t b0, uint32_t b1, float4 c)
 {
     if constexpr (XT == LBV_F16) {
         asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
-            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};\n"
+            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
             : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y),
+              "f"(c.z), "f"(c.w));
     } else {
         asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};\n"
+            "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
             : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y),
+              "f"(c.z), "f"(c.w));
     }
 }
 
@@ -630,8 +632,6 @@ struct Geometry {
     // + the X barrier and a flag word (16), the CTA's argmax keys of the fused
     // head (64)
     static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16 + 64;
-    // corrections and row sums per group of the slice
-    static constexpr int CORR_ARRAYS = T::AFFINE ? 2 : 1;
 };
 
 // Bytes between X rows in shared memory: the slice plus 16 bytes, so the 8
@@ -652,7 +652,9 @@ __host__ __device__ inline size_t smem_bytes_for(int cps, int tiles_max, int spl
     using T = Traits<FMT, GROUP>;
     size_t b = G::RING_B + G::BAR_B;
     b += 8 * x_row_stride<FMT, GROUP>(cps);
-    b += (size_t)cps * T::GPC * 8 * 4 * G::CORR_ARRAYS;
+    b += (size_t)cps * T::GPC * 16 * 4;                       // corrections (C quads)
+    if (T::AFFINE)
+        b += (size_t)cps * T::GPC * 8 * 4;                    // row sums
     if (splits > 1)
         b += (size_t)((tiles_max + splits - 1) / splits) * splits * 512u;
     return b;
@@ -728,7 +730,7 @@ struct VerifyKernel {
     template <int HALF, int KTL>
     static __device__ __forceinline__ void ktile(const uint4 (&w)[TPW], uint32_t b0, uint32_t b1,
                                                  const uint32_t (&bases)[NB],
-                                                 const float2 (&init)[NSET],
+                                                 const float4 (&init)[NSET],
                                                  float (&acc)[TPW][NSET][4])
     {
         constexpr int kt = HALF * (T::KT / 2) + KTL;
@@ -743,7 +745,7 @@ struct VerifyKernel {
             const uint32_t a2 = decode<FMT, XT, 2 * KTL + 1>(wa, bases);
             const uint32_t a3 = decode<FMT, XT, 2 * KTL + 1>(wb, bases);
             if constexpr (first)
-                mma16816_c<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1, init[set].x, init[set].y);
+                mma16816_c<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1, init[set]);
             else
                 mma16816<XT>(acc[tl][set], a0, a1, a2, a3, b0, b1);
         }
@@ -755,7 +757,7 @@ struct VerifyKernel {
     static __device__ __forceinline__ void pairs(std::integer_sequence<int, P...>,
                                                  const uint4 (&w)[TPW], uint32_t xa,
                                                  const uint32_t (&bases)[NB],
-                                                 const float2 (&init)[NSET],
+                                                 const float4 (&init)[NSET],
                                                  float (&acc)[TPW][NSET][4])
     {
         (
@@ -813,13 +815,15 @@ struct VerifyKernel {
                                                          float (&y)[TPW][4], int lane)
     {
         const int t = lane & 3;
-        const float* corr_c = corr + cl * T::GPC * 8;
+        const float* corr_c = corr + cl * T::GPC * 16;
         const float* rsum_c = rsum + cl * T::GPC * 8;
         float acc[TPW][NSET][4];
-        float2 init[NSET];                  // each group's correction, rows 2t, 2t + 1
+        // each group's correction as the C fragment of its chain's first MMA:
+        // rows 2t, 2t + 1 for columns g and g + 8, one 16-byte load
+        float4 init[NSET];
 #pragma unroll
         for (int j = 0; j < NSET; ++j)
-            init[j] = *reinterpret_cast<const float2*>(corr_c + j * 8 + 2 * t);
+            init[j] = *reinterpret_cast<const float4*>(corr_c + j * 16 + 4 * t);
         pairs(std::make_integer_sequence<int, T::KT / 4>{}, w, xa + cl * T::CHUNK_K * 2, bases,
               init, acc);
         epilogue(std::make_integer_sequence<int, T::GPC>{}, sd, corr_c, rsum_c, acc, y, t);
@@ -974,11 +978,14 @@ struct VerifyKernel {
                 rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
                 rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
                 if (t == 0) {
+                    // corr holds each group's C fragment: for lane t the quad
+                    // (row 2t, row 2t + 1, row 2t, row 2t + 1)
                     const int gr = cl * T::GPC + i;
-                    if constexpr (FMT == LBV_FMT_Q4_0)        // w = d (q - 8)
-                        corr[gr * 8 + g] = -(cs[i] + 8.f * rs[i]);
-                    else
-                        corr[gr * 8 + g] = -cs[i];
+                    const float c = FMT == LBV_FMT_Q4_0 ? -(cs[i] + 8.f * rs[i])   // w = d (q - 8)
+                                                        : -cs[i];
+                    float* q = corr + gr * 16 + 4 * (g >> 1) + (g & 1);
+                    q[0] = c;
+                    q[2] = c;
                     if constexpr (T::AFFINE)
                         rsum[gr * 8 + g] = rs[i];
                 }
@@ -1040,8 +1047,8 @@ struct VerifyKernel {
         const int RS = x_row_stride<FMT, GROUP>(p.cps);
         const uint32_t xbar = smem_u32(bars) + (uint32_t)(NW * STAGES * 8);
         float* corr = reinterpret_cast<float*>(xs + (size_t)8 * RS);
-        float* rsum = corr + p.cps * T::GPC * 8;
-        float* part = corr + p.cps * T::GPC * 8 * G::CORR_ARRAYS;
+        float* rsum = corr + p.cps * T::GPC * 16;
+        float* part = rsum + (T::AFFINE ? p.cps * T::GPC * 8 : 0);
 
         const uint32_t ring_w = smem_u32(ring) + warp * STAGES * G::SLOT_B;
         const uint32_t bars_w = smem_u32(bars) + warp * STAGES * 8;

@@ -1,5 +1,7 @@
 // aux_kernels.cu -- the blockwise FWHT-128 activation rotation, the 1-row
 // (GEMV) path and the dense fp16 dequant test export.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -212,114 +214,129 @@ cudaError_t launch_dequant(lbv_format fmt, int group, const uint8_t* Wp, int K, 
 }
 
 // ---------------------------------------------------------------------------
-// 1-row path (the plain decode step): one warp per 16-column tile over all of
-// K, fp32 FMAs on the FMA pipe, run once per row.  Each lane decodes the same
-// codes the few-row kernel's lane does; the 4 lanes of a column pair reduce
-// by shuffles.
-
-// Elements k and k + 1 of an X row.  Two 16-bit loads: X need only be 2-byte
-// aligned and ldx may be odd, so a 4-byte load could be misaligned.
-template <int DT>
-__device__ __forceinline__ float2 x_pair(const uint16_t* x, int k)
-{
-    const uint32_t v = (uint32_t)x[k] | ((uint32_t)x[k + 1] << 16);
-    if constexpr (DT == LBV_F16) {
-        return __half22float2(*reinterpret_cast<const __half2*>(&v));
-    } else {
-        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-    }
-}
+// 1-row path (the plain decode step), run once per row on the FMA pipe.  A CTA
+// stages the row of X in shared memory as fp32 (plain 2-byte loads: X need
+// only be 2-byte aligned), then its warps walk 16-column tiles (grid-stride,
+// a warp per tile over all of K).  Per chunk one 16-byte load per lane gives
+// the same codes the few-row kernel's lane reads (columns g and g + 8, k
+// pairs of its fragment); each code meets its activation with one fp32 add
+// or FMA (a sign weight flips the activation's sign bit), the group's scale
+// (and bias times the group's row sum) is applied per group, and the 4 lanes
+// of a column pair reduce by shuffles.
 
 template <int FMT, int DT, int GROUP>
 __global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int row)
 {
     using A = AuxTraits<FMT, GROUP>;
     constexpr int KTG = A::GK / 16;                  // k-tiles per scale group
+    extern __shared__ float xrow[];                  // [nchunks * CK] fp32, zero past K
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int tile = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (tile >= p.ntiles)
-        return;
     const uint16_t* x = reinterpret_cast<const uint16_t*>(p.X) + (size_t)row * p.ldx;
-    float y0 = 0.f, y1 = 0.f;                        // columns g and g + 8
-    for (int chunk = 0; chunk < p.nchunks; ++chunk) {
-        const size_t tc = (size_t)tile * p.nchunks + chunk;
-        const uint8_t* rec = p.W + tc * A::REC;
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
-        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-        const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
+    const int kpad = p.nchunks * A::CK;
+    for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
+        float v = 0.f;
+        if (k < p.K) {
+            if constexpr (DT == LBV_F16)
+                v = __half2float(__ushort_as_half(x[k]));
+            else
+                v = __bfloat162float(__ushort_as_bfloat16(x[k]));
+        }
+        xrow[k] = v;
+    }
+    __syncthreads();
+    const int nwarps = gridDim.x * (blockDim.x >> 5);
+    for (int tile = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < p.ntiles;
+         tile += nwarps) {
+        float y0 = 0.f, y1 = 0.f;                    // columns g and g + 8
+        const uint8_t* rec = p.W + (size_t)tile * p.nchunks * A::REC;
+        for (int chunk = 0; chunk < p.nchunks; ++chunk, rec += A::REC) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 512 + g * (A::SIDE_W * 4));
+            const float* xc = xrow + chunk * A::CK;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            // k-tiles of this half, grouped by scale group
-#pragma unroll
-            for (int kt0 = 0; kt0 < A::KT / 2; kt0 += (KTG < A::KT / 2 ? KTG : A::KT / 2)) {
-                float a0 = 0.f, a1 = 0.f, r = 0.f;   // column g, column g + 8, row sum
+            for (int half = 0; half < 2; ++half) {
                 constexpr int span = KTG < A::KT / 2 ? KTG : A::KT / 2;
 #pragma unroll
-                for (int kk = 0; kk < span; ++kk) {
-                    const int ktl = kt0 + kk;
-                    const int kt = half * (A::KT / 2) + ktl;
+                for (int kt0 = 0; kt0 < A::KT / 2; kt0 += span) {
+                    float a0 = 0.f, a1 = 0.f, r = 0.f;   // column g, column g + 8, row sum
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int s = 2 * ktl + rr;
-                        const int k = chunk * A::CK + 16 * kt + 8 * rr + 2 * t;
-                        float2 xv = make_float2(0.f, 0.f);
-                        if (k < p.K)
-                            xv = x_pair<DT>(x, k);
+                    for (int kk = 0; kk < span; ++kk) {
+                        const int ktl = kt0 + kk;
+                        const int kt = half * (A::KT / 2) + ktl;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float xs = h ? xv.y : xv.x;
-                            const int sh = s * A::W + 16 * h;
-                            const uint32_t c0 = (wv[2 * half] >> sh) & ((1u << A::W) - 1u);
-                            const uint32_t c1 = (wv[2 * half + 1] >> sh) & ((1u << A::W) - 1u);
-                            if constexpr (FMT == LBV_FMT_SIGN1_G128) {
-                                a0 += c0 ? xs : -xs;
-                                a1 += c1 ? xs : -xs;
-                            } else if constexpr (FMT == LBV_FMT_AFFINE2) {
-                                a0 = fmaf((float)c0, xs, a0);
-                                a1 = fmaf((float)c1, xs, a1);
-                                r += xs;
-                            } else {
-                                a0 = fmaf((float)((int)c0 - 8), xs, a0);
-                                a1 = fmaf((float)((int)c1 - 8), xs, a1);
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int s = 2 * ktl + rr;
+                            const float2 xv =
+                                *reinterpret_cast<const float2*>(xc + 16 * kt + 8 * rr + 2 * t);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const float xs = h ? xv.y : xv.x;
+                                const int sh = s * A::W + 16 * h;
+                                const uint32_t w0 = wv[2 * half], w1 = wv[2 * half + 1];
+                                if constexpr (FMT == LBV_FMT_SIGN1_G128) {
+                                    // bit 1 -> +x, bit 0 -> -x: flip the sign bit of x
+                                    const uint32_t xb = __float_as_uint(xs);
+                                    a0 += __uint_as_float(xb ^ ((~w0 << (31 - sh)) & 0x80000000u));
+                                    a1 += __uint_as_float(xb ^ ((~w1 << (31 - sh)) & 0x80000000u));
+                                } else if constexpr (FMT == LBV_FMT_AFFINE2) {
+                                    a0 = fmaf((float)((w0 >> sh) & 3u), xs, a0);
+                                    a1 = fmaf((float)((w1 >> sh) & 3u), xs, a1);
+                                    r += xs;
+                                } else {
+                                    a0 = fmaf((float)((int)((w0 >> sh) & 15u) - 8), xs, a0);
+                                    a1 = fmaf((float)((int)((w1 >> sh) & 15u) - 8), xs, a1);
+                                }
                             }
                         }
                     }
-                }
-                const int gi = (16 * (half * (A::KT / 2) + kt0)) / A::GK;
-                if constexpr (FMT == LBV_FMT_AFFINE2) {
-                    const uint32_t sc = sw[2 * gi], bi = sw[2 * gi + 1];
-                    y0 = fmaf(h2f(side_half(sc, 0)), a0, fmaf(h2f(side_half(bi, 0)), r, y0));
-                    y1 = fmaf(h2f(side_half(sc, 1)), a1, fmaf(h2f(side_half(bi, 1)), r, y1));
-                } else {
-                    const uint32_t sc = sw[gi];
-                    y0 = fmaf(h2f(side_half(sc, 0)), a0, y0);
-                    y1 = fmaf(h2f(side_half(sc, 1)), a1, y1);
+                    const int gi = (16 * (half * (A::KT / 2) + kt0)) / A::GK;
+                    if constexpr (FMT == LBV_FMT_AFFINE2) {
+                        const uint32_t sc = sw[2 * gi], bi = sw[2 * gi + 1];
+                        y0 = fmaf(h2f(side_half(sc, 0)), a0, fmaf(h2f(side_half(bi, 0)), r, y0));
+                        y1 = fmaf(h2f(side_half(sc, 1)), a1, fmaf(h2f(side_half(bi, 1)), r, y1));
+                    } else {
+                        const uint32_t sc = sw[gi];
+                        y0 = fmaf(h2f(side_half(sc, 0)), a0, y0);
+                        y1 = fmaf(h2f(side_half(sc, 1)), a1, y1);
+                    }
                 }
             }
         }
-    }
-    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
-    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
-    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
-    if (t == 0) {
-        const int n0 = tile * 16 + g, n1 = n0 + 8;
-        float* yr = p.Y + (size_t)row * p.ldy;
-        if (n0 < p.N)
-            yr[n0] = y0;
-        if (n1 < p.N)
-            yr[n1] = y1;
+        y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+        y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+        if (t == 0) {
+            const int n0 = tile * 16 + g, n1 = n0 + 8;
+            float* yr = p.Y + (size_t)row * p.ldy;
+            if (n0 < p.N)
+                yr[n0] = y0;
+            if (n1 < p.N)
+                yr[n1] = y1;
+        }
     }
 }
 
 template <int FMT, int GROUP>
 static cudaError_t gemv_t(lbv_dtype xt, const VerifyParams& p, int row, cudaStream_t st)
 {
-    const dim3 grid((unsigned)((p.ntiles + 7) / 8));
+    using A = AuxTraits<FMT, GROUP>;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int ctas = std::min((p.ntiles + 7) / 8, 4 * std::max(sms, 1));
+    const size_t smem = (size_t)p.nchunks * A::CK * sizeof(float);
+    void* k = xt == LBV_F16 ? (void*)lbv_gemv_kernel<FMT, LBV_F16, GROUP>
+                            : (void*)lbv_gemv_kernel<FMT, LBV_BF16, GROUP>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)std::max<size_t>(smem, 48 * 1024));
+    if (e != cudaSuccess)
+        return e;
     if (xt == LBV_F16)
-        lbv_gemv_kernel<FMT, LBV_F16, GROUP><<<grid, 256, 0, st>>>(p, row);
+        lbv_gemv_kernel<FMT, LBV_F16, GROUP><<<ctas, 256, smem, st>>>(p, row);
     else
-        lbv_gemv_kernel<FMT, LBV_BF16, GROUP><<<grid, 256, 0, st>>>(p, row);
+        lbv_gemv_kernel<FMT, LBV_BF16, GROUP><<<ctas, 256, smem, st>>>(p, row);
     return cudaGetLastError();
 }
 

@@ -53,10 +53,14 @@ def padded_x(xb, ldx):
     (synth.Q4_0, 1024, 72, 32, "f16"),
 ])
 @pytest.mark.parametrize("dx,dy", [(8, 0), (3, 5), (1, 16)])
-def test_verify_strided(fmtname, K, N, group, xdtype, dx, dy):
+@pytest.mark.parametrize("flags", [0, lbv.PLAN_FORCE_GEMV])
+def test_verify_strided(fmtname, K, N, group, xdtype, dx, dy, flags):
+    """Odd ldx puts rows >= 1 on 2-byte boundaries: the few-row kernel stages
+    them element-wise and the 1-row path (PLAN_FORCE_GEMV) reads 2-byte
+    elements, so neither makes a misaligned wider load."""
     parts, xb = gen(fmtname, K, N, group, xdtype, K + dx)
     fmt = FMT[fmtname]
-    plan = lbv.Plan(fmt, K, N, group, DT[xdtype])
+    plan = lbv.Plan(fmt, K, N, group, DT[xdtype], flags)
     Wp = dev(lbv.pack(fmt, parts, K, N, group))
     ldx, ldy = K + dx, N + dy
     Xp = padded_x(xb, ldx)

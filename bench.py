@@ -58,8 +58,9 @@ def parse_args():
     ap.add_argument("--no-measure", action="store_true",
                     help="plans without LBV_PLAN_MEASURE (default launch shapes)")
     ap.add_argument("--shape", default="", help="warps,tpw,splits[,ctas] override of the launch shape")
-    ap.add_argument("--kernel", default="mma", choices=["mma", "tc"],
-                    help="few-row kernel: mma.sync (default plans) or tcgen05 (PLAN_TCGEN05)")
+    ap.add_argument("--kernel", default="mma", choices=["mma", "tc", "tc8"],
+                    help="few-row kernel: mma.sync (default plans), tcgen05 with fp16 operands "
+                         "(PLAN_TCGEN05) or tcgen05 with e4m3 operands (PLAN_TC_E4M3)")
     ap.add_argument("--head", default="fused", choices=["fused", "two-call", "greedy"],
                     help="rotated head: rotation fused into the verify launch (default), "
                          "lbv_fwht128 then lbv_verify_gemm, or fused rotation and per-row "
@@ -193,7 +194,8 @@ class Stack:
         import few_row_packed_gb300 as lbv
         wl = synth.WORKLOADS[workload]
         self.mats = list(wl.matrices)
-        flags = (lbv.PLAN_PDL if pdl else 0) | (lbv.PLAN_TCGEN05 if kernel == "tc" else 0)
+        flags = ((lbv.PLAN_PDL if pdl else 0) | (lbv.PLAN_TCGEN05 if kernel == "tc" else 0) |
+                 (lbv.PLAN_TC_E4M3 if kernel == "tc8" else 0))
         # plans are set up once per weight shape, timing their candidate launch
         # shapes and the 1-row crossover (LBV_PLAN_MEASURE)
         mflag = lbv.PLAN_MEASURE if measure else 0

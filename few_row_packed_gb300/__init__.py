@@ -26,9 +26,11 @@ PLAN_FORCE_GEMV = 0x4
 PLAN_PDL = 0x8
 PLAN_TCGEN05 = 0x10
 PLAN_TEST_WAIT_LIMIT = 0x20
+PLAN_TC_E4M3 = 0x40
 KERNEL_FEWROW = 1
 KERNEL_GEMV = 2
 KERNEL_FEWROW_TC = 3
+KERNEL_FEWROW_TC8 = 4
 FUSED_ROTATE = 0x1
 FUSED_ARGMAX = 0x2
 
@@ -187,7 +189,7 @@ def pack_q4_0(blocks, K: int, N: int) -> np.ndarray:
 
 def pack(fmt: int, parts, K: int, N: int, group: int = 128, plan=None) -> np.ndarray:
     """Canonical arrays (as produced for the format) -> device-layout bytes: the
-    default layout, or the layout `plan` reads (needed for PLAN_TCGEN05 plans)."""
+    default layout, or the layout `plan` reads (needed for PLAN_TCGEN05 and PLAN_TC_E4M3 plans)."""
     if plan is not None:
         return plan.pack(parts)
     if fmt == FMT_SIGN1_G128:

@@ -21,6 +21,7 @@ LIB = os.path.join(HERE, "liblbv.so")
 SOURCES = [
     "api.cpp",
     "tc_api.cpp",
+    "t8_api.cpp",
     "aux_kernels.cu",
     "verify_sign1.cu",
     "verify_affine2_g32.cu",
@@ -34,6 +35,8 @@ SOURCES = [
     "tc_affine2_g64.cu",
     "tc_affine2_g128.cu",
     "tc_q4_0.cu",
+    "t8_sign1.cu",
+    "t8_affine2_g128.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",

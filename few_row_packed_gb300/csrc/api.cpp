@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "lbv_internal.h"
+#include "t8_api.h"
 #include "tc_api.h"
 #include "verify_ops.h"
 
@@ -381,12 +382,16 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: both FORCE flags set");
     if ((flags & LBV_PLAN_TCGEN05) && (flags & LBV_PLAN_FORCE_GEMV))
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: TCGEN05 with FORCE_GEMV");
+    if ((flags & LBV_PLAN_TC_E4M3) &&
+        (flags & (LBV_PLAN_TCGEN05 | LBV_PLAN_FORCE_GEMV | LBV_PLAN_TEST_WAIT_LIMIT)))
+        return fail(LBV_ERR_INVALID_ARG,
+                    "lbv_plan_create: TC_E4M3 with TCGEN05, FORCE_GEMV or TEST_WAIT_LIMIT");
     if ((flags & LBV_PLAN_TEST_WAIT_LIMIT) &&
         (flags & (LBV_PLAN_TCGEN05 | LBV_PLAN_FORCE_GEMV | LBV_PLAN_MEASURE)))
         return fail(LBV_ERR_INVALID_ARG,
                     "lbv_plan_create: TEST_WAIT_LIMIT with TCGEN05, FORCE_GEMV or MEASURE");
     if (flags & ~(LBV_PLAN_MEASURE | LBV_PLAN_FORCE_FEWROW | LBV_PLAN_FORCE_GEMV | LBV_PLAN_PDL |
-                  LBV_PLAN_TCGEN05 | LBV_PLAN_TEST_WAIT_LIMIT))
+                  LBV_PLAN_TCGEN05 | LBV_PLAN_TEST_WAIT_LIMIT | LBV_PLAN_TC_E4M3))
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: unknown flags 0x%x", flags);
 
     lbv_plan* P = new (std::nothrow) lbv_plan();
@@ -426,6 +431,13 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         lbv_plan_destroy(P);
         return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_create: no tcgen05 launch shape fits K=%d", K);
     }
+    P->t8 = (flags & LBV_PLAN_TC_E4M3) ? 1 : 0;
+    if (P->t8 && !lbv::t8_plan_setup(P)) {
+        lbv_plan_destroy(P);
+        return fail(LBV_ERR_UNSUPPORTED,
+                    "lbv_plan_create: the e4m3 tensor-memory kernel reads sign1 g128 and affine2 "
+                    "g128 only, and needs a launch shape that fits K=%d", K);
+    }
     for (int m = 0; m <= 8; ++m)
         P->use_gemv[m] = (flags & LBV_PLAN_FORCE_GEMV) ? 1 : 0;
     P->crossover = (flags & LBV_PLAN_FORCE_GEMV) ? 9 : 1;
@@ -455,7 +467,7 @@ size_t lbv_plan_packed_bytes(const lbv_plan* P)
 {
     if (!P)
         return 0;
-    return P->tc ? lbv::tc_packed_bytes(P) : P->layout.total;
+    return P->t8 ? lbv::t8_packed_bytes(P) : P->tc ? lbv::tc_packed_bytes(P) : P->layout.total;
 }
 
 lbv_status lbv_plan_pack(const lbv_plan* P, const void* part0, const void* part1,
@@ -469,6 +481,10 @@ lbv_status lbv_plan_pack(const lbv_plan* P, const void* part0, const void* part1
     const size_t need = lbv_plan_packed_bytes(P);
     if (out_bytes < need)
         return fail(LBV_ERR_WORKSPACE, "lbv_plan_pack: out_bytes %zu < %zu", out_bytes, need);
+    if (P->t8) {
+        lbv::t8_pack(P, part0, part1, part2, static_cast<uint8_t*>(out));
+        return LBV_OK;
+    }
     if (P->tc) {
         lbv::tc_pack(P, part0, part1, part2, static_cast<uint8_t*>(out));
         return LBV_OK;
@@ -513,9 +529,12 @@ lbv_status lbv_plan_query(const lbv_plan* P, int M, int* kernel_id, int* splits,
     if (M < 1 || M > 8)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_query: M=%d outside 1..8", M);
     if (kernel_id)
-        *kernel_id = P->tc ? LBV_KERNEL_FEWROW_TC : P->use_gemv[M] ? LBV_KERNEL_GEMV : LBV_KERNEL_FEWROW;
+        *kernel_id = P->t8 ? LBV_KERNEL_FEWROW_TC8
+                     : P->tc ? LBV_KERNEL_FEWROW_TC
+                     : P->use_gemv[M] ? LBV_KERNEL_GEMV : LBV_KERNEL_FEWROW;
     if (splits)
-        *splits = P->tc ? P->tc_shape.splits : P->use_gemv[M] ? 1 : P->shape.splits;
+        *splits = P->t8 ? P->t8_shape.splits
+                  : P->tc ? P->tc_shape.splits : P->use_gemv[M] ? 1 : P->shape.splits;
     if (workspace_bytes)
         *workspace_bytes = 0;
     return LBV_OK;
@@ -526,6 +545,13 @@ lbv_status lbv_plan_shape(const lbv_plan* P, int* warps, int* tpw, int* splits, 
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_shape: plan is NULL");
+    if (P->t8) {
+        if (warps) *warps = 0;
+        if (tpw) *tpw = 0;
+        if (splits) *splits = P->t8_shape.splits;
+        if (ctas_n) *ctas_n = P->t8_shape.ctas_n;
+        return LBV_OK;
+    }
     if (P->tc) {
         if (warps) *warps = 0;
         if (tpw) *tpw = 0;
@@ -545,6 +571,13 @@ lbv_status lbv_plan_set_shape(lbv_plan* P, int warps, int tpw, int splits, int c
     g_err.clear();
     if (!P)
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: plan is NULL");
+    if (P->t8) {
+        if ((splits != 1 && splits != 2 && splits != 4 && splits != 8) || ctas_n < 0)
+            return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: splits=%d ctas_n=%d", splits, ctas_n);
+        if (!lbv::t8_set_shape(P, splits, ctas_n) || P->t8_shape.splits != splits)
+            return fail(LBV_ERR_UNSUPPORTED, "lbv_plan_set_shape: shape does not fit (smem, occupancy or K)");
+        return LBV_OK;
+    }
     if (P->tc) {
         if (splits < 1 || splits > 8 || ctas_n < 0)
             return fail(LBV_ERR_INVALID_ARG, "lbv_plan_set_shape: splits=%d ctas_n=%d", splits, ctas_n);
@@ -632,6 +665,13 @@ lbv_status lbv_verify_launch_internal(const lbv_plan* P, const void* X, int M, i
                                       cudaStream_t st)
 {
     cudaError_t e;
+    if (P->t8) {
+        const lbv::T8Fused f = {0, 1, nullptr, nullptr, nullptr, nullptr, nullptr};
+        e = lbv::t8_verify_launch(P, X, M, ldx, Wp, Y, ldy, f, (P->flags & LBV_PLAN_PDL) != 0, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "lbv_verify_gemm: launch");
+        return LBV_OK;
+    }
     if (P->tc) {
         e = lbv::tc_verify_launch(P, X, M, ldx, Wp, Y, ldy, (P->flags & LBV_PLAN_PDL) != 0, st);
         if (e != cudaSuccess)
@@ -703,7 +743,7 @@ lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, co
             return fail(LBV_ERR_UNSUPPORTED, "lbv_verify_fused: rotation needs K %% 128 == 0 (K=%d)",
                         P->K);
         const int cps = shape_cps(P->shape, P->layout.nchunks, slice_step(P));
-        if (P->shape.splits > 1 && (cps * P->fi.chunk_k) % 128 != 0)
+        if (!P->t8 && P->shape.splits > 1 && (cps * P->fi.chunk_k) % 128 != 0)
             return fail(LBV_ERR_UNSUPPORTED,
                         "lbv_verify_fused: the plan's K slices (%d elements) are not whole "
                         "128-element blocks", cps * P->fi.chunk_k);
@@ -721,6 +761,22 @@ lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, co
             return fail(LBV_ERR_WORKSPACE,
                         "lbv_verify_fused: argmax needs a 16-byte aligned, zero-initialised "
                         "workspace of %zu bytes", kFusedWorkspace);
+    }
+    if (P->t8) {
+        lbv::T8Fused f = {rotate ? 1 : 0, Y ? 1 : 0, rotate ? signs : nullptr, nullptr, nullptr,
+                          nullptr, nullptr};
+        if (argmax) {
+            f.amax_keys = static_cast<unsigned long long*>(workspace);
+            f.amax_done = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(workspace) + 64);
+            f.amax_idx = argmax_idx;
+            f.amax_val = argmax_val;
+        }
+        const cudaError_t e = lbv::t8_verify_launch(P, X, M, ldx, Wp, Y, Y ? ldy : P->N, f,
+                                                    (P->flags & LBV_PLAN_PDL) != 0,
+                                                    reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "lbv_verify_fused: launch");
+        return LBV_OK;
     }
     lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, Y ? ldy : P->N);
     p.rot = rotate ? 1 : 0;
@@ -826,7 +882,8 @@ lbv_status lbv_dequant_fp16(const lbv_plan* P, const void* Wp, uint16_t* W, lbv_
     if ((reinterpret_cast<uintptr_t>(Wp) & 15u) != 0 || (reinterpret_cast<uintptr_t>(W) & 1u))
         return fail(LBV_ERR_INVALID_ARG, "lbv_dequant_fp16: misaligned pointer");
     cudaError_t e =
-        P->tc ? lbv::tc_dequant(P, Wp, W, reinterpret_cast<cudaStream_t>(stream))
+        P->t8 ? lbv::t8_dequant(P, Wp, W, reinterpret_cast<cudaStream_t>(stream))
+        : P->tc ? lbv::tc_dequant(P, Wp, W, reinterpret_cast<cudaStream_t>(stream))
               : lbv::launch_dequant(P->fmt, P->group, static_cast<const uint8_t*>(Wp), P->K, P->N,
                                     (int)P->layout.ntiles, (int)P->layout.nchunks, W,
                                     reinterpret_cast<cudaStream_t>(stream));
@@ -978,6 +1035,36 @@ lbv_status lbv_plan_measure_internal(lbv_plan* P)
     cudaStream_t st = nullptr;
     const int reps = 7;
 
+    if (P->t8) {
+        // e4m3 tensor-memory plans: every K split that fits; the kernel serves every M
+        lbv::T8Shape best = P->t8_shape;
+        float best_us = 1e30f;
+        for (int sp = 1; sp <= 8; sp <<= 1) {
+            if (!lbv::t8_set_shape(P, sp, 0) || P->t8_shape.splits != sp)
+                continue;
+            float us = 0.f;
+            lbv_status rc = time_cold(
+                [&] { return lbv_verify_launch_internal(P, s.x, 8, P->K, s.w, s.y, P->N, false, st); },
+                s, st, reps, &us);
+            if (rc != LBV_OK)
+                return rc;
+            if (us < best_us) {
+                best_us = us;
+                best = P->t8_shape;
+            }
+        }
+        P->t8_shape = best;
+        for (int m = 1; m <= 8; ++m) {
+            float few = 0.f;
+            lbv_status rc = time_cold(
+                [&] { return lbv_verify_launch_internal(P, s.x, m, P->K, s.w, s.y, P->N, false, st); },
+                s, st, reps, &few);
+            if (rc != LBV_OK)
+                return rc;
+            P->measured_us[m][0] = few;
+        }
+        return LBV_OK;
+    }
     if (P->tc) {
         // tcgen05 plans: every K split that fits; the kernel serves every M
         lbv::TcShape best = P->tc_shape;

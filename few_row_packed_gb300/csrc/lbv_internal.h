@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "layout.h"
+#include "t8_layout.h"
 #include "tc_layout.h"
 
 namespace lbv {
@@ -150,4 +151,9 @@ struct lbv_plan {
     lbv::TcFmtInfo tc_fi;
     lbv::TcLayout tc_layout;
     lbv::TcShape tc_shape;
+    // plans created with LBV_PLAN_TC_E4M3: the e4m3 tensor-memory kernel and its layout
+    int t8;
+    lbv::T8FmtInfo t8_fi;
+    lbv::T8Layout t8_layout;
+    lbv::T8Shape t8_shape;
 };

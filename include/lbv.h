@@ -93,6 +93,19 @@ typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
                                       layout: pack with lbv_plan_pack and size
                                       buffers with lbv_plan_packed_bytes.  Not
                                       combinable with LBV_PLAN_FORCE_GEMV. */
+#define LBV_PLAN_TC_E4M3      0x40u /* use the e4m3 tensor-memory kernel for every M
+                                      (1-bit sign g128 and 2-bit affine g128
+                                      only, K % 128 == 0; LBV_ERR_UNSUPPORTED
+                                      otherwise): weights decoded to e4m3 bytes
+                                      in tensor memory, the activations split
+                                      exactly into three e4m3 terms per row,
+                                      tcgen05.mma kind::f8f6f4, fp32
+                                      accumulation.  Such a plan reads its own
+                                      device layout: pack with lbv_plan_pack and
+                                      size buffers with lbv_plan_packed_bytes.
+                                      Not combinable with LBV_PLAN_TCGEN05,
+                                      LBV_PLAN_FORCE_GEMV or
+                                      LBV_PLAN_TEST_WAIT_LIMIT. */
 #define LBV_PLAN_TEST_WAIT_LIMIT 0x20u /* test only: the few-row kernel's waits
                                       on its weight stages give up after 256
                                       tries, and the first warp of the first
@@ -110,6 +123,7 @@ typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
 #define LBV_KERNEL_FEWROW    1     /* mma.sync few-row kernel (default)       */
 #define LBV_KERNEL_GEMV      2     /* 1-row path, run once per row           */
 #define LBV_KERNEL_FEWROW_TC 3     /* tcgen05 few-row kernel (LBV_PLAN_TCGEN05) */
+#define LBV_KERNEL_FEWROW_TC8 4    /* e4m3 tensor-memory kernel (LBV_PLAN_TC_E4M3) */
 
 typedef struct lbv_plan lbv_plan;   /* opaque, library-owned */
 
@@ -170,8 +184,9 @@ LBV_API lbv_status lbv_plan_destroy(lbv_plan* plan);
 /* Size in bytes of the device layout the plan's kernels read: equal to
  * lbv_packed_bytes() of the plan's shape, except for LBV_PLAN_TCGEN05 plans,
  * whose layout is one record per (128-column tile, K chunk) (128 K for sign1
- * and affine2 g128, 64 K otherwise), padded with zero codes and scales.
- * 0 for a NULL plan. */
+ * and affine2 g128, 64 K otherwise), padded with zero codes and scales, and
+ * LBV_PLAN_TC_E4M3 plans, whose layout is one record per (128-column tile,
+ * 32-column quarter, 128-K group), padded the same way.  0 for a NULL plan. */
 LBV_API size_t lbv_plan_packed_bytes(const lbv_plan* plan);
 
 /* Packs canonical host arrays into the plan's device layout (host buffer of
@@ -183,7 +198,8 @@ LBV_API lbv_status lbv_plan_pack(const lbv_plan* plan, const void* part0, const 
                                  const void* part2, void* out, size_t out_bytes);
 
 /* For a row count M (1..8): the kernel that lbv_verify_gemm will launch
- * (LBV_KERNEL_FEWROW, LBV_KERNEL_GEMV or LBV_KERNEL_FEWROW_TC), its K split (cluster size) and the
+ * (LBV_KERNEL_FEWROW, LBV_KERNEL_GEMV, LBV_KERNEL_FEWROW_TC or LBV_KERNEL_FEWROW_TC8), its K
+ * split (cluster size) and the
  * workspace it needs (always 0 in this build).  Any output may be NULL. */
 LBV_API lbv_status lbv_plan_query(const lbv_plan* plan, int M, int* kernel_id, int* splits,
                           size_t* workspace_bytes);
@@ -201,7 +217,8 @@ LBV_API lbv_status lbv_plan_shape(const lbv_plan* plan, int* warps, int* tiles_p
  * For tuning sweeps; not thread-safe against concurrent verify calls.
  * LBV_PLAN_TCGEN05 plans report warps = tiles_per_warp = 0 and ignore both
  * on input (their kernel has a fixed CTA: three decode warpgroups and one
- * MMA warp each). */
+ * MMA warp each); so do LBV_PLAN_TC_E4M3 plans (four warpgroups of four
+ * decode warps and one MMA warp each), whose splits must be 1, 2, 4 or 8. */
 LBV_API lbv_status lbv_plan_set_shape(lbv_plan* plan, int warps, int tiles_per_warp, int splits,
                               int ctas_n);
 
@@ -287,7 +304,8 @@ LBV_API size_t lbv_fused_workspace_bytes(void);
  * Errors: LBV_ERR_INVALID_ARG as lbv_verify_gemm, for unknown ops bits, for
  * no output (Y NULL without LBV_FUSED_ARGMAX), for argmax_idx NULL with
  * LBV_FUSED_ARGMAX and for misaligned signs, argmax_idx or argmax_val;
- * LBV_ERR_UNSUPPORTED for LBV_PLAN_TCGEN05 plans, for the rotation with
+ * LBV_ERR_UNSUPPORTED for LBV_PLAN_TCGEN05 plans (LBV_PLAN_TC_E4M3 plans
+ * support every op), for the rotation with
  * K % 128 != 0 or with K slices of the plan's launch shape that are not
  * whole 128-element blocks.  If a bounded wait in the kernel gives up, the
  * plan's device status records it (lbv_plan_device_status) and argmax_idx

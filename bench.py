@@ -434,8 +434,8 @@ def kernel_hash():
 
 def recorded_traffic(workload, M, kernel):
     """DRAM bytes per verify launch from the committed ncu capture of this
-    workload and kernel ("mma" or "tc"), if it was taken on the current
-    kernel sources."""
+    workload and kernel ("mma", "tc", "tc8" or "grouped"), if it was taken on
+    the current kernel sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
@@ -725,7 +725,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                       ("programmatic dependent launch, " if not args.no_pdl else "") +
                       "back to back on one stream",
             "shape": head_summary["shape"],
-            "kernel": "tcgen05" if args.kernel == "tc" else "mma.sync",
+            "kernel": {"tc": "tcgen05 (fp16 operands)", "tc8": "tcgen05 (e4m3 operands)"}.get(
+                args.kernel, "mma.sync"),
             "head": head_summary["head"],
             "us_per_step": round(head_extra["ms_per_step"] * 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -736,7 +737,8 @@ def run_lbv(args, rank, world, barrier, reduce_max):
                      "unit": "GB/s", "frac": round(head_extra["achieved"] / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": ("lbv_verify_grouped_kernel" if head_extra["grouped"] else
-                                "lbv_tc_kernel" if args.kernel == "tc" else "lbv_verify_kernel"),
+                                {"tc": "lbv_tc_kernel", "tc8": "lbv_t8_kernel"}.get(
+                                    args.kernel, "lbv_verify_kernel")),
                      "bytes_per_launch": head_extra["bytes_launch"],
                      "us_per_launch": round(head_extra["us_launch"], 3)},
         "e2e": head_extra["e2e"],

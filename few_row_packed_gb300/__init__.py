@@ -27,7 +27,6 @@ PLAN_PDL = 0x8
 PLAN_TCGEN05 = 0x10
 PLAN_TEST_WAIT_LIMIT = 0x20
 PLAN_TC_E4M3 = 0x40
-PLAN_X_SHARE = 0x80
 KERNEL_FEWROW = 1
 KERNEL_GEMV = 2
 KERNEL_FEWROW_TC = 3

@@ -108,7 +108,7 @@ size_t tile_chunk_bytes(const lbv_plan* P)
 // splits) choice: one cluster of `splits` CTAs per `splits` SMs, as many
 // clusters as can be resident at once, each owning a contiguous tile range.
 // ctas_req > 0 caps the number of clusters.  Returns false if nothing fits.
-bool complete_shape_as(const lbv_plan* P, lbv::Shape& sh, int ctas_req, bool share)
+bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
 {
     const lbv::VerifyOps* ops = ops_for(P->fmt, P->group);
     finish_shape(sh, P->layout.nchunks, slice_step(P));
@@ -117,11 +117,6 @@ bool complete_shape_as(const lbv_plan* P, lbv::Shape& sh, int ctas_req, bool sha
     int64_t G = std::max<int64_t>(1, std::min<int64_t>(ntiles, P->sms / sh.splits));
     if (ctas_req > 0)
         G = std::min<int64_t>(G, ctas_req);
-    // X-sharing pairs: no K split, an even number of CTAs along N, and a
-    // slice of at least two 128-element blocks
-    const int xunit = P->fi.chunk_k >= 128 ? 1 : 128 / P->fi.chunk_k;
-    sh.xshare = (share && sh.splits == 1 && G >= 2 && G % 2 == 0 &&
-                 P->layout.nchunks >= 2 * xunit) ? 1 : 0;
     for (int it = 0; it < 4; ++it) {
         const int tiles_max = (int)((ntiles + G - 1) / G);
         sh.smem = std::max(ops->smem(sh.warps, sh.tpw, cps, tiles_max, sh.splits), kSmemOnePerSm);
@@ -131,7 +126,7 @@ bool complete_shape_as(const lbv_plan* P, lbv::Shape& sh, int ctas_req, bool sha
         if (ops->prepare(P->xdtype, sh) != cudaSuccess)
             return false;
         const int maxc = ops->max_clusters(P->xdtype, sh);
-        if (maxc < (sh.xshare ? 2 : 1))
+        if (maxc < 1)
             return false;
         if (G <= maxc)
             return true;
@@ -141,18 +136,6 @@ bool complete_shape_as(const lbv_plan* P, lbv::Shape& sh, int ctas_req, bool sha
                        kSmemOnePerSm);
     sh.ctas_n = (int)G;
     return ops->prepare(P->xdtype, sh) == cudaSuccess;
-}
-
-// X sharing is used wherever it applies on plans created with
-// LBV_PLAN_X_SHARE; a shape whose pairs cannot be resident falls back to
-// unpaired CTAs.
-bool complete_shape(const lbv_plan* P, lbv::Shape& sh, int ctas_req)
-{
-    const lbv::Shape in = sh;
-    if ((P->flags & LBV_PLAN_X_SHARE) && complete_shape_as(P, sh, ctas_req, true))
-        return true;
-    sh = in;
-    return complete_shape_as(P, sh, ctas_req, false);
 }
 
 // Default launch shape: 16 warps of two-tile units; the K split that
@@ -408,8 +391,7 @@ lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xd
         return fail(LBV_ERR_INVALID_ARG,
                     "lbv_plan_create: TEST_WAIT_LIMIT with TCGEN05, FORCE_GEMV or MEASURE");
     if (flags & ~(LBV_PLAN_MEASURE | LBV_PLAN_FORCE_FEWROW | LBV_PLAN_FORCE_GEMV | LBV_PLAN_PDL |
-                  LBV_PLAN_TCGEN05 | LBV_PLAN_TEST_WAIT_LIMIT | LBV_PLAN_TC_E4M3 |
-                  LBV_PLAN_X_SHARE))
+                  LBV_PLAN_TCGEN05 | LBV_PLAN_TEST_WAIT_LIMIT | LBV_PLAN_TC_E4M3))
         return fail(LBV_ERR_INVALID_ARG, "lbv_plan_create: unknown flags 0x%x", flags);
 
     lbv_plan* P = new (std::nothrow) lbv_plan();
@@ -674,7 +656,6 @@ static lbv::VerifyParams make_params(const lbv_plan* P, const void* X, int M, in
     p.amax_done = nullptr;
     p.amax_idx = nullptr;
     p.amax_val = nullptr;
-    p.xshare = P->shape.xshare;
     return p;
 }
 

@@ -34,7 +34,6 @@ struct VerifyParams {
     unsigned* amax_done;    // workspace: CTAs finished with their keys
     int* amax_idx;          // [M] argmax column of each row
     float* amax_val;        // [M] its logit (NULL: not written)
-    int xshare;             // 1: CTAs pair up along N (clusters of 2) to stage X once
 };
 
 // Grouped verify: one problem of the launch (a compact VerifyParams).
@@ -68,7 +67,6 @@ struct Shape {
     int splits;             // K slices (cluster size), 1..8
     int ctas_n;             // clusters along N (grid y); each owns a contiguous tile range
     size_t smem;            // dynamic shared memory bytes
-    int xshare;             // 1: splits == 1 and CTAs pair up along N (X staged once per pair)
 };
 
 // Dynamic shared-memory limit set on every few-row kernel function: the

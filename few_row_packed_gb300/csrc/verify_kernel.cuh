@@ -384,67 +384,6 @@ __device__ __forceinline__ void bulk_g2s_if(uint32_t pred, uint32_t dst, const v
                  : "memory");
 }
 
-// 1-D bulk copy from this CTA's shared memory into a peer CTA's (dst and bar
-// are shared::cluster addresses of the peer), completion on the peer's bar.
-__device__ __forceinline__ void bulk_s2peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
-        ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t mapa_peer(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cta_rank_in_cluster()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n"
-                 ::"r"(cluster_addr)
-                 : "memory");
-}
-
-// Bounded wait with cluster-scope acquire (an arrival from a peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster_scope(uint32_t bar, uint32_t parity,
-                                                        uint32_t limit = 1u << 20)
-{
-    for (uint32_t i = 0; i < limit; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok)
-            return true;
-        if (i >= 4096u)
-            __nanosleep(1000);
-    }
-    return false;
-}
-
 __device__ __forceinline__ void fence_proxy_async_if(uint32_t pred)
 {
     asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
@@ -691,9 +630,8 @@ struct Geometry {
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr size_t RING_B = (size_t)NW * STAGES * SLOT_B;
     // + the X barrier and a flag word (16), the CTA's argmax keys of the fused
-    // head (64), the barriers of an X-sharing pair (16: the peer's half
-    // landed, the peer took this CTA's half)
-    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16 + 64 + 16;
+    // head (64)
+    static constexpr size_t BAR_B = (size_t)NW * STAGES * 8 + 16 + 64;
 };
 
 // Bytes between X rows in shared memory: the slice plus 16 bytes, so the 8
@@ -957,32 +895,29 @@ struct VerifyKernel {
     // threads copy it with plain loads.  Rows >= M are left as they are: they
     // only reach output columns >= M, which are never stored.
     static __device__ __forceinline__ bool stage_x(const VerifyParams& p, unsigned char* xs, int RS,
-                                                   uint32_t xbar, int c0, int ca, int cb)
+                                                   uint32_t xbar, int c0, int nch)
     {
-        // chunks [ca, cb) of the slice: K values [kb, kb + span), of which
-        // `have` lie inside K
-        const int kb = (c0 + ca) * T::CHUNK_K;
-        const int span = (cb - ca) * T::CHUNK_K;
-        const int have = max(0, min(span, p.K - kb));        // K % 16 == 0
-        unsigned char* xr = xs + (size_t)ca * T::CHUNK_K * 2;
+        const int kb = c0 * T::CHUNK_K;
+        const int span = nch * T::CHUNK_K;                   // elements per row slice
+        const int have = min(span, p.K - kb);                // elements inside K (K % 16 == 0)
         const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
         if (p.x_vec) {
             if (threadIdx.x == 0) {
                 mbar_expect_tx(xbar, (uint32_t)(p.M * have * 2));
-                for (int m = 0; m < p.M && have > 0; ++m)
-                    bulk_g2s_if(1u, smem_u32(xr + (size_t)m * RS), X + (size_t)m * p.ldx + kb,
+                for (int m = 0; m < p.M; ++m)
+                    bulk_g2s_if(1u, smem_u32(xs + (size_t)m * RS), X + (size_t)m * p.ldx + kb,
                                 (uint32_t)(have * 2), xbar);
             }
             const int tail = (span - have) / 8;              // 16-byte pieces past K, per row
             for (int i = threadIdx.x; i < p.M * tail; i += NW * 32) {
                 const int m = i / tail, k8 = have + (i - m * tail) * 8;
-                *reinterpret_cast<uint4*>(xr + (size_t)m * RS + k8 * 2) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(xs + (size_t)m * RS + k8 * 2) = make_uint4(0u, 0u, 0u, 0u);
             }
             return true;
         }
         for (int i = threadIdx.x; i < p.M * span; i += NW * 32) {
             const int m = i / span, k = i - m * span;
-            reinterpret_cast<uint16_t*>(xr + (size_t)m * RS)[k] =
+            reinterpret_cast<uint16_t*>(xs + (size_t)m * RS)[k] =
                 k < have ? X[(size_t)m * p.ldx + kb + k] : (uint16_t)0;
         }
         return false;
@@ -1026,10 +961,10 @@ struct VerifyKernel {
     }
 
     static __device__ __forceinline__ void corrections(uint32_t xs_a, int RS, float* corr, float* rsum,
-                                                       int ca, int cb, int warp, int lane)
+                                                       int nch, int warp, int lane)
     {
         const int g = lane >> 2, t = lane & 3;
-        for (int cl = ca + warp; cl < cb; cl += NW) {
+        for (int cl = warp; cl < nch; cl += NW) {
             float cs[T::GPC], rs[T::GPC];
 #pragma unroll
             for (int i = 0; i < T::GPC; ++i)
@@ -1105,22 +1040,12 @@ struct VerifyKernel {
         const int nch = min(p.cps, p.nchunks - c0);          // >= 1 (host guarantees)
         const int t0 = (int)(((unsigned)p.ntiles * cy) / ny);
         const int t1 = (int)(((unsigned)p.ntiles * (cy + 1)) / ny);
-        // X-sharing pair (p.xshare, no K split): the two CTAs of a cluster along
-        // N stage, rotate and correct chunks [0, nA) and [nA, nch) of the slice
-        // (whole 128-element blocks) and push their half into the peer
-        const int xsh = p.xshare;
-        const int pr = xsh ? (int)cta_rank_in_cluster() : 0;
-        constexpr int XUNIT = T::CHUNK_K >= 128 ? 1 : 128 / T::CHUNK_K;
-        const int nA = xsh ? min(nch, ((nch + 1) / 2 + XUNIT - 1) / XUNIT * XUNIT) : nch;
-        const int ca = pr ? nA : 0, cb = pr ? nch : nA;      // this CTA's chunks
-        const int np = xsh ? (pr ? nA : nch - nA) : 0;       // the peer's chunk count
 
         unsigned char* ring = smem;
         unsigned char* bars = ring + G::RING_B;
         unsigned char* xs = bars + G::BAR_B;
         const int RS = x_row_stride<FMT, GROUP>(p.cps);
         const uint32_t xbar = smem_u32(bars) + (uint32_t)(NW * STAGES * 8);
-        const uint32_t xpeer = xbar + 80, xack = xbar + 88;  // the pair's barriers
         float* corr = reinterpret_cast<float*>(xs + (size_t)8 * RS);
         float* rsum = corr + p.cps * T::GPC * 16;
         float* part = rsum + (T::AFFINE ? p.cps * T::GPC * 8 : 0);
@@ -1143,17 +1068,9 @@ struct VerifyKernel {
 #pragma unroll 1
             for (int s = 0; s < STAGES; ++s)
                 mbar_init(bars_w + s * 8, 1);
-            if (warp == 0) {
+            if (warp == 0)
                 mbar_init(xbar, 1);
-                if (xsh) {
-                    mbar_init(xpeer, 1);
-                    mbar_init(xack, 1);
-                }
-            }
             mbar_init_fence();
-            if (warp == 0 && xsh)                    // arm the receipt of the peer's half
-                mbar_expect_tx(xpeer, (uint32_t)(np * (p.M * T::CHUNK_K * 2 + T::GPC * 16 * 4 +
-                                                       (T::AFFINE ? T::GPC * 8 * 4 : 0))));
         }
         __syncwarp();
 
@@ -1192,59 +1109,30 @@ struct VerifyKernel {
         }
 
         griddep_wait();
-        const bool x_async = stage_x(p, xs, RS, xbar, c0, ca, cb);
+        const bool x_async = stage_x(p, xs, RS, xbar, c0, nch);
 #pragma unroll 1
         for (; lq < npre; ++lq) {
             issue(lcur, tstride, leader && lq != skip_q, ring_w, bars_w, lq);
             cursor_next(p, t0, t1, c0, nch, nstage, lcur);
         }
         __syncthreads();               // X barrier initialised, tails zeroed (or X copied)
-        if (xsh)
-            cluster_arrive_release();  // the pair's barriers initialised and armed
         bool x_ok = true;
         if (x_async && !mbar_try(xbar, 0) && !mbar_wait(xbar, 0))
             x_ok = false;
         const uint32_t xs_a = smem_u32(xs);
         if (p.rot) {
             // every thread's wait on X has ended before X is rewritten
-            const int kb = (c0 + ca) * T::CHUNK_K;
-            const int have = max(0, min((cb - ca) * T::CHUNK_K, p.K - kb));
+            const int kb = c0 * T::CHUNK_K, have = min(nch * T::CHUNK_K, p.K - kb);
             if (__syncthreads_and(x_ok)) {
                 if (p.signs) {
-                    flip_signs(p.signs, xs + (size_t)ca * T::CHUNK_K * 2, RS, p.M, kb, have,
-                               threadIdx.x, NW * 32);
+                    flip_signs(p.signs, xs, RS, p.M, kb, have, threadIdx.x, NW * 32);
                     __syncthreads();
                 }
-                rotate_x<XT>(xs_a + (uint32_t)(ca * T::CHUNK_K * 2), RS, have / 128, warp, NW, lane);
+                rotate_x<XT>(xs_a, RS, have / 128, warp, NW, lane);
             }
             __syncthreads();
         }
-        corrections(xs_a, RS, corr, rsum, ca, cb, warp, lane);
-        if (xsh) {
-            // push this CTA's rows, corrections and row sums into the peer, take
-            // the peer's, and tell the peer its copies landed
-            fence_proxy_async_smem();  // generic writes of this half before the bulk engine reads it
-            __syncthreads();
-            cluster_wait_acquire();    // the peer runs, its barriers armed
-            const uint32_t peer = (uint32_t)(pr ^ 1);
-            if (threadIdx.x == 0 && cb > ca) {
-                const uint32_t rbar = mapa_peer(xpeer, peer);
-                for (int m = 0; m < p.M; ++m) {
-                    const uint32_t src = smem_u32(xs + (size_t)m * RS + (size_t)ca * T::CHUNK_K * 2);
-                    bulk_s2peer(mapa_peer(src, peer), src, (uint32_t)((cb - ca) * T::CHUNK_K * 2), rbar);
-                }
-                const uint32_t cs = smem_u32(corr + ca * T::GPC * 16);
-                bulk_s2peer(mapa_peer(cs, peer), cs, (uint32_t)((cb - ca) * T::GPC * 16 * 4), rbar);
-                if constexpr (T::AFFINE) {
-                    const uint32_t rs = smem_u32(rsum + ca * T::GPC * 8);
-                    bulk_s2peer(mapa_peer(rs, peer), rs, (uint32_t)((cb - ca) * T::GPC * 8 * 4), rbar);
-                }
-            }
-            const bool got = mbar_try(xpeer, 0) || mbar_wait(xpeer, 0);
-            x_ok = __syncthreads_and(x_ok && got);
-            if (threadIdx.x == 0)
-                mbar_arrive_peer(mapa_peer(xack, peer));
-        }
+        corrections(xs_a, RS, corr, rsum, nch, warp, lane);
         __syncthreads();
         if (S > 1)
             cluster_wait();            // all peers run: their partial buffers are live
@@ -1332,8 +1220,6 @@ struct VerifyKernel {
                     mbar_wait(bars_w + (r % STAGES) * 8, (uint32_t)((r / STAGES) & 1));
             if (x_async && !x_ok)
                 mbar_wait(xbar, 0);
-            if (xsh && !x_ok)
-                mbar_wait(xpeer, 0);
         }
 
         if (S == 1 && p.amax_keys) {                          // the warp's keys into the CTA's
@@ -1350,9 +1236,6 @@ struct VerifyKernel {
             cluster_reduce(p, part, t0, t1, akeys);
         if (p.amax_keys)
             amax_finish(p, akeys, reinterpret_cast<unsigned*>(bars + NW * STAGES * 8 + 8));
-        // the peer has taken this CTA's half before its shared memory goes away
-        if (xsh && threadIdx.x == 0 && !mbar_wait_cluster_scope(xack, 0))
-            atomicOr(p.err, 1u);
     }
 
     // After the cluster barrier each CTA sums, in rank order 0..S-1, the
@@ -1451,7 +1334,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     p.amax_done = nullptr;
     p.amax_idx = nullptr;
     p.amax_val = nullptr;
-    p.xshare = 0;
     constexpr int SC = stage_chunks<FMT, GROUP, TPW>();
     VerifyKernel<FMT, XT, GROUP, NW, TPW, SC>::run(p, smem, y - gp.ybegin[lo],
                                                    gp.ybegin[lo + 1] - gp.ybegin[lo]);
@@ -1505,10 +1387,10 @@ inline void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2],
     cfg.dynamicSmemBytes = sh.smem;
     cfg.stream = st;
     unsigned na = 0;
-    if (sh.splits > 1 || sh.xshare) {
+    if (sh.splits > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = (unsigned)sh.splits;
-        attr[na].val.clusterDim.y = sh.xshare ? 2u : 1u;   // an X-sharing pair along N
+        attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
@@ -1571,13 +1453,13 @@ inline int max_clusters_t(const Shape& sh, bool grouped = false)
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     Shape s1 = sh;
-    s1.ctas_n = sh.xshare ? 2 : 1;
+    s1.ctas_n = 1;
     fill_config(cfg, attr, s1, false, nullptr);
     int n = 0;
-    if (sh.splits > 1 || sh.xshare) {
+    if (sh.splits > 1) {
         if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess)
             return 0;
-        return sh.xshare ? 2 * n : n;                     // X-sharing pairs: CTAs along N
+        return n;
     }
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, sh.warps * 32, sh.smem) !=
         cudaSuccess)

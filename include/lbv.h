@@ -106,18 +106,6 @@ typedef enum { LBV_F16 = 0, LBV_BF16 = 1 } lbv_dtype;
                                       Not combinable with LBV_PLAN_TCGEN05,
                                       LBV_PLAN_FORCE_GEMV or
                                       LBV_PLAN_TEST_WAIT_LIMIT. */
-#define LBV_PLAN_X_SHARE     0x80u /* few-row kernel without K split: pair CTAs
-                                      along N (clusters of 2) to stage the
-                                      activations once per pair: each CTA stages,
-                                      rotates (fused head) and corrects half of the
-                                      K range and copies its half into the other's
-                                      shared memory (distributed shared memory, no
-                                      multicast).  Results are the same bit for
-                                      bit.  Measured slower on GB300 (the pairs
-                                      couple two SMs' start and prologue), so off
-                                      by default.  Ignored where it does not apply
-                                      (a K split, an odd CTA count along N, fewer
-                                      than two 128-element blocks of K). */
 #define LBV_PLAN_TEST_WAIT_LIMIT 0x20u /* test only: the few-row kernel's waits
                                       on its weight stages give up after 256
                                       tries, and the first warp of the first

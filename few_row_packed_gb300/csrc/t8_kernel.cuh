@@ -10,12 +10,18 @@
 // as the e4m3 value code * 2^(f - 9) (subnormals, continued by the lowest
 // normals), so four weights take one LOP3 and no base offset or correction
 // term exists.  The activations are the B operand of kind::f8f6f4 as well:
-// each row, scaled by a power of two so its largest |x * 2^-f| lies in
-// [2^7, 2^8), is split exactly into three e4m3 terms (t0 = RN(v),
-// t1 = RN(16 (v - t0)), t2 = RN(16 (16 (v - t0) - t1)); an fp16 or bf16
-// value has at most 11 significant bits and each term takes 4), one B row
-// per (term, activation row): N = 32 (24 used).  Products of e4m3 values are
-// exact and the tensor core sums them in fp32.
+// per 128-K group and row, x * 2^(sig - f) with the power of two that brings
+// the group's largest |x * 2^-f| into [2^7, 2^8) is split exactly into three
+// e4m3 terms t0 + t1/16 + t2/256, each the leading 4 significant bits of
+// what is left (an fp16 or bf16 value has at most 11 significant bits), one
+// B row per (term, activation row): N = 32 (24 used).  Products of e4m3
+// values are exact and the tensor core sums them in fp32.
+//
+// Measured on GB300 this kernel is slower than the mma.sync one: every group
+// stores 4 KB of A and reads back 3 KB of accumulator per warp (the fp16
+// group scale has to be applied outside the tensor core), and tensor memory
+// sustains only ~81 B/clk/SM of such mixed traffic (177 B/clk stores alone,
+// 323 B/clk loads alone).  It is kept as an opt-in, parity-tested path.
 //
 // Structure (one CTA per SM, 640 threads):
 //   * Four warpgroups, each of four decode warps (warp q owns tensor-memory
@@ -30,8 +36,8 @@
 //     (tcgen05.st), and arrives on the slot's mbarrier; the MMA warp issues
 //     four M128 N32 K32 MMAs into the slot's accumulator and commits; one
 //     group later the decode threads read the accumulator back (tcgen05.ld)
-//     and fold  scale * (acc0 + acc1/16 + acc2/256)  (+ bias * row sum) into
-//     eight fp32 row sums.  Two A slots and two accumulators per warpgroup
+//     and fold  scale * 2^(9 - sig) * (acc0 + acc1/16 + acc2/256)
+//     (+ bias * row sum) into eight fp32 row sums.  Two A slots and two accumulators per warpgroup
 //     (4 x 128 tensor-memory columns).
 //   * K is split across the S CTAs of a cluster.  Tile i of the cluster
 //     belongs to rank i % S; the other ranks write their partial rows into
@@ -41,12 +47,11 @@
 //     Y or updates the argmax keys.
 //   * Prologue: the X slice is staged (bulk copies, after
 //     griddepcontrol.wait), optionally sign-flipped and rotated (FWHT-128,
-//     the fused head), then split into the B tiles and the row sums; packed
-//     weights start streaming before the wait.  Every wait is bounded; a wait
+//     the fused head), then split into the B tiles and the per-(group, row)
+//     constants (2^(9 - sig), row sum), one warp per group; packed weights
+//     start streaming before the wait.  Every wait is bounded; a wait
 //     that gives up sets the plan's status word and lets the kernel end.
 #pragma once
-
-#include <cooperative_groups.h>
 
 #include "t8_internal.h"
 #include "verify_kernel.cuh"
@@ -54,8 +59,6 @@
 namespace lbv {
 
 namespace t8 {
-
-namespace cg = cooperative_groups;
 
 // ---------------------------------------------------------------------------
 // tcgen05 / cluster helpers

@@ -679,6 +679,16 @@ def run_lbv(args, rank, world, barrier, reduce_max):
     peak, peak_kind = peaks()
     phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev)).split(",")[dev]
     configs = ([(args.workload, args.stack)] if args.workload != "all" else ALL_CONFIGS)
+    skipped = []
+    if args.kernel == "tc8":
+        # the e4m3 tensor-memory kernel reads the g128 formats only
+        keep = [c for c in configs if all(m.group == 128 and m.fmt != synth.Q4_0
+                                          for m in synth.WORKLOADS[c[0]].matrices)]
+        skipped = [{"workload": w, "stack": st, "skipped": "the e4m3 kernel reads sign1 g128 "
+                    "and affine2 g128 only"} for w, st in configs if (w, st) not in keep]
+        configs = keep
+    if not configs:
+        raise SystemExit("no configuration runs on the chosen kernel")
 
     sampler = ClockSampler(int(phys) if phys.isdigit() else dev)
     sampler.start()
@@ -745,7 +755,7 @@ def run_lbv(args, rank, world, barrier, reduce_max):
         "gpu_launches": args.steps * head_stack.launches_per_step,
         "clocks": clocks,
         "dense_fp16_context": head_extra.get("dense"),
-        "configs": results,
+        "configs": results + skipped,
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(workload, args.M, budget_s=10.0, head=args.head)

@@ -923,41 +923,68 @@ struct VerifyKernel {
         return false;
     }
 
-    // Per-group corrections of the slice, one warp per chunk:
-    //   corr = -sum_k c_k x_k (Q4_0: -sum_k (c_k + 8) x_k), rsum = rowsum.
+    // Per-group corrections of the slice, one warp per chunk, on the tensor
+    // cores: for each k-tile one m16n8k16 MMA of the staged X fragments (the
+    // main loop's B operands) with a constant A whose rows 0..7 hold the
+    // decode offset c of each K position (Q4_0: c + 8, as w = d (q - 8)) and
+    // rows 8..15 ones, chained over the group's k-tiles.  So lane (g, t) holds
+    //   D[g][2t + j]     = sum_k c_k x_k   (row 2t + j of X)
+    //   D[g + 8][2t + j] = sum_k x_k       (its row sum)
+    // and corr = -sum_k c_k x_k, rsum = the row sum.  Every product is exact
+    // (c and x are fp16/bf16 values); the sums are the tensor core's fp32.
+    static __host__ __device__ constexpr uint32_t small_int_bits(int xt, int v)
+    {
+        // v = 0 or a positive integer exact in the X dtype
+        int e = 0;
+        while ((2 << e) <= v)
+            ++e;
+        return v == 0 ? 0u
+               : xt == LBV_F16
+                   ? (uint32_t)((e + 15) << 10) | (uint32_t)((v - (1 << e)) << (10 - e))
+                   : (uint32_t)((e + 127) << 7) | (uint32_t)((v - (1 << e)) << (7 - e));
+    }
+
+    static __host__ __device__ constexpr uint32_t offset_pair(int slot)
+    {
+        const int c = dec_spec<FMT>(XT, slot).c + (FMT == LBV_FMT_Q4_0 ? 8 : 0);
+        const uint32_t h = small_int_bits(XT, c);
+        return h | (h << 16);
+    }
+
+    static __host__ __device__ constexpr bool offsets_exact()
+    {
+        for (int slot = 0; slot < T::KT; ++slot) {
+            const int c = dec_spec<FMT>(XT, slot).c + (FMT == LBV_FMT_Q4_0 ? 8 : 0);
+            if (half_bits_value(XT, offset_pair(slot) & 0xFFFFu) != (double)c)
+                return false;
+        }
+        return true;
+    }
+    static_assert(offsets_exact(), "a decode offset is not exact in the X dtype");
+
     template <int... KP>
     static __device__ __forceinline__ void corr_pairs(std::integer_sequence<int, KP...>,
-                                                      uint32_t xa, float (&cs)[T::GPC],
-                                                      float (&rs)[T::GPC])
+                                                      uint32_t xa, float (&d)[T::GPC][4])
     {
+        constexpr uint32_t one = XT == LBV_F16 ? 0x3C003C00u : 0x3F803F80u;
         (
             [&] {
-                constexpr int kt0 = 2 * KP;
-                const uint4 q = ldsm_x4(xa + KP * 64);
+                const uint4 q = ldsm_x4(xa + KP * 64);            // k-tiles 2 KP, 2 KP + 1
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int kt = kt0 + e;                       // folds after unrolling
-                    const float2 f0 = pair_to_float2<XT>(e ? q.z : q.x);
-                    const float2 f1 = pair_to_float2<XT>(e ? q.w : q.y);
-                    const float s0 = f0.x + f0.y, s1 = f1.x + f1.y;
+                    const int kt = 2 * KP + e;                    // folds after unrolling
                     const int ktl = kt % (T::KT / 2);
                     const int gi = kt / T::KTG;
-                    cs[gi] += coef(2 * ktl) * s0 + coef(2 * ktl + 1) * s1;
-                    rs[gi] += s0 + s1;
+                    const uint32_t a0 = offset_pair(2 * ktl), a2 = offset_pair(2 * ktl + 1);
+                    const uint32_t b0 = e ? q.z : q.x, b1 = e ? q.w : q.y;
+                    if (kt % T::KTG == 0)
+                        mma16816_c<XT>(d[gi], a0, one, a2, one, b0, b1,
+                                       make_float4(0.f, 0.f, 0.f, 0.f));
+                    else
+                        mma16816<XT>(d[gi], a0, one, a2, one, b0, b1);
                 }
             }(),
             ...);
-    }
-
-    static __device__ __forceinline__ float coef(int s)
-    {
-        // s is a constant after unrolling; the chain folds to one value.
-        float c = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i == s)
-                c = (float)dec_spec<FMT>(XT, i).c;
-        return c;
     }
 
     static __device__ __forceinline__ void corrections(uint32_t xs_a, int RS, float* corr, float* rsum,
@@ -965,29 +992,20 @@ struct VerifyKernel {
     {
         const int g = lane >> 2, t = lane & 3;
         for (int cl = warp; cl < nch; cl += NW) {
-            float cs[T::GPC], rs[T::GPC];
-#pragma unroll
-            for (int i = 0; i < T::GPC; ++i)
-                cs[i] = rs[i] = 0.f;
+            float d[T::GPC][4];
             corr_pairs(std::make_integer_sequence<int, T::KT / 2>{},
-                       xs_a + ldsm_lane_offset(RS, lane) + cl * T::CHUNK_K * 2, cs, rs);
+                       xs_a + ldsm_lane_offset(RS, lane) + cl * T::CHUNK_K * 2, d);
+            if (g == 0) {
 #pragma unroll
-            for (int i = 0; i < T::GPC; ++i) {
-                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 1);
-                cs[i] += __shfl_xor_sync(0xffffffffu, cs[i], 2);
-                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
-                rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
-                if (t == 0) {
+                for (int i = 0; i < T::GPC; ++i) {
                     // corr holds each group's C fragment: for lane t the quad
                     // (row 2t, row 2t + 1, row 2t, row 2t + 1)
                     const int gr = cl * T::GPC + i;
-                    const float c = FMT == LBV_FMT_Q4_0 ? -(cs[i] + 8.f * rs[i])   // w = d (q - 8)
-                                                        : -cs[i];
-                    float* q = corr + gr * 16 + 4 * (g >> 1) + (g & 1);
-                    q[0] = c;
-                    q[2] = c;
+                    *reinterpret_cast<float4*>(corr + gr * 16 + 4 * t) =
+                        make_float4(-d[i][0], -d[i][1], -d[i][0], -d[i][1]);
                     if constexpr (T::AFFINE)
-                        rsum[gr * 8 + g] = rs[i];
+                        *reinterpret_cast<float2*>(rsum + gr * 8 + 2 * t) =
+                            make_float2(d[i][2], d[i][3]);
                 }
             }
         }

@@ -144,6 +144,36 @@ __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint64_t b0, u
         : "memory");
 }
 
+// Two fp32 values as one 64-bit register pair (lo first), and the packed
+// fp32x2 arithmetic of sm_100+: each half is rounded like its scalar op.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2unpack(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Bounded wait with cluster-scope acquire (arrivals from peer CTAs).
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   uint32_t limit = 1u << 20)
@@ -367,10 +397,11 @@ struct T8Kernel {
     // t0 + t1/16 + t2/256 with each term v, 16 (v - t0), ... truncated to its
     // leading 4 significant bits (the fp32 pattern masked): exact for the 11
     // significant bits of an fp16 (8 of a bf16) value, every term below 256.
-    // ep[g][m] = (2^(9 - sig), row sum of the group's x in fp32); rows >= M
+    // ep[g] = (U_0..U_7, R_0..R_7): U_m = 2^(9 - sig), R_m the row sum of the
+    // group's x in fp32 (negated for sign1, whose fold is s (2 acc - R)); rows >= M
     // and the fourth term (B rows 24..31) are zeros.
     static __device__ void build_b(const unsigned char* xs, int RS, int M, int gcnt,
-                                   unsigned char* bsm, float2* ep)
+                                   unsigned char* bsm, float* ep)
     {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int m = lane & 7, jq = lane >> 3;
@@ -428,8 +459,10 @@ struct T8Kernel {
                         make_uint4(t[j][4 * h], t[j][4 * h + 1], t[j][4 * h + 2], t[j][4 * h + 3]);
                 *reinterpret_cast<uint4*>(dst + h * 128 + 3 * 256) = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (jq == 0)
-                ep[g * 8 + m] = m < M ? make_float2(t8::pow2f(9 - sg), sum) : make_float2(0.f, 0.f);
+            if (jq == 0) {
+                ep[g * 16 + m] = m < M ? t8::pow2f(9 - sg) : 0.f;
+                ep[g * 16 + 8 + m] = m < M ? (W == 2 ? sum : -sum) : 0.f;
+            }
         }
     }
 
@@ -486,7 +519,7 @@ struct T8Kernel {
         unsigned char* bsm = smem + cv.b;
         const int RS = ks * 2 + 16;
         unsigned char* xs = smem + cv.x;
-        float2* ep = reinterpret_cast<float2*>(smem + cv.ep);
+        float* ep = reinterpret_cast<float*>(smem + cv.ep);
         float* part = reinterpret_cast<float*>(smem + cv.part);
         uint64_t* bars = reinterpret_cast<uint64_t*>(smem + cv.bars);
         // ring[4][NS], full[4][2], done[4][2], pready[owned], xbar
@@ -591,7 +624,9 @@ struct T8Kernel {
 
         const uint32_t tm_wg = tmem + (uint32_t)(wg * 128);
         if (is_issuer) {
-            // ---- MMA warp: one group per A slot, alternating slots
+            // ---- MMA warp: one group per A slot, alternating slots.  Once
+            // the four decode warps have stored the last group of a ring
+            // stage they have read all of it, so the MMA warp refills its slot.
             int done_n = 0;
             int g = 0;
             for (int c = 0; c < total && ok; ++c) {
@@ -599,6 +634,11 @@ struct T8Kernel {
                 if (!mbar_wait(bar_full + (wg * 2 + slot) * 8, (uint32_t)((c >> 1) & 1))) {
                     ok = false;
                     break;
+                }
+                if ((g % GPS) == GPS - 1 || g == gcnt - 1) {
+                    if (lane == 0 && issued < nstage)
+                        issue_s(issued);
+                    issued = min(issued + 1, nstage);
                 }
                 t8::tc_fence_after();
                 t8::mma_group(tm_wg + 64u + (uint32_t)slot * 32u, tm_wg + (uint32_t)slot * 32u,
@@ -612,14 +652,20 @@ struct T8Kernel {
             for (int c = max(0, done_n - 2); c < done_n; ++c)
                 if (!mbar_wait(bar_done + (wg * 2 + (c & 1)) * 8, (uint32_t)((c >> 1) & 1)))
                     ok = false;
+            // every stage issued has landed before the CTA exits (the last NS
+            // issued; an earlier stage of a slot was read before its slot was
+            // refilled)
+            for (int st = max(0, issued - NS); st < issued; ++st)
+                if (!mbar_wait(bar_ring + (wg * NS + st % NS) * 8, (uint32_t)((st / NS) & 1)))
+                    ok = false;
 
         } else {
             // ---- decode warp
             const uint32_t ta = tm_wg | ((uint32_t)(q * 32) << 16);
-            float Y[8];
+            uint64_t Y2[4];                          // rows 2i, 2i + 1 as packed pairs
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-                Y[m] = 0.f;
+            for (int i = 0; i < 4; ++i)
+                Y2[i] = 0ull;
             float s_prev = 0.f, b_prev = 0.f;        // scale, bias of the group behind
             float pend[8];                           // an owned tile's own partial, parked
             int pend_li = -1;
@@ -653,9 +699,7 @@ struct T8Kernel {
                     ++consumed;
                 return true;
             };
-            // folds accumulator e (group ge of tile te) into Y; after the last
-            // group of a ring stage (every decode warp has read it: its MMAs are
-            // done), decode warp 0 refills the stage's slot; at a tile's last
+            // folds accumulator e (group ge of tile te) into Y; at a tile's last
             // group, with a K split, hands the partial to the owner, or (owner)
             // parks it and reduces the tile parked before, whose partials
             // arrived a tile ago
@@ -665,26 +709,40 @@ struct T8Kernel {
                 t8::tc_fence_after();
                 float d[24];
                 t8::tmem_ld24(ta + 64u + (uint32_t)((e & 1) * 32), d);
-                if (q == 0 && ((ge % GPS) == GPS - 1 || ge == gcnt - 1)) {
-                    if (lane == 0 && issued < nstage)
-                        issue_s(issued);
-                    issued = min(issued + 1, nstage);
-                }
-                const float4* e4 = reinterpret_cast<const float4*>(ep + ge * 8);
-                const float4 E0 = e4[0], E1 = e4[1], E2 = e4[2], E3 = e4[3];
-                const float U[8] = {E0.x, E0.z, E1.x, E1.z, E2.x, E2.z, E3.x, E3.z};
-                const float R[8] = {E0.y, E0.w, E1.y, E1.w, E2.y, E2.w, E3.y, E3.w};
+                const float4* e4 = reinterpret_cast<const float4*>(ep + ge * 16);
+                const float4 Ua = e4[0], Ub = e4[1], Ra = e4[2], Rb = e4[3];
+                const uint64_t U2[4] = {t8::f2pack(Ua.x, Ua.y), t8::f2pack(Ua.z, Ua.w),
+                                        t8::f2pack(Ub.x, Ub.y), t8::f2pack(Ub.z, Ub.w)};
+                const uint64_t R2[4] = {t8::f2pack(Ra.x, Ra.y), t8::f2pack(Ra.z, Ra.w),
+                                        t8::f2pack(Rb.x, Rb.y), t8::f2pack(Rb.z, Rb.w)};
+                const uint64_t k16 = t8::f2pack(1.f / 16.f, 1.f / 16.f);
+                const uint64_t k256 = t8::f2pack(1.f / 256.f, 1.f / 256.f);
+                const uint64_t s2 = t8::f2pack(s_prev, s_prev);
+                const uint64_t b2 = W == 2 ? t8::f2pack(b_prev, b_prev) : t8::f2pack(2.f, 2.f);
+                // rows 2i, 2i + 1 at once:
+                //   acc = U (d0 + d1 / 16 + d2 / 256)  (the three terms of X)
+                //   affine2: Y += s acc + b R;  sign1: Y += s (2 acc - R)
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float acc =
-                        U[m] * fmaf(d[16 + m], 1.f / 256.f, fmaf(d[8 + m], 1.f / 16.f, d[m]));
+                for (int i = 0; i < 4; ++i) {
+                    const uint64_t t0 = t8::f2pack(d[2 * i], d[2 * i + 1]);
+                    const uint64_t t1 = t8::f2pack(d[8 + 2 * i], d[9 + 2 * i]);
+                    const uint64_t t2 = t8::f2pack(d[16 + 2 * i], d[17 + 2 * i]);
+                    const uint64_t acc =
+                        t8::fmul2(U2[i], t8::ffma2(t2, k256, t8::ffma2(t1, k16, t0)));
                     if constexpr (W == 2)
-                        Y[m] = fmaf(s_prev, acc, fmaf(b_prev, R[m], Y[m]));
+                        Y2[i] = t8::ffma2(s2, acc, t8::ffma2(b2, R2[i], Y2[i]));
                     else
-                        Y[m] = fmaf(s_prev, fmaf(2.f, acc, -R[m]), Y[m]);
+                        Y2[i] = t8::ffma2(s2, t8::ffma2(b2, acc, R2[i]), Y2[i]);
                 }
                 if (++ge == gcnt) {
                     const int li = wg + 4 * te;
+                    float Y[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 v = t8::f2unpack(Y2[i]);
+                        Y[2 * i] = v.x;
+                        Y[2 * i + 1] = v.y;
+                    }
                     if (S == 1) {
                         emit(p, t0 + li, q * 32 + lane, lane, Y, akeys);
                     } else if (li % S != rank) {
@@ -701,14 +759,14 @@ struct T8Kernel {
                     ge = 0;
                     ++te;
 #pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        Y[m] = 0.f;
+                    for (int i = 0; i < 4; ++i)
+                        Y2[i] = 0ull;
                 }
                 return true;
             };
             // Per group c: decode (codes loaded one group ahead), tensor-memory
-            // store, arrive (the MMAs of c run meanwhile), load group c + 1,
-            // then the epilogue of group c - 1.
+            // store, load group c + 1 while the store completes, arrive (the
+            // MMAs of c run meanwhile), then the epilogue of group c - 1.
             if (total > 0 && !load_group(0))
                 ok = false;
             int g = 0;                               // decode cursor (slice-local group)
@@ -725,7 +783,8 @@ struct T8Kernel {
                 const float s_c = s_nx, b_c = b_nx;
                 if (++g == gcnt)
                     g = 0;
-                if (c + 1 < total && !load_group(g)) {
+                const bool loaded = c + 1 >= total || load_group(g);
+                if (!loaded) {
                     ok = false;
                     break;
                 }
@@ -738,13 +797,6 @@ struct T8Kernel {
             }
             if (ok && total > 0 && !epilogue(total - 1))
                 ok = false;
-            // every stage issued has landed before the CTA exits (the last NS
-            // issued; an earlier stage of a slot was waited on before its slot
-            // was refilled)
-            if (q == 0)
-                for (int st = max(0, issued - NS); st < issued; ++st)
-                    if (!mbar_wait(bar_ring + (wg * NS + st % NS) * 8, (uint32_t)((st / NS) & 1)))
-                        ok = false;
             if (pend_li >= 0 && ok)
                 reduce_emit(p, t0 + pend_li, pend_li, q * 32 + lane, lane, rank, pend, part,
                             bar_pready, akeys, ok);
@@ -809,8 +861,10 @@ struct T8Kernel {
         const int si = rank < owner ? rank : rank - 1;
         const uint32_t base = smem_u32(part + ((size_t)(j * (S - 1) + si) * 8) * 128 + col);
         const uint32_t rbase = t8::mapa(base, (uint32_t)owner);
-        for (int m = 0; m < p.M; ++m)
-            t8::st_cluster_f32(rbase + (uint32_t)(m * 128 * 4), y[m]);
+#pragma unroll
+        for (int m = 0; m < 8; ++m)                   // unrolled: y stays in registers
+            if (m < p.M)
+                t8::st_cluster_f32(rbase + (uint32_t)(m * 128 * 4), y[m]);
         t8::mbar_arrive_remote(t8::mapa(bar_pready + (uint32_t)j * 8, (uint32_t)owner));
     }
 

@@ -208,9 +208,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
                  : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v)
+// Four fp32 values into a peer CTA's shared memory (16-byte aligned), counted
+// on the peer's mbarrier as 16 bytes of its transaction once they land.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
+                                            float d, uint32_t cluster_bar)
 {
-    asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(cluster_addr), "f"(v) : "memory");
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n"
+        ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank()
@@ -262,7 +268,7 @@ __device__ __forceinline__ float pow2f(int e)
 // size query alike:
 //   ring [NS][4 warpgroups][stage] | B tiles [gps * 4][1024] | X rows [8][RS]
 //   (unless staged in the ring) | epilogue constants [gps][8] float2 |
-//   partial slots [owned][S - 1][8][128] float | mbarriers ring [4][NS],
+//   partial slots [owned][S - 1][128][8] float | mbarriers ring [4][NS],
 //   full [4][2], done [4][2], pready [owned], X | misc words [18] | keys [8]
 struct T8Carve {
     size_t b, x, ep, part, bars, misc, keys, end;
@@ -559,9 +565,13 @@ struct T8Kernel {
                 mbar_init(bar_done + i * 8, 1);
             }
             for (int i = 0; i < p.owned; ++i)
-                mbar_init(bar_pready + i * 8, (uint32_t)(S - 1) * 128u);
+                mbar_init(bar_pready + i * 8, 1);
             mbar_init(xbar, 1);
             mbar_init_fence();
+            // an owned tile's slot completes once the other ranks' partial
+            // rows (128 columns x 8 rows each) have landed
+            for (int i = 0; i < p.owned; ++i)
+                mbar_expect_tx(bar_pready + i * 8, (uint32_t)(S - 1) * 128u * 8u * 4u);
         }
         if (tid < 8)
             akeys[tid] = 0ull;
@@ -848,10 +858,9 @@ struct T8Kernel {
     }
 
     // K split: cluster tile li belongs to rank li % S, at slot li / S.  A
-    // non-owner writes its partial rows (m < M) into the owner's slot for its
-    // rank (distributed shared memory) and arrives on the owner's mbarrier of
-    // that tile (each of the 128 threads of the warpgroup, release at cluster
-    // scope).
+    // non-owner writes its partial rows (all 8, column-major) into the
+    // owner's slot for its rank (distributed shared memory) with asynchronous
+    // stores that count on the owner's mbarrier of that tile.
     static __device__ __forceinline__ void send_partial(const T8Params& p, int li, int col,
                                                         int rank, const float (&y)[8],
                                                         const float* part, uint32_t bar_pready)
@@ -859,13 +868,11 @@ struct T8Kernel {
         const int S = p.splits;
         const int owner = li % S, j = li / S;
         const int si = rank < owner ? rank : rank - 1;
-        const uint32_t base = smem_u32(part + ((size_t)(j * (S - 1) + si) * 8) * 128 + col);
+        const uint32_t base = smem_u32(part + ((size_t)(j * (S - 1) + si) * 128 + col) * 8);
         const uint32_t rbase = t8::mapa(base, (uint32_t)owner);
-#pragma unroll
-        for (int m = 0; m < 8; ++m)                   // unrolled: y stays in registers
-            if (m < p.M)
-                t8::st_cluster_f32(rbase + (uint32_t)(m * 128 * 4), y[m]);
-        t8::mbar_arrive_remote(t8::mapa(bar_pready + (uint32_t)j * 8, (uint32_t)owner));
+        const uint32_t rbar = t8::mapa(bar_pready + (uint32_t)j * 8, (uint32_t)owner);
+        t8::st_async_v4(rbase, y[0], y[1], y[2], y[3], rbar);
+        t8::st_async_v4(rbase + 16u, y[4], y[5], y[6], y[7], rbar);
     }
 
     // The owner of cluster tile li: wait for the other slices' partials, add
@@ -891,11 +898,17 @@ struct T8Kernel {
                     acc[m] += own[m];
             } else {
                 const int si = rk < rank ? rk : rk - 1;
-                const float* src = part + ((size_t)(j * (S - 1) + si) * 8) * 128 + col;
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    if (m < p.M)
-                        acc[m] += src[m * 128];
+                const float4* src =
+                    reinterpret_cast<const float4*>(part + ((size_t)(j * (S - 1) + si) * 128 + col) * 8);
+                const float4 lo = src[0], hi = src[1];
+                acc[0] += lo.x;
+                acc[1] += lo.y;
+                acc[2] += lo.z;
+                acc[3] += lo.w;
+                acc[4] += hi.x;
+                acc[5] += hi.y;
+                acc[6] += hi.z;
+                acc[7] += hi.w;
             }
         }
         emit(p, tile, col, lane, acc, akeys);

@@ -17,11 +17,12 @@
 // B row per (term, activation row): N = 32 (24 used).  Products of e4m3
 // values are exact and the tensor core sums them in fp32.
 //
-// Measured on GB300 this kernel is slower than the mma.sync one: every group
+// Measured on GB300 this kernel is slower than the mma.sync one.  Every group
 // stores 4 KB of A and reads back 3 KB of accumulator per warp (the fp16
-// group scale has to be applied outside the tensor core), and tensor memory
-// sustains only ~81 B/clk/SM of such mixed traffic (177 B/clk stores alone,
-// 323 B/clk loads alone).  It is kept as an opt-in, parity-tested path.
+// group scale has to be applied outside the tensor core), and each decode
+// warp runs that store, its wait, the read-back, its wait and the shared
+// loads as one serial chain per group, four such warps per scheduler.  It
+// is kept as an opt-in, parity-tested path.
 //
 // Structure (one CTA per SM, 640 threads):
 //   * Four warpgroups, each of four decode warps (warp q owns tensor-memory
@@ -31,20 +32,21 @@
 //     time.
 //   * Per group: each decode thread loads its column's codes from its
 //     warpgroup's ring of bulk-copied stages (one copy per stage of the tile's
-//     four quarters; decode warp 0 refills a slot once the MMAs of its last
-//     group are done), writes 32 e4m3 words to the group's A slot
-//     (tcgen05.st), and arrives on the slot's mbarrier; the MMA warp issues
-//     four M128 N32 K32 MMAs into the slot's accumulator and commits; one
-//     group later the decode threads read the accumulator back (tcgen05.ld)
-//     and fold  scale * 2^(9 - sig) * (acc0 + acc1/16 + acc2/256)
-//     (+ bias * row sum) into eight fp32 row sums.  Two A slots and two accumulators per warpgroup
-//     (4 x 128 tensor-memory columns).
+//     four quarters; the MMA warp refills a slot once the decode warps have
+//     stored the slot's last group), writes 32 e4m3 words to the group's A
+//     slot (tcgen05.st), and arrives on the slot's mbarrier; the MMA warp
+//     issues four M128 N32 K32 MMAs into the slot's accumulator and commits;
+//     one group later the decode threads read the accumulator back
+//     (tcgen05.ld) and fold  scale * 2^(9 - sig) * (acc0 + acc1/16 + acc2/256)
+//     (+ bias * row sum) into eight fp32 row sums, two rows per fp32x2 op.
+//     Two A slots and two accumulators per warpgroup (4 x 128 tensor-memory
+//     columns).
 //   * K is split across the S CTAs of a cluster.  Tile i of the cluster
-//     belongs to rank i % S; the other ranks write their partial rows into
-//     the owner's shared memory (distributed shared memory) and arrive on its
-//     mbarrier; the owner parks its own partial until it finishes its next
-//     tile, then adds the S partials in rank order (deterministic) and writes
-//     Y or updates the argmax keys.
+//     belongs to rank i % S; the other ranks send their partial rows into the
+//     owner's shared memory with asynchronous stores counted on its mbarrier
+//     for that tile; the owner parks its own partial until it finishes its
+//     next tile, then adds the S partials in rank order (deterministic) and
+//     writes Y or updates the argmax keys.
 //   * Prologue: the X slice is staged (bulk copies, after
 //     griddepcontrol.wait), optionally sign-flipped and rotated (FWHT-128,
 //     the fused head), then split into the B tiles and the per-(group, row)

@@ -30,10 +30,10 @@
 //     visited alternately from its two halves (two interleaved accumulator
 //     chains for groups of 64 or fewer), and each tile of a unit has its own.
 //   * The offsets c enter each group's accumulator as its initial value
-//     -sum_k c_k x_k, computed once per CTA from the staged activations (the
-//     "row-sum prep" of the dflash-mlx-bonsai2 README); the group scale (and
-//     bias * row sum for affine) is applied in fp32 once per group, so every
-//     tensor-core operand is an exact small integer.
+//     -sum_k c_k x_k, computed once per CTA from the staged activations on the
+//     tensor cores (the "row-sum prep" of the dflash-mlx-bonsai2 README); the
+//     group scale (and bias * row sum for affine) is applied in fp32 once per
+//     group, so every tensor-core operand is an exact small integer.
 #pragma once
 
 #include <cooperative_groups.h>

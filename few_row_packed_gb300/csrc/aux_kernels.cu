@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 
 #include "lbv_internal.h"
+#include "verify_kernel.cuh"
 
 namespace lbv {
 
@@ -318,6 +319,191 @@ __global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int
     }
 }
 
+// 1-row path for the 1-bit format, by table lookup.  In the record layout a
+// lane's word w of chunk c, half H (one 128-K group of one column) holds at
+// bit 4i + j, i < 8, j < 4, the sign of k = 256 c + 16 (8 H + 2 (i & 3) +
+// (j >> 1)) + 8 (j & 1) + 2 t + (i >> 2) for the lane's t = lane & 3 (the
+// few-row kernel's fragment order).  So the 4-bit field i of w selects one of
+// 16 signed sums of four activations:
+//   T[c][H][i][v][t] = sum_j (bit j of v ? +x_k : -x_k),
+// which each CTA tabulates once in shared memory, and a group's dot product
+// is 8 table reads per word.  Warps take (tile, K quarter) items, four tiles
+// per CTA at a time; each warp fetches an item's records with one bulk copy
+// into one of two buffers, the next item's while it works on the current one
+// (the first two are issued before the table is built), and the four
+// quarters' partial sums of a tile meet in shared memory and are added in
+// quarter order.  Table rows of one field are 272 bytes apart, so the 8 fields a
+// warp writes or reads at once fall in different banks.
+constexpr int kLutWarps = 16, kLutTiles = kLutWarps / 4;
+constexpr int kLutField = 272;                       // bytes per (chunk, half, field): 16 x 4 floats + pad
+constexpr int kLutHalf = 8 * kLutField;
+constexpr int kLutChunk = 2 * kLutHalf;
+
+struct Sign1LutGeom {
+    int kq, cpq;                                     // K quarters, chunks per quarter
+    size_t table, xrow, buf, part, bars, end;        // byte offsets of the carve-up
+};
+
+__host__ __device__ inline Sign1LutGeom sign1_lut_geom(int nchunks, int K)
+{
+    using A = AuxTraits<LBV_FMT_SIGN1_G128, 128>;
+    Sign1LutGeom gm;
+    gm.kq = nchunks < 4 ? nchunks : 4;
+    gm.cpq = (nchunks + gm.kq - 1) / gm.kq;
+    gm.table = 0;
+    gm.xrow = (size_t)nchunks * kLutChunk;
+    gm.buf = gm.xrow + (((size_t)nchunks * A::CK * 2 + 15) / 16) * 16;
+    gm.part = gm.buf + (size_t)kLutWarps * 2 * gm.cpq * A::REC;    // two buffers per warp
+    gm.bars = gm.part + (size_t)kLutWarps * 32 * 2 * sizeof(float);
+    gm.end = gm.bars + (size_t)kLutWarps * 2 * 8;
+    (void)K;
+    return gm;
+}
+
+// Sum of the 8 table entries that word w's fields select; tb points at the
+// (chunk, half) block for this lane's t (entries 16 bytes apart by value).
+__device__ __forceinline__ float lut_word(uint32_t w, const unsigned char* tb)
+{
+    float e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t off = i == 0 ? (w << 4) & 0xF0u : (w >> (4 * i - 4)) & 0xF0u;
+        e[i] = *reinterpret_cast<const float*>(tb + i * kLutField + off);
+    }
+    return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kLutWarps * 32) lbv_gemv_sign1_lut_kernel(const VerifyParams p,
+                                                                             int row)
+{
+    using A = AuxTraits<LBV_FMT_SIGN1_G128, 128>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Sign1LutGeom gm = sign1_lut_geom(p.nchunks, p.K);
+    unsigned char* tbl = smem + gm.table;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + gm.xrow);
+    float* part = reinterpret_cast<float*>(smem + gm.part);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int tl = warp % kLutTiles, q = warp / kLutTiles;
+    const int ca = min(q * gm.cpq, p.nchunks), cz = min(ca + gm.cpq, p.nchunks);
+    const uint32_t bar0 = smem_u32(smem + gm.bars) + warp * 16;       // per buffer
+    unsigned char* buf0 = smem + gm.buf + (size_t)warp * 2 * gm.cpq * A::REC;
+    if (lane == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    // this warp's records of item n (tile tile0_n + tl) into buffer n & 1;
+    // bit b of pend: a copy into buffer b issued and not yet waited for; bit b
+    // of phase: the parity buffer b's next wait is for
+    bool ok = true;
+    uint32_t pend = 0u, phase = 0u;
+    const int stride = gridDim.x * kLutTiles;
+    auto fetch = [&](int n) {
+        const int tile = blockIdx.x * kLutTiles + n * stride + tl, b = n & 1;
+        if (ok && tile < p.ntiles && q < gm.kq && cz > ca) {
+            if (lane == 0) {
+                const uint32_t bytes = (uint32_t)(cz - ca) * A::REC;
+                mbar_expect_tx(bar0 + b * 8, bytes);
+                bulk_g2s_if(1u, smem_u32(buf0 + (size_t)b * gm.cpq * A::REC),
+                            p.W + ((size_t)tile * p.nchunks + ca) * A::REC, bytes, bar0 + b * 8);
+            }
+            pend |= 1u << b;
+        }
+    };
+    fetch(0);
+    fetch(1);
+
+    const uint16_t* x = reinterpret_cast<const uint16_t*>(p.X) + (size_t)row * p.ldx;
+    for (int k = tid; k < p.nchunks * A::CK; k += kLutWarps * 32)
+        xs[k] = k < p.K ? x[k] : (uint16_t)0;
+    __syncthreads();
+    // the table: one (chunk, half, field, t) row of 16 sums per thread and turn
+    const int nrows = p.nchunks * 64;
+    for (int r = tid; r < nrows; r += kLutWarps * 32) {
+        const int tt = r & 3, i = (r >> 2) & 7, H = (r >> 5) & 1, c = r >> 6;
+        float xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = c * A::CK + 16 * (8 * H + 2 * (i & 3) + (j >> 1)) + 8 * (j & 1) + 2 * tt +
+                          (i >> 2);
+            if constexpr (DT == LBV_F16)
+                xv[j] = __half2float(__ushort_as_half(xs[k]));
+            else
+                xv[j] = __bfloat162float(__ushort_as_bfloat16(xs[k]));
+        }
+        const float a[4] = {-xv[0] - xv[1], xv[0] - xv[1], -xv[0] + xv[1], xv[0] + xv[1]};
+        const float b[4] = {-xv[2] - xv[3], xv[2] - xv[3], -xv[2] + xv[3], xv[2] + xv[3]};
+        float* out = reinterpret_cast<float*>(tbl + (size_t)c * kLutChunk + H * kLutHalf +
+                                              i * kLutField) + tt;
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+            out[v * 4] = a[v & 3] + b[v >> 2];
+    }
+    __syncthreads();
+
+    int n = 0;
+    for (int tile0 = blockIdx.x * kLutTiles; tile0 < p.ntiles; tile0 += stride, ++n) {
+        const int tile = tile0 + tl, b = n & 1;
+        float y0 = 0.f, y1 = 0.f;                    // columns g and g + 8
+        if ((pend >> b) & 1u) {
+            const uint32_t bar = bar0 + b * 8, par = (phase >> b) & 1u;
+            const bool landed = mbar_try(bar, par) || mbar_wait(bar, par);
+            if (__all_sync(0xffffffffu, landed)) {
+                phase ^= 1u << b;
+                pend &= ~(1u << b);
+            } else {
+                ok = false;
+            }
+        }
+        if (ok && tile < p.ntiles && q < gm.kq && cz > ca) {
+            const unsigned char* tb = tbl + (size_t)ca * kLutChunk + t * 4;
+            const unsigned char* rec = buf0 + (size_t)b * gm.cpq * A::REC;
+            for (int c = ca; c < cz; ++c, rec += A::REC, tb += kLutChunk) {
+                const uint4 w = reinterpret_cast<const uint4*>(rec)[lane];
+                const uint2 sw = *reinterpret_cast<const uint2*>(rec + 512 + g * 8);
+                // x: column g, group 0; y: column g + 8, group 0; z, w: group 1
+                y0 = fmaf(h2f(side_half(sw.x, 0)), lut_word(w.x, tb), y0);
+                y1 = fmaf(h2f(side_half(sw.x, 1)), lut_word(w.y, tb), y1);
+                y0 = fmaf(h2f(side_half(sw.y, 0)), lut_word(w.z, tb + kLutHalf), y0);
+                y1 = fmaf(h2f(side_half(sw.y, 1)), lut_word(w.w, tb + kLutHalf), y1);
+            }
+        }
+        __syncwarp();
+        fence_proxy_async_if(lane == 0);                 // the buffer's reads before its refill
+        fetch(n + 2);                                    // item n + 2 into this buffer
+        // the 4 lanes of a column pair, then the quarters in order
+        y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+        y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+        part[(warp * 32 + lane) * 2] = y0;
+        part[(warp * 32 + lane) * 2 + 1] = y1;
+        __syncthreads();
+        if (q == 0 && t == 0 && tile < p.ntiles) {
+            float s0 = 0.f, s1 = 0.f;
+            for (int qq = 0; qq < gm.kq; ++qq) {
+                const float* pp = part + ((qq * kLutTiles + tl) * 32 + lane) * 2;
+                s0 += pp[0];
+                s1 += pp[1];
+            }
+            const int n0 = tile * 16 + g, n1 = n0 + 8;
+            float* yr = p.Y + (size_t)row * p.ldy;
+            if (n0 < p.N)
+                yr[n0] = s0;
+            if (n1 < p.N)
+                yr[n1] = s1;
+        }
+        __syncthreads();
+    }
+    for (int b = 0; b < 2; ++b)                      // a copy that did not land in time
+        if ((pend >> b) & 1u)
+            mbar_wait(bar0 + b * 8, (phase >> b) & 1u);
+    if (!ok && lane == 0)
+        atomicOr(p.err, 1u);
+}
+
 template <int FMT, int GROUP>
 static cudaError_t gemv_t(lbv_dtype xt, const VerifyParams& p, int row, cudaStream_t st)
 {
@@ -340,11 +526,33 @@ static cudaError_t gemv_t(lbv_dtype xt, const VerifyParams& p, int row, cudaStre
     return cudaGetLastError();
 }
 
+static cudaError_t gemv_sign1_lut(lbv_dtype xt, const VerifyParams& p, int row, cudaStream_t st)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = sign1_lut_geom(p.nchunks, p.K).end;
+    const int ctas = std::min((p.ntiles + kLutTiles - 1) / kLutTiles, std::max(sms, 1));
+    void* k = xt == LBV_F16 ? (void*)lbv_gemv_sign1_lut_kernel<LBV_F16>
+                            : (void*)lbv_gemv_sign1_lut_kernel<LBV_BF16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)std::max<size_t>(smem, 48 * 1024));
+    if (e != cudaSuccess)
+        return e;
+    if (xt == LBV_F16)
+        lbv_gemv_sign1_lut_kernel<LBV_F16><<<ctas, kLutWarps * 32, smem, st>>>(p, row);
+    else
+        lbv_gemv_sign1_lut_kernel<LBV_BF16><<<ctas, kLutWarps * 32, smem, st>>>(p, row);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemv(lbv_format fmt, lbv_dtype xt, int group, const VerifyParams& p, int row,
                         cudaStream_t st)
 {
     switch (fmt) {
     case LBV_FMT_SIGN1_G128:
+        if (sign1_lut_geom(p.nchunks, p.K).end <= (size_t)kMaxDynSmem)
+            return gemv_sign1_lut(xt, p, row, st);
         return gemv_t<LBV_FMT_SIGN1_G128, 128>(xt, p, row, st);
     case LBV_FMT_AFFINE2:
         if (group == 32)

@@ -162,6 +162,23 @@ def test_gemv_path_parity_and_dispatch():
         assert c2.plan.query(1)[0] == lbv.KERNEL_FEWROW
 
 
+@pytest.mark.parametrize("K,N,xdtype", [
+    (128, 16, "f16"), (384, 40, "bf16"), (1408, 200, "f16"), (5120, 72, "f16"),
+    (5632, 24, "bf16"), (5888, 24, "f16")])
+def test_gemv_sign1_table_path(K, N, xdtype):
+    """The 1-bit 1-row path reads its codes through a per-CTA table of signed
+    4-activation sums; K spans one chunk, ragged chunks, the largest K whose
+    table and code buffers fit in shared memory (22 chunks) and the next one
+    (the generic 1-row kernel).  Rows >= M stay untouched; repeated calls
+    agree bitwise."""
+    c = Case(synth.SIGN1_G128, K, N, 128, xdtype, seed=5, flags=lbv.PLAN_FORCE_GEMV)
+    for M in (1, 3, 8):
+        assert c.plan.query(M)[0] == lbv.KERNEL_GEMV
+        Y = c.run(M)
+        c.check(Y, M)
+        assert np.array_equal(Y, c.run(M))
+
+
 def test_pdl_back_to_back():
     """Programmatic dependent launch: a chain of calls where each call's X is
     the previous call's output (rounded to fp16 by a torch kernel in between)

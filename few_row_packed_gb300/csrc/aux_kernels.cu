@@ -325,15 +325,17 @@ __global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int
 // (j >> 1)) + 8 (j & 1) + 2 t + (i >> 2) for the lane's t = lane & 3 (the
 // few-row kernel's fragment order).  So the 4-bit field i of w selects one of
 // 16 signed sums of four activations:
-//   T[c][H][i][v][t] = sum_j (bit j of v ? +x_k : -x_k),
+//   T[c][H][i][t][v] = sum_j (bit j of v ? +x_k : -x_k),
 // which each CTA tabulates once in shared memory, and a group's dot product
 // is 8 table reads per word.  Warps take (tile, K quarter) items, four tiles
 // per CTA at a time; each warp fetches an item's records with one bulk copy
 // into one of two buffers, the next item's while it works on the current one
 // (the first two are issued before the table is built), and the four
 // quarters' partial sums of a tile meet in shared memory and are added in
-// quarter order.  Table rows of one field are 272 bytes apart, so the 8 fields a
-// warp writes or reads at once fall in different banks.
+// quarter order.  Within a (chunk, half, field) row of 272 bytes, entry
+// (t, v) sits at word 16 t + v: the 16 values of one t take 16 different
+// banks, so a warp's read conflicts only between lanes t and t + 2 that pick
+// the same value.
 constexpr int kLutWarps = 16, kLutTiles = kLutWarps / 4;
 constexpr int kLutField = 272;                       // bytes per (chunk, half, field): 16 x 4 floats + pad
 constexpr int kLutHalf = 8 * kLutField;
@@ -361,13 +363,13 @@ __host__ __device__ inline Sign1LutGeom sign1_lut_geom(int nchunks, int K)
 }
 
 // Sum of the 8 table entries that word w's fields select; tb points at the
-// (chunk, half) block for this lane's t (entries 16 bytes apart by value).
+// (chunk, half) block plus this lane's t (entries 4 bytes apart by value).
 __device__ __forceinline__ float lut_word(uint32_t w, const unsigned char* tb)
 {
     float e[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t off = i == 0 ? (w << 4) & 0xF0u : (w >> (4 * i - 4)) & 0xF0u;
+        const uint32_t off = i == 0 ? (w << 2) & 0x3Cu : (w >> (4 * i - 2)) & 0x3Cu;
         e[i] = *reinterpret_cast<const float*>(tb + i * kLutField + off);
     }
     return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
@@ -436,10 +438,10 @@ __global__ void __launch_bounds__(kLutWarps * 32) lbv_gemv_sign1_lut_kernel(cons
         const float a[4] = {-xv[0] - xv[1], xv[0] - xv[1], -xv[0] + xv[1], xv[0] + xv[1]};
         const float b[4] = {-xv[2] - xv[3], xv[2] - xv[3], -xv[2] + xv[3], xv[2] + xv[3]};
         float* out = reinterpret_cast<float*>(tbl + (size_t)c * kLutChunk + H * kLutHalf +
-                                              i * kLutField) + tt;
+                                              i * kLutField) + 16 * tt;
 #pragma unroll
         for (int v = 0; v < 16; ++v)
-            out[v * 4] = a[v & 3] + b[v >> 2];
+            out[v] = a[v & 3] + b[v >> 2];
     }
     __syncthreads();
 
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kLutWarps * 32) lbv_gemv_sign1_lut_kernel(cons
             }
         }
         if (ok && tile < p.ntiles && q < gm.kq && cz > ca) {
-            const unsigned char* tb = tbl + (size_t)ca * kLutChunk + t * 4;
+            const unsigned char* tb = tbl + (size_t)ca * kLutChunk + t * 64;
             const unsigned char* rec = buf0 + (size_t)b * gm.cpq * A::REC;
             for (int c = ca; c < cz; ++c, rec += A::REC, tb += kLutChunk) {
                 const uint4 w = reinterpret_cast<const uint4*>(rec)[lane];

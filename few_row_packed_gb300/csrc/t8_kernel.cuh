@@ -716,13 +716,15 @@ struct T8Kernel {
             // parks it and reduces the tile parked before, whose partials
             // arrived a tile ago
             auto epilogue = [&](int e) -> bool {
+                // the group's constants first: their shared loads then overlap the
+                // wait for the MMAs and the accumulator read instead of following it
+                const float4* e4 = reinterpret_cast<const float4*>(ep + ge * 16);
+                const float4 Ua = e4[0], Ub = e4[1], Ra = e4[2], Rb = e4[3];
                 if (!mbar_wait(bar_done + (wg * 2 + (e & 1)) * 8, (uint32_t)((e >> 1) & 1)))
                     return false;
                 t8::tc_fence_after();
                 float d[24];
                 t8::tmem_ld24(ta + 64u + (uint32_t)((e & 1) * 32), d);
-                const float4* e4 = reinterpret_cast<const float4*>(ep + ge * 16);
-                const float4 Ua = e4[0], Ub = e4[1], Ra = e4[2], Rb = e4[3];
                 const uint64_t U2[4] = {t8::f2pack(Ua.x, Ua.y), t8::f2pack(Ua.z, Ua.w),
                                         t8::f2pack(Ub.x, Ub.y), t8::f2pack(Ub.z, Ub.w)};
                 const uint64_t R2[4] = {t8::f2pack(Ra.x, Ra.y), t8::f2pack(Ra.z, Ra.w),

@@ -678,13 +678,13 @@ struct T8Kernel {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 Y2[i] = 0ull;
-            float s_prev = 0.f, b_prev = 0.f;        // scale, bias of the group behind
+            uint32_t sb_prev = 0u;                   // side word (fp16 scale, bias) of the group behind
             float pend[8];                           // an owned tile's own partial, parked
             int pend_li = -1;
             int consumed = 0;                        // ring stages read
             int ge = 0, te = 0;                      // epilogue cursor: group, tile index
             uint4 cw[CB / 16];                       // codes of the next group to decode
-            float s_nx = 0.f, b_nx = 0.f;
+            uint32_t sb_nx = 0u;                     // converted where it is used, one group later
             // loads group gl's codes and side values (waiting for its stage
             // first when gl opens one)
             auto load_group = [&](int gl) -> bool {
@@ -699,14 +699,10 @@ struct T8Kernel {
 #pragma unroll
                 for (int i = 0; i < CB / 16; ++i)
                     cw[i] = *reinterpret_cast<const uint4*>(rec + i * 512 + lane * 16);
-                if constexpr (W == 2) {
-                    const float2 f = f16pair(*reinterpret_cast<const uint32_t*>(rec + CB * 32 + lane * 4));
-                    s_nx = f.x;
-                    b_nx = f.y;
-                } else {
-                    s_nx = __half2float(__ushort_as_half(
-                        *reinterpret_cast<const uint16_t*>(rec + CB * 32 + lane * 2)));
-                }
+                if constexpr (W == 2)
+                    sb_nx = *reinterpret_cast<const uint32_t*>(rec + CB * 32 + lane * 4);
+                else
+                    sb_nx = *reinterpret_cast<const uint16_t*>(rec + CB * 32 + lane * 2);
                 if (gi == GPS - 1 || gl == gcnt - 1)
                     ++consumed;
                 return true;
@@ -731,8 +727,9 @@ struct T8Kernel {
                                         t8::f2pack(Rb.x, Rb.y), t8::f2pack(Rb.z, Rb.w)};
                 const uint64_t k16 = t8::f2pack(1.f / 16.f, 1.f / 16.f);
                 const uint64_t k256 = t8::f2pack(1.f / 256.f, 1.f / 256.f);
-                const uint64_t s2 = t8::f2pack(s_prev, s_prev);
-                const uint64_t b2 = W == 2 ? t8::f2pack(b_prev, b_prev) : t8::f2pack(2.f, 2.f);
+                const float2 sb = f16pair(sb_prev);   // (scale, bias); sign1: (scale, 0)
+                const uint64_t s2 = t8::f2pack(sb.x, sb.x);
+                const uint64_t b2 = W == 2 ? t8::f2pack(sb.y, sb.y) : t8::f2pack(2.f, 2.f);
                 // rows 2i, 2i + 1 at once:
                 //   acc = U (d0 + d1 / 16 + d2 / 256)  (the three terms of X)
                 //   affine2: Y += s acc + b R;  sign1: Y += s (2 acc - R)
@@ -794,7 +791,7 @@ struct T8Kernel {
                 if (lane == 0)
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n"
                                  ::"r"(bar_full + (wg * 2 + (c & 1)) * 8) : "memory");
-                const float s_c = s_nx, b_c = b_nx;
+                const uint32_t sb_c = sb_nx;
                 if (++g == gcnt)
                     g = 0;
                 const bool loaded = c + 1 >= total || load_group(g);
@@ -806,8 +803,7 @@ struct T8Kernel {
                     ok = false;
                     break;
                 }
-                s_prev = s_c;
-                b_prev = b_c;
+                sb_prev = sb_c;
             }
             if (ok && total > 0 && !epilogue(total - 1))
                 ok = false;

@@ -776,8 +776,8 @@ struct T8Kernel {
                 return true;
             };
             // Per group c: decode (codes loaded one group ahead), tensor-memory
-            // store, load group c + 1 while the store completes, arrive (the
-            // MMAs of c run meanwhile), then the epilogue of group c - 1.
+            // store, arrive (the MMAs of c run meanwhile), load group c + 1,
+            // then the epilogue of group c - 1.
             if (total > 0 && !load_group(0))
                 ok = false;
             int g = 0;                               // decode cursor (slice-local group)

@@ -647,15 +647,16 @@ struct T8Kernel {
                     ok = false;
                     break;
                 }
+                t8::tc_fence_after();
+                t8::mma_group(tm_wg + 64u + (uint32_t)slot * 32u, tm_wg + (uint32_t)slot * 32u,
+                              t8::b_desc(smem_u32(bsm) + (uint32_t)g * 4096u),
+                              bar_done + (wg * 2 + slot) * 8);
+                // after the MMAs, so that a full copy queue stalls only the refill
                 if ((g % GPS) == GPS - 1 || g == gcnt - 1) {
                     if (lane == 0 && issued < nstage)
                         issue_s(issued);
                     issued = min(issued + 1, nstage);
                 }
-                t8::tc_fence_after();
-                t8::mma_group(tm_wg + 64u + (uint32_t)slot * 32u, tm_wg + (uint32_t)slot * 32u,
-                              t8::b_desc(smem_u32(bsm) + (uint32_t)g * 4096u),
-                              bar_done + (wg * 2 + slot) * 8);
                 done_n = c + 1;
                 if (++g == gcnt)
                     g = 0;

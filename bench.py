@@ -22,6 +22,7 @@ owns its own stack).  value = bytes of all ranks / max time over ranks.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -324,6 +325,23 @@ class Stack:
                                  idx=self.idx, val=self.val, workspace=self.ws)
 
 
+@contextlib.contextmanager
+def nvtx_range(name):
+    """An NVTX range around a phase of the bench, for Nsight timelines; a
+    no-op where torch was built without NVTX.  Host-side markers only."""
+    import torch
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pushed = False
+    try:
+        yield
+    finally:
+        if pushed:
+            torch.cuda.nvtx.range_pop()
+
+
 def timed(torch, fn, steps, warmup, barrier):
     for _ in range(warmup):
         fn()
@@ -560,18 +578,22 @@ def measure_config(args, workload, stack_mode, l2, peak, barrier, reduce_max, wo
     context.  Returns (summary dict, Stack, extra headline fields)."""
     import torch
 
-    stack = Stack(workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
-                  use_graphs=not args.no_graph, head=args.head, stack=stack_mode,
-                  measure=not args.no_measure)
-    grouped = stack.group is not None
-    rotated = any(l[0].rotate for l in stack.layers)
-    stack.run(args.M)
-    t_end = time.time() + (0.0 if args.quick else 1.0)
-    while time.time() < t_end:
-        for _ in range(max(1, args.warmup)):
-            stack.run(args.M)
-        torch.cuda.synchronize()
-    ms = reduce_max(timed(torch, lambda: stack.run(args.M), args.steps, args.warmup, barrier))
+    tag = f"lbv/{workload}" + (f"/{stack_mode}" if stack_mode else "")
+    with nvtx_range(f"{tag}/setup"):
+        stack = Stack(workload, not args.no_pdl, args.shape, l2, args.M, kernel=args.kernel,
+                      use_graphs=not args.no_graph, head=args.head, stack=stack_mode,
+                      measure=not args.no_measure)
+        grouped = stack.group is not None
+        rotated = any(l[0].rotate for l in stack.layers)
+        stack.run(args.M)
+        t_end = time.time() + (0.0 if args.quick else 1.0)
+        while time.time() < t_end:
+            for _ in range(max(1, args.warmup)):
+                stack.run(args.M)
+            torch.cuda.synchronize()
+    with nvtx_range(f"{tag}/timed M={args.M}"):
+        ms = reduce_max(timed(torch, lambda: stack.run(args.M), args.steps, args.warmup,
+                              barrier))
     ms_per_step = ms / args.steps
     bytes_step = stack.bytes_per_step[args.M]
     value = replica_value(bytes_step, world, ms_per_step)
@@ -579,8 +601,9 @@ def measure_config(args, workload, stack_mode, l2, peak, barrier, reduce_max, wo
     # the dominant kernel: the verify launch, timed alone (verify-only loop)
     # when the step also launches the separate rotation
     if rotated and args.head == "two-call":
-        ms_v = reduce_max(timed(torch, lambda: stack.run(args.M, verify_only=True), args.steps,
-                                args.warmup, barrier))
+        with nvtx_range(f"{tag}/verify only"):
+            ms_v = reduce_max(timed(torch, lambda: stack.run(args.M, verify_only=True),
+                                    args.steps, args.warmup, barrier))
     else:
         ms_v = ms
     verify_launches = stack.group.launches() if grouped else stack.calls
@@ -592,7 +615,8 @@ def measure_config(args, workload, stack_mode, l2, peak, barrier, reduce_max, wo
     if not args.no_sweep:
         for M in range(1, 9):
             n = max(10, args.steps // 2)
-            msm = reduce_max(timed(torch, lambda: stack.run(M), n, args.warmup, barrier))
+            with nvtx_range(f"{tag}/sweep M={M}"):
+                msm = reduce_max(timed(torch, lambda: stack.run(M), n, args.warmup, barrier))
             us = msm * 1e3 / (n * stack.calls)
             gbs = stack.bytes_per_step[M] / stack.calls / (us * 1e-6) / 1e9
             per_M[str(M)] = {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
@@ -623,10 +647,12 @@ def measure_config(args, workload, stack_mode, l2, peak, barrier, reduce_max, wo
              "achieved": achieved, "bytes_launch": bytes_launch, "us_launch": us_launch,
              "grouped": grouped, "rotated": rotated, "kernel_key": "grouped" if grouped else args.kernel}
     if headline:
-        extra["e2e"] = e2e_measure(args, stack, bytes_step, world, barrier, reduce_max)
+        with nvtx_range(f"{tag}/e2e"):
+            extra["e2e"] = e2e_measure(args, stack, bytes_step, world, barrier, reduce_max)
         if not args.no_dense:
-            dense = dense_context(stack, args.M, l2, max(3, args.steps // 4), args.warmup, peak,
-                                  barrier, reduce_max)
+            with nvtx_range(f"{tag}/dense fp16 context"):
+                dense = dense_context(stack, args.M, l2, max(3, args.steps // 4), args.warmup,
+                                      peak, barrier, reduce_max)
             dense["packed_speedup"] = round(dense["us_per_call"] / (ms_per_step * 1e3 / stack.calls), 2)
             extra["dense"] = dense
     return summary, stack, extra

@@ -88,6 +88,11 @@ def lib():
             "lbv_plan_measured": (st, [P, I, ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
             "lbv_plan_device_status": (st, [P]),
+            "lbv_plan_rows_histogram": (st, [P, P]),
+            "lbv_plan_rows_reset": (st, [P]),
+            "lbv_group_rows_histogram": (st, [P, P]),
+            "lbv_group_rows_reset": (st, [P]),
+            "lbv_rows_histogram": (st, [P]),
             "lbv_verify_gemm": (st, [P, P, I, I, P, P, I, P, S, P]),
             "lbv_fwht128": (st, [P, P, I, I, I, P, P]),
             "lbv_fused_workspace_bytes": (S, []),
@@ -260,6 +265,13 @@ class Plan:
                                        ctypes.byref(c)))
         return f.value, g.value, c.value
 
+    def rows_histogram(self):
+        """{M: calls} over the plan's successful verify calls since creation or reset."""
+        return _rows(lambda c: lib().lbv_plan_rows_histogram(self.handle, c))
+
+    def rows_reset(self):
+        _check(lib().lbv_plan_rows_reset(self.handle))
+
 
 class Group:
     """A grouped-verify plan: problems of shapes K[i] x N[i], one format."""
@@ -304,6 +316,24 @@ class Group:
 
     def device_status(self):
         _check(lib().lbv_group_device_status(self.handle))
+
+    def rows_histogram(self):
+        """{M: active problems} over the group's successful calls since creation or reset."""
+        return _rows(lambda c: lib().lbv_group_rows_histogram(self.handle, c))
+
+    def rows_reset(self):
+        _check(lib().lbv_group_rows_reset(self.handle))
+
+
+def _rows(call):
+    c = (ctypes.c_uint64 * 8)()
+    _check(call(c))
+    return {m: int(c[m - 1]) for m in range(1, 9)}
+
+
+def rows_histogram():
+    """{M: calls} over every plan and group of the process since the library loaded."""
+    return _rows(lambda c: lib().lbv_rows_histogram(c))
 
 
 def verify_grouped(group: Group, problems, stream=None):

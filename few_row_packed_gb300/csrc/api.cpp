@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -36,6 +37,38 @@ lbv_status cuda_fail(cudaError_t e, const char* what)
 {
     return fail(LBV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
+
+// Rows-per-call counts of the whole process ([m - 1]: calls or active grouped
+// problems with M = m), and the report at exit that LBV_VERIFY_STATS=1 asks
+// for ("dflash-mlx-bonsai2" README, Commands: a rows-per-call histogram of the
+// verify, printed at exit).
+std::atomic<unsigned long long> g_rows[8];
+
+void count_rows(std::atomic<unsigned long long> (&own)[8], int M)
+{
+    own[M - 1].fetch_add(1, std::memory_order_relaxed);
+    g_rows[M - 1].fetch_add(1, std::memory_order_relaxed);
+}
+
+struct RowsReport {
+    ~RowsReport()
+    {
+        const char* v = getenv("LBV_VERIFY_STATS");
+        if (!v || !*v || strcmp(v, "0") == 0)
+            return;
+        unsigned long long calls = 0, rows = 0;
+        for (int m = 1; m <= 8; ++m) {
+            const unsigned long long c = g_rows[m - 1].load(std::memory_order_relaxed);
+            calls += c;
+            rows += c * (unsigned long long)m;
+        }
+        fprintf(stderr, "lbv: verify rows per call:");
+        for (int m = 1; m <= 8; ++m)
+            fprintf(stderr, " %d:%llu", m, g_rows[m - 1].load(std::memory_order_relaxed));
+        fprintf(stderr, " (calls %llu, mean rows %.2f)\n", calls,
+                calls ? (double)rows / (double)calls : 0.0);
+    }
+} g_rows_report;
 
 const lbv::VerifyOps* ops_for(lbv_format fmt, int group)
 {
@@ -520,6 +553,26 @@ lbv_status lbv_plan_device_status(const lbv_plan* P)
     return LBV_OK;
 }
 
+lbv_status lbv_plan_rows_histogram(const lbv_plan* P, uint64_t* counts)
+{
+    g_err.clear();
+    if (!P || !counts)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_rows_histogram: NULL plan or counts");
+    for (int m = 0; m < 8; ++m)
+        counts[m] = P->rows_calls[m].load(std::memory_order_relaxed);
+    return LBV_OK;
+}
+
+lbv_status lbv_plan_rows_reset(lbv_plan* P)
+{
+    g_err.clear();
+    if (!P)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_plan_rows_reset: plan is NULL");
+    for (int m = 0; m < 8; ++m)
+        P->rows_calls[m].store(0, std::memory_order_relaxed);
+    return LBV_OK;
+}
+
 lbv_status lbv_plan_query(const lbv_plan* P, int M, int* kernel_id, int* splits,
                           size_t* workspace_bytes)
 {
@@ -702,8 +755,11 @@ lbv_status lbv_verify_gemm(const lbv_plan* P, const void* X, int M, int ldx, con
                                       workspace_bytes);
     if (st != LBV_OK)
         return st;
-    return lbv_verify_launch_internal(P, X, M, ldx, Wp, Y, ldy, P->use_gemv[M] != 0,
-                                      reinterpret_cast<cudaStream_t>(stream));
+    st = lbv_verify_launch_internal(P, X, M, ldx, Wp, Y, ldy, P->use_gemv[M] != 0,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (st == LBV_OK)
+        count_rows(P->rows_calls, M);
+    return st;
 }
 
 // --------------------------------------------------------------------------
@@ -776,6 +832,7 @@ lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, co
                                                     reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess)
             return cuda_fail(e, "lbv_verify_fused: launch");
+        count_rows(P->rows_calls, M);
         return LBV_OK;
     }
     lbv::VerifyParams p = make_params(P, X, M, ldx, Wp, Y, Y ? ldy : P->N);
@@ -795,6 +852,7 @@ lbv_status lbv_verify_fused(const lbv_plan* P, const void* X, int M, int ldx, co
                                        reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "lbv_verify_fused: launch");
+    count_rows(P->rows_calls, M);
     return LBV_OK;
 }
 
@@ -1733,5 +1791,38 @@ lbv_status lbv_verify_grouped(const lbv_group* G, const lbv_problem* problems, l
         if (st != LBV_OK)
             return st;
     }
+    for (int i = 0; i < G->count; ++i)
+        if (M[i] > 0)
+            count_rows(G->rows_calls, M[i]);
+    return LBV_OK;
+}
+
+lbv_status lbv_group_rows_histogram(const lbv_group* G, uint64_t* counts)
+{
+    g_err.clear();
+    if (!G || !counts)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_rows_histogram: NULL group or counts");
+    for (int m = 0; m < 8; ++m)
+        counts[m] = G->rows_calls[m].load(std::memory_order_relaxed);
+    return LBV_OK;
+}
+
+lbv_status lbv_group_rows_reset(lbv_group* G)
+{
+    g_err.clear();
+    if (!G)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_group_rows_reset: group is NULL");
+    for (int m = 0; m < 8; ++m)
+        G->rows_calls[m].store(0, std::memory_order_relaxed);
+    return LBV_OK;
+}
+
+lbv_status lbv_rows_histogram(uint64_t* counts)
+{
+    g_err.clear();
+    if (!counts)
+        return fail(LBV_ERR_INVALID_ARG, "lbv_rows_histogram: counts is NULL");
+    for (int m = 0; m < 8; ++m)
+        counts[m] = g_rows[m].load(std::memory_order_relaxed);
     return LBV_OK;
 }

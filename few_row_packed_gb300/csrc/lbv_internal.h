@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "layout.h"
 #include "t8_layout.h"
 #include "tc_layout.h"
@@ -131,6 +133,9 @@ struct lbv_group {
     int ntiles[lbv::kMaxGroup], nchunks[lbv::kMaxGroup], cps[lbv::kMaxGroup];
     double bytes[lbv::kMaxGroup];              // packed bytes of each problem
     unsigned* dev_err;
+    // rows-per-call counts: [m - 1] = active problems with M = m, over the
+    // calls that enqueued their launches
+    mutable std::atomic<unsigned long long> rows_calls[8];
 };
 
 struct lbv_plan {
@@ -156,4 +161,7 @@ struct lbv_plan {
     lbv::T8FmtInfo t8_fi;
     lbv::T8Layout t8_layout;
     lbv::T8Shape t8_shape;
+    // rows-per-call counts: [m - 1] = verify calls with M = m that enqueued
+    // their launches (the plan's own launch measurement is not counted)
+    mutable std::atomic<unsigned long long> rows_calls[8];
 };

@@ -235,6 +235,21 @@ LBV_API lbv_status lbv_plan_measured(const lbv_plan* plan, int M, float* fewrow_
  * Synchronises with the device. */
 LBV_API lbv_status lbv_plan_device_status(const lbv_plan* plan);
 
+/*
+ * Rows-per-call statistics ("dflash-mlx-bonsai2" README, Commands: the fork
+ * keeps a histogram of how many drafted rows each verify call carried and
+ * prints it at exit on request).  counts: host array of 8; counts[m - 1] =
+ * the calls of this plan with M = m (lbv_verify_gemm, lbv_verify_fused,
+ * lbv_verify_fused_noalloc) that returned LBV_OK since the plan was created
+ * or last reset.  Failed calls and the plan's own launch measurement are not
+ * counted.  A call counts when it is enqueued: one captured into a CUDA graph
+ * counts once, at capture, since the graph's replays do not pass through the
+ * library.  Counting is atomic: plans stay safe to share between threads.
+ * LBV_ERR_INVALID_ARG for a NULL plan or counts.
+ */
+LBV_API lbv_status lbv_plan_rows_histogram(const lbv_plan* plan, uint64_t* counts);
+LBV_API lbv_status lbv_plan_rows_reset(lbv_plan* plan);
+
 /* ------------------------------------------------------------------------ */
 /* The verify matmul.                                                         */
 
@@ -411,6 +426,20 @@ LBV_API lbv_status lbv_verify_grouped(const lbv_group* group, const lbv_problem*
 
 /* As lbv_plan_device_status, for the group's kernels. */
 LBV_API lbv_status lbv_group_device_status(const lbv_group* group);
+
+/* As lbv_plan_rows_histogram, per active problem of each lbv_verify_grouped
+ * call that returned LBV_OK: counts[m - 1] = problems run with M = m. */
+LBV_API lbv_status lbv_group_rows_histogram(const lbv_group* group, uint64_t* counts);
+LBV_API lbv_status lbv_group_rows_reset(lbv_group* group);
+
+/*
+ * The same counts over every plan and group of the process since the library
+ * was loaded (not reset by the calls above).  With the environment variable
+ * LBV_VERIFY_STATS set (and not "0"), the library prints them to stderr when
+ * the process exits: one line, "lbv: verify rows per call: 1:n1 ... 8:n8
+ * (calls C, mean rows R)".
+ */
+LBV_API lbv_status lbv_rows_histogram(uint64_t* counts);
 
 /*
  * Test export: X' exactly as lbv_verify_fused with LBV_FUSED_ROTATE computes

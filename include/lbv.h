@@ -176,7 +176,10 @@ LBV_API lbv_status lbv_pack_q4_0(const uint8_t* blocks, int K, int N, void* out,
 
 /* Creates a plan for the current device.  Returns LBV_ERR_INVALID_ARG for
  * K, N <= 0 or a K the format cannot hold, LBV_ERR_UNSUPPORTED for a group
- * other than 32/64/128 (affine2).  *out is NULL on failure. */
+ * other than 32/64/128 (affine2) or a K so large that no K split (at most 8
+ * CTAs) leaves each CTA's slice of X room in shared memory beside its weight
+ * ring: on GB300 about 44-53 thousand, by format and activation dtype.  *out
+ * is NULL on failure. */
 LBV_API lbv_status lbv_plan_create(lbv_format fmt, int K, int N, int group, lbv_dtype xdtype,
                            unsigned flags, lbv_plan** out);
 LBV_API lbv_status lbv_plan_destroy(lbv_plan* plan);

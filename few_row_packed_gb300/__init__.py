@@ -34,10 +34,13 @@ KERNEL_FEWROW_TC8 = 4
 FUSED_ROTATE = 0x1
 FUSED_ARGMAX = 0x2
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT, ERR_BOUNDS = range(7)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "liblbv.so")
+# LBV_LIBRARY=checked selects liblbv_checked.so, the build whose kernels check
+# their copy and buffer ranges; the default is the release liblbv.so
+CHECKED = os.environ.get("LBV_LIBRARY", "") == "checked"
+LIB_PATH = os.path.join(_HERE, "liblbv_checked.so" if CHECKED else "liblbv.so")
 _lib = None
 
 FMT_BY_NAME = {"sign1_g128": FMT_SIGN1_G128, "affine2": FMT_AFFINE2, "q4_0": FMT_Q4_0}
@@ -57,9 +60,9 @@ class LbvError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compile liblbv.so in-tree for sm_103a (nvcc); returns its path."""
+    """Compile the library LIB_PATH names in-tree for sm_103a (nvcc); returns its path."""
     from . import buildlib
-    return buildlib.build(force=force)
+    return buildlib.build(force=force, checked=CHECKED)
 
 
 def lib():
@@ -110,6 +113,7 @@ def lib():
             "lbv_dequant_fp16": (st, [P, P, P, P]),
             "lbv_last_error": (ctypes.c_char_p, []),
             "lbv_version": (ctypes.c_char_p, []),
+            "lbv_checked_build": (I, []),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -3,6 +3,11 @@
 Each translation unit is compiled in parallel, then linked into
 few_row_packed_gb300/liblbv.so (git-ignored).  No cmake, no torch extension
 machinery: the library is a plain C ABI (include/lbv.h).
+
+build(checked=True) makes liblbv_checked.so instead: the same sources with
+LBV_CHECKED defined, whose kernels check their copy and buffer ranges, record
+a bounds error in the plan's status word and skip the access (the release
+library's device code is unchanged by those checks).
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblbv.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "liblbv_checked.so")
 
 SOURCES = [
     "api.cpp",
@@ -57,22 +64,24 @@ def _deps():
     return files
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    lib, bdir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
+    flags = FLAGS + (["-DLBV_CHECKED"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -83,14 +92,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     jobs = min(len(SOURCES), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(jobs) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

@@ -210,6 +210,15 @@ const char* lbv_version(void)
     return "lbv 0.1.0 (sm_103a)";
 }
 
+int lbv_checked_build(void)
+{
+#ifdef LBV_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 size_t lbv_packed_bytes(lbv_format fmt, int K, int N, int group)
 {
     lbv::FmtInfo fi;
@@ -548,6 +557,9 @@ lbv_status lbv_plan_device_status(const lbv_plan* P)
         return cuda_fail(e, "lbv_plan_device_status");
     if (v) {
         cudaMemset(P->dev_err, 0, sizeof v);
+        if (v & 2u)
+            return fail(LBV_ERR_BOUNDS, "a kernel of this plan found a copy or buffer range "
+                                        "outside its bounds and skipped it");
         return fail(LBV_ERR_TIMEOUT, "a verify kernel gave up waiting for its weight copies");
     }
     return LBV_OK;
@@ -1753,6 +1765,9 @@ lbv_status lbv_group_device_status(const lbv_group* G)
         return cuda_fail(e, "lbv_group_device_status");
     if (v) {
         cudaMemset(G->dev_err, 0, sizeof v);
+        if (v & 2u)
+            return fail(LBV_ERR_BOUNDS, "a grouped verify kernel found a copy or buffer range "
+                                        "outside its bounds and skipped it");
         return fail(LBV_ERR_TIMEOUT, "a grouped verify kernel gave up waiting for its weight copies");
     }
     return LBV_OK;

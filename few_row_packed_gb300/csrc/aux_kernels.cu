@@ -234,6 +234,19 @@ __global__ void __launch_bounds__(256) lbv_gemv_kernel(const VerifyParams p, int
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const uint16_t* x = reinterpret_cast<const uint16_t*>(p.X) + (size_t)row * p.ldx;
     const int kpad = p.nchunks * A::CK;
+#ifdef LBV_CHECKED
+    {
+        // checked build: the fp32 row fits the launch's shared memory and the
+        // row lies inside X's rows
+        uint32_t dyn;
+        asm volatile("mov.u32 %0, %%dynamic_smem_size;\n" : "=r"(dyn));
+        if ((size_t)kpad * sizeof(float) > dyn || row < 0 || row >= p.M || kpad < p.K) {
+            if (threadIdx.x == 0)
+                atomicOr(p.err, 2u);
+            return;
+        }
+    }
+#endif
     for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
         float v = 0.f;
         if (k < p.K) {
@@ -382,6 +395,19 @@ __global__ void __launch_bounds__(kLutWarps * 32) lbv_gemv_sign1_lut_kernel(cons
     using A = AuxTraits<LBV_FMT_SIGN1_G128, 128>;
     extern __shared__ __align__(128) unsigned char smem[];
     const Sign1LutGeom gm = sign1_lut_geom(p.nchunks, p.K);
+#ifdef LBV_CHECKED
+    {
+        // checked build: the table kernel's carve-up fits the launch's shared
+        // memory and the row lies inside X's rows
+        uint32_t dyn;
+        asm volatile("mov.u32 %0, %%dynamic_smem_size;\n" : "=r"(dyn));
+        if (gm.end > dyn || row < 0 || row >= p.M) {
+            if (threadIdx.x == 0)
+                atomicOr(p.err, 2u);
+            return;
+        }
+    }
+#endif
     unsigned char* tbl = smem + gm.table;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + gm.xrow);
     float* part = reinterpret_cast<float*>(smem + gm.part);

@@ -848,6 +848,13 @@ struct VerifyKernel {
                 cg::cluster_group cl = cg::this_cluster();
                 const int S = p.splits;
                 const int i = tile - tbase;
+#ifdef LBV_CHECKED
+                // the slot lies inside the owner's partial buffer
+                if (i < 0 || (i / S + 1) * S > (t1 - tbase + S - 1) / S * S) {
+                    atomicOr(p.err, 2u);
+                    continue;
+                }
+#endif
                 float* dst = cl.map_shared_rank(part, (unsigned)(i % S)) +
                              ((i / S) * S + (int)cl.block_rank()) * 128;
 #pragma unroll
@@ -887,6 +894,36 @@ struct VerifyKernel {
         }
     }
 
+#ifdef LBV_CHECKED
+    // Checked build: walks a warp's whole copy schedule (the cursor the loads
+    // follow) and checks that every copy reads inside the packed matrix and
+    // fits its ring slot.  False (and the bounds bit set) if one does not; the
+    // warp then issues nothing and does no work.
+    static __device__ bool copies_in_range(const VerifyParams& p, int t0, int t1, int c0, int nch,
+                                           int nstage, int nu, int warp, int lane)
+    {
+        const uint8_t* end = p.W + (size_t)p.ntiles * p.nchunks * G::REC;
+        const size_t tstride = (size_t)p.nchunks * G::REC;
+        Cursor c;
+        c.unit = warp;
+        c.stage = 0;
+        if (nu > 0)
+            cursor_set(p, t0, t1, c0, nch, c);
+        for (int i = 0; i < nu * nstage; ++i) {
+            const bool ok = c.nvalid >= 1 && c.nvalid <= TPW && c.nc >= 1 && c.nc <= G::CPS &&
+                            c.rec >= p.W &&
+                            c.rec + (size_t)(c.nvalid - 1) * tstride + (size_t)c.nc * G::REC <= end;
+            if (!ok) {
+                if (lane == 0)
+                    atomicOr(p.err, 2u);
+                return false;
+            }
+            cursor_next(p, t0, t1, c0, nch, nstage, c);
+        }
+        return true;
+    }
+#endif
+
     // Stage X[0..8) x [kb, kb + nch*CHUNK_K) in fragment order (rows >= M
     // and K >= p.K are zero).
     // X slice [kb, kb + nch * CHUNK_K) of rows m < M, row-major at xs + m * RS.
@@ -899,6 +936,15 @@ struct VerifyKernel {
     {
         const int kb = c0 * T::CHUNK_K;
         const int span = nch * T::CHUNK_K;                   // elements per row slice
+#ifdef LBV_CHECKED
+        // the slice starts inside K and fits the row buffer: otherwise nothing
+        // is staged (the result is then wrong and the status says so)
+        if (kb > p.K || nch < 1 || span * 2 + 16 > RS) {
+            if (threadIdx.x == 0)
+                atomicOr(p.err, 2u);
+            return false;
+        }
+#endif
         const int have = min(span, p.K - kb);                // elements inside K (K % 16 == 0)
         const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
         if (p.x_vec) {
@@ -1067,6 +1113,23 @@ struct VerifyKernel {
         float* corr = reinterpret_cast<float*>(xs + (size_t)8 * RS);
         float* rsum = corr + p.cps * T::GPC * 16;
         float* part = rsum + (T::AFFINE ? p.cps * T::GPC * 8 : 0);
+#ifdef LBV_CHECKED
+        // Checked build: the carve-up, with the partial slots of a K split, ends
+        // inside the launch's dynamic shared memory.  The test reads only values
+        // a cluster's CTAs share (the launch, t0, t1), so a cluster leaves whole
+        // and no CTA is left waiting at a cluster barrier.
+        {
+            const size_t need = (size_t)(reinterpret_cast<unsigned char*>(part) - smem) +
+                                (S > 1 ? (size_t)((t1 - t0 + S - 1) / S) * S * 512u : 0u);
+            uint32_t dyn;
+            asm volatile("mov.u32 %0, %%dynamic_smem_size;\n" : "=r"(dyn));
+            if (need > dyn || p.M < 1 || p.M > 8 || p.cps < 1) {
+                if (threadIdx.x == 0)
+                    atomicOr(p.err, 2u);
+                return;
+            }
+        }
+#endif
 
         const uint32_t ring_w = smem_u32(ring) + warp * STAGES * G::SLOT_B;
         const uint32_t bars_w = smem_u32(bars) + warp * STAGES * 8;
@@ -1102,7 +1165,11 @@ struct VerifyKernel {
         // Packed weights are read-only: start streaming before waiting on the
         // previous kernel in the stream.
         const int nstage = (nch + G::CPS - 1) / G::CPS;
+#ifdef LBV_CHECKED
+        const int Q = copies_in_range(p, t0, t1, c0, nch, nstage, nu, warp, lane) ? nu * nstage : 0;
+#else
         const int Q = nu * nstage;
+#endif
         const uint32_t leader = lane == 0;
         // wait-limit test (LBV_PLAN_TEST_WAIT_LIMIT): the first warp of the
         // first CTA does not issue its ring stage skip_q, so its wait on that
@@ -1215,6 +1282,15 @@ struct VerifyKernel {
                 slot = 0;
                 parity ^= 1u;
             }
+#ifdef LBV_CHECKED
+            // the stage's chunks lie inside the staged X slice and its corrections
+            if (nc < 1 || cc + nc > p.cps) {
+                if (lane == 0)
+                    atomicOr(p.err, 2u);
+                ok = false;
+                break;
+            }
+#endif
 #pragma unroll
             for (int ci = 0; ci < G::CPS; ++ci)
                 if (ci == 0 || ci < nc)
@@ -1272,6 +1348,12 @@ struct VerifyKernel {
         unsigned long long best = 0ull;
         for (int e = (int)threadIdx.x; e < nown * 128; e += NW * 32) {
             const int k = e >> 7, r = e & 127;
+#ifdef LBV_CHECKED
+            if ((k + 1) * S > (t1 - t0 + S - 1) / S * S) {   // inside the partial buffer
+                atomicOr(p.err, 2u);
+                continue;
+            }
+#endif
             const float* src = part + (k * S) * 128 + r;
             float acc = 0.f;
             for (int q = 0; q < S; ++q)

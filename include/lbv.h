@@ -51,7 +51,9 @@ typedef enum {
     LBV_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement     */
     LBV_ERR_CUDA = 3,          /* a CUDA runtime call failed (message has details) */
     LBV_ERR_WORKSPACE = 4,     /* caller buffer too small                           */
-    LBV_ERR_TIMEOUT = 5        /* a bounded device wait gave up                     */
+    LBV_ERR_TIMEOUT = 5,       /* a bounded device wait gave up                     */
+    LBV_ERR_BOUNDS = 6         /* a kernel's own range check failed (an internal
+                                  error: the access was skipped, the output is wrong) */
 } lbv_status;
 
 typedef enum {
@@ -234,8 +236,11 @@ LBV_API lbv_status lbv_plan_measured(const lbv_plan* plan, int M, float* fewrow_
 
 /* Reads (and clears) the plan's device status word: LBV_ERR_TIMEOUT if a
  * verify kernel of this plan gave up a bounded wait for its weight copies
- * since the last check (its output is then incomplete), else LBV_OK.
- * Synchronises with the device. */
+ * since the last check (its output is then incomplete), LBV_ERR_BOUNDS if a
+ * kernel found one of its copy or buffer ranges outside its bounds and skipped
+ * the access (the checked build's range checks, and the e4m3 kernel's
+ * shared-memory carve-up check in every build), else LBV_OK.  Synchronises
+ * with the device. */
 LBV_API lbv_status lbv_plan_device_status(const lbv_plan* plan);
 
 /*
@@ -465,6 +470,20 @@ LBV_API const char* lbv_last_error(void);
 
 /* Library version string. */
 LBV_API const char* lbv_version(void);
+
+/*
+ * 1 in the checked build (liblbv_checked.so, compiled with LBV_CHECKED), 0 in
+ * the release library.  The checked build's kernels test, before each access
+ * they cannot prove in range by construction, that it lies inside its buffer:
+ * the shared-memory carve-up against the launch's dynamic shared memory, every
+ * weight copy against the packed matrix and its ring slot, the X slice against
+ * K and its row buffer, a stage's chunks against the staged slice, the K split's
+ * partial slots against their buffer.  A failed test sets the status word's
+ * bounds bit (LBV_ERR_BOUNDS from lbv_plan_device_status) and skips the access;
+ * the kernel still ends, and its output is then wrong.  It stands in for a
+ * memory checker where none can run.
+ */
+LBV_API int lbv_checked_build(void);
 
 #ifdef __cplusplus
 }

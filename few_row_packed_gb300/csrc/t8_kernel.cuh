@@ -341,6 +341,14 @@ struct T8Kernel {
     {
         const size_t rec = ((size_t)tile * (size_t)p.ngroups + (size_t)g) * 4;
         const uint32_t bytes = (uint32_t)ngr * 4 * REC;
+#ifdef LBV_CHECKED
+        // checked build: the stage lies inside the packed matrix (else no copy:
+        // its waiters give up and the status records both)
+        if (tile < 0 || tile >= p.ntiles || g < 0 || ngr < 1 || g + ngr > p.ngroups) {
+            atomicOr(p.err, 2u);
+            return;
+        }
+#endif
         mbar_expect_tx(bar, bytes);
         bulk_g2s(dst, p.W + rec * REC, bytes, bar);
     }
@@ -352,6 +360,14 @@ struct T8Kernel {
                                                    uint32_t xbar, int k0, int ks)
     {
         const uint16_t* X = reinterpret_cast<const uint16_t*>(p.X);
+#ifdef LBV_CHECKED
+        // checked build: the slice lies inside K and fits the row buffer
+        if (k0 < 0 || ks < 0 || k0 + ks > p.K || ks * 2 > RS || p.M < 1 || p.M > 8) {
+            if (threadIdx.x == 0)
+                atomicOr(p.err, 2u);
+            return false;
+        }
+#endif
         if (p.x_vec) {
             if (threadIdx.x == 0) {
                 mbar_expect_tx(xbar, (uint32_t)(p.M * ks * 2));

@@ -625,6 +625,16 @@ struct TcKernel {
         const int tile = c.t0 + w.tl + w.TL * u;
         const uint8_t* src = p.W + ((size_t)tile * p.nchunks + c.c0 + w.cw0 + cl) * G::REC;
         const int st = q % G::NST;
+#ifdef LBV_CHECKED
+        // checked build: the record lies inside the packed matrix (else no copy:
+        // its waiters give up and the status records both)
+        if (tile < 0 || tile >= p.ntiles || c.c0 + w.cw0 + cl < 0 ||
+            c.c0 + w.cw0 + cl >= p.nchunks) {
+            if (lane == 0)
+                atomicOr(p.err, 2u);
+            return;
+        }
+#endif
         if (lane == 0) {
             const uint32_t fb = bar_addr(c, wg, B_FULL + st);
             mbar_expect_tx(fb, (uint32_t)G::REC);

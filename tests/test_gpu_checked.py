@@ -4,8 +4,9 @@ and records a bounds error instead of making the access.  Run in a child
 process that loads it (LBV_LIBRARY=checked), small cases of every kernel of the
 default path must agree with the oracle and leave the plan's status clean:
 every format and dtype, ragged N and K, K splits 2..8, both warp shapes, the
-fused head with rotation and argmax, the grouped launch, and both 1-row
-kernels.  This stands in for a memory checker, which cannot run here."""
+fused head with rotation and argmax, the grouped launch, both 1-row kernels,
+and the two tcgen05 kernels over several K splits.  This stands in for a
+memory checker, which cannot run here."""
 import os
 import subprocess
 import sys
@@ -79,6 +80,37 @@ def child():
             P.device_status()
             check(Y.cpu().numpy(), M, Yref, A)
             n += 1
+
+    # the tcgen05 kernels (fp16 operands: every format; e4m3: the g128 formats),
+    # every K split whose shape fits
+    TC = [("sign1_g128", 2048, 520, 128, "f16", lbv.PLAN_TCGEN05, (1, 2, 3, 6)),
+          ("affine2", 1536, 260, 32, "f16", lbv.PLAN_TCGEN05, (1, 4)),
+          ("q4_0", 1024, 400, 32, "f16", lbv.PLAN_TCGEN05, (2, 8)),
+          ("sign1_g128", 2048, 520, 128, "f16", lbv.PLAN_TC_E4M3, (1, 2, 4, 8)),
+          ("affine2", 2048, 300, 128, "bf16", lbv.PLAN_TC_E4M3, (1, 2, 4))]
+    for fmtname, K, N, group, xd, flag, splits in TC:
+        fmt = FMT[fmtname]
+        mat = synth.Matrix("t", fmtname, K, N, group, xd)
+        parts, xb = synth.gen_matrix(mat, 6)
+        P = lbv.Plan(fmt, K, N, group, lbv.DTYPE_BY_NAME[xd], lbv.PLAN_PDL | flag)
+        Wp = dev(lbv.pack(fmt, parts, K, N, group, plan=P))
+        X = dev(xb.view(np.int16))
+        Yref, A = oracle.verify(fmt, parts, oracle.x_to_f64(xb, xd), K, N, group)
+        ran = 0
+        for s in splits:
+            try:
+                P.set_shape(0, 0, s, 0)
+            except lbv.LbvError:
+                continue
+            for M in (1, 8):
+                Y = torch.full((8, N), float(SENTINEL), dtype=torch.float32, device="cuda")
+                lbv.verify_gemm(P, X, M, Wp, Y)
+                torch.cuda.synchronize()
+                P.device_status()
+                check(Y.cpu().numpy(), M, Yref, A)
+                n += 1
+            ran += 1
+        assert ran > 0, (fmtname, flag)
 
     # fused head: rotation in the prologue, logits and argmax
     K, N = 1024, 200
